@@ -1,0 +1,422 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA mixer core on GB300.
+
+Prints one JSON line.  The headline is chunked-prefill throughput in tokens
+per second per KDA layer on the long K3-shaped workload (B=1, T=32768, H=96,
+d=128, bf16 I/O, fp32 state): one step is one kda_prefill call (pre-stage,
+recurrence, RMSNormGated epilogue, ring update) over the whole sequence, with
+inputs resident in HBM.  Alongside it:
+  decode     batched decode of 256 sessions x 32 heads (state GB/s, session*tokens/s)
+  e2e        the same prefill through the C ABI from pinned HOST buffers,
+             host->device copies and the device->host read of o inside the timed region
+  roofline   the dominant kernel's achieved HBM bandwidth vs the measured peak
+  cpu_baseline  the fp64 oracle on a bounded sample of the same workload
+
+--impl reference times the oracle (the only other implementation) as the
+reference arm.  Multi-GPU (torchrun) runs independent replicas: every rank
+processes its own copy of the workload (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import kda_synth  # noqa: E402
+
+D = 128
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------- helpers
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def source_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, src: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)[kernel]
+        if d.get("source_sha") != source_sha(src):
+            return None
+        return float(d["dram_bytes_per_launch"]) * d.get("scale", 1.0)
+    except Exception:
+        return None
+
+
+class Clocks:
+    """nvidia-smi sampler running during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            uuid = None
+            try:
+                uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+                if not uuid.startswith("GPU-"):
+                    uuid = "GPU-" + uuid
+            except Exception:
+                uuid = None
+            sel = uuid or os.environ.get("CUDA_VISIBLE_DEVICES", str(self.dev)).split(",")[self.dev]
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", sel], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def allreduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------- algorithmic bytes
+def prestage_bytes_per_token_head(io_bytes, out_bytes):
+    # reads q,k,v,z (d each) + b; writes q^,k^,v^ + gate (fp32) + beta
+    return 4 * D * io_bytes + io_bytes + 3 * D * out_bytes + 4 * D + 4
+
+
+def recurrence_bytes_per_token_head(op_bytes):
+    # reads q^,k^,v^ + gate (fp32) + beta; writes o_core (fp32)
+    return 3 * D * op_bytes + 4 * D + 4 + 4 * D
+
+
+def epilogue_bytes_per_token_head(io_bytes):
+    # reads o_core (fp32) + gout; writes o
+    return 4 * D + 2 * D * io_bytes
+
+
+def decode_bytes_per_session_head(io_bytes):
+    # S read + write (fp32), q,k,v,z,gout + b in, o out, ring read + write
+    return 2 * D * D * 4 + 5 * D * io_bytes + io_bytes + D * io_bytes + 2 * 3 * 3 * D * io_bytes
+
+
+# ------------------------------------------------------------------- arms
+def prefill_arm(args, dev, world, rank):
+    import gated_delta_rule_04_gb300 as kda
+    w = kda_synth.workload(3, device=dev)
+    H, T, W = w.H, w.total_tokens, w.H * D
+    kp = kda.make_params(w.params.conv_w, w.params.A_log, w.params.dt_bias, w.params.norm_w,
+                         io_dtype=w.io, algo=args.algo)
+    toks = list(w.tokens.fields())
+    o = torch.empty(T, W, dtype=torch.bfloat16, device=dev)
+    S_out = torch.empty(1, H, D, D, device=dev)
+    ring_out = torch.empty(1, 3, 3, W, dtype=torch.bfloat16, device=dev)
+    ws_bytes = kda.kda_prefill_workspace_bytes(kp, 1, T)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    cu = w.cu_seqlens
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        kda.kda_prefill(kp, *toks, cu, S_out=S_out, ring_out=ring_out, o=o, workspace=ws,
+                        stream=stream, stage_events=evs)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(kda.KDA_PREFILL_EVENTS)]
+              for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for evs in evsets:  # create the handles outside the timed region
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    with Clocks(dev.index or 0) as clk:
+        start.record(stream)
+        for evs in evsets:
+            step(evs)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = start.elapsed_time(end) / args.steps
+    stage_ms = [statistics.mean(evs[i].elapsed_time(evs[i + 1]) for evs in evsets) for i in range(4)]
+    ms_max = allreduce_max(ms, world)
+    ws_status = kda.kda_workspace_status(ws, stream)
+    return dict(w=w, ms=ms, ms_max=ms_max, stage_ms=stage_ms, clocks=clk.summary(), kp=kp,
+                launches=4 * args.steps, ws_status=ws_status, algo_resolved=kda.kda_prefill_algo(kp))
+
+
+def e2e_arm(args, dev, w, kp):
+    """Same prefill through the C ABI from pinned host buffers."""
+    import gated_delta_rule_04_gb300 as kda
+    H, T, W = w.H, w.total_tokens, w.H * D
+    host = [t.cpu().pin_memory() for t in w.tokens.fields()]
+    dbuf = [torch.empty_like(t, device=dev) for t in host]
+    o = torch.empty(T, W, dtype=torch.bfloat16, device=dev)
+    o_host = torch.empty(T, W, dtype=torch.bfloat16).pin_memory()
+    S_out = torch.empty(1, H, D, D, device=dev)
+    ring_out = torch.empty(1, 3, 3, W, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(kda.kda_prefill_workspace_bytes(kp, 1, T), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for d_, h_ in zip(dbuf, host):
+            d_.copy_(h_, non_blocking=True)
+        kda.kda_prefill(kp, *dbuf, w.cu_seqlens, S_out=S_out, ring_out=ring_out, o=o, workspace=ws, stream=stream)
+        o_host.copy_(o, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / args.steps
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = o_host.numel() * o_host.element_size()
+    return ms, h2d, d2h
+
+
+def decode_arm(args, dev):
+    import gated_delta_rule_04_gb300 as kda
+    w = kda_synth.workload(1, device=dev)
+    kp = kda.make_params(w.params.conv_w, w.params.A_log, w.params.dt_bias, w.params.norm_w,
+                         io_dtype=w.io, algo=args.algo)
+    # state and ring from 512 warm-up tokens per session (input for timing)
+    _, S, ring = kda.kda_prefill(kp, *w.warmup_tokens.fields(), w.warmup_cu)
+    toks = list(w.tokens.fields())
+    o = torch.empty_like(toks[0])
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        kda.kda_decode(kp, *toks, S, ring, o=o, stream=stream)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = max(args.steps, 20)
+    start.record(stream)
+    for _ in range(steps):
+        kda.kda_decode(kp, *toks, S, ring, o=o, stream=stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    n_units = w.n_seqs * w.H
+    return dict(ms=ms, sessions=w.n_seqs, H=w.H, bytes=n_units * decode_bytes_per_session_head(2) , steps=steps)
+
+
+def cpu_baseline(args, sample_heads=32, sample_tokens=16384):
+    """The fp64 oracle, as it stands, on a bounded sample of the long
+    workload: `sample_heads` heads x the first `sample_tokens` tokens."""
+    import oracle
+    from tests.kda_testlib import oracle_run  # marshalling helper only
+    w = kda_synth.workload(3, device="cuda" if torch.cuda.is_available() else "cpu")
+    heads = list(range(sample_heads))
+    sub = kda_synth.Tokens(*[t[:sample_tokens] for t in w.tokens.fields()])
+    t0 = time.perf_counter()
+    oracle_run(w.params.to("cpu"), sub, [0, sample_tokens], heads=heads)
+    dt = time.perf_counter() - t0
+    token_heads = sample_heads * sample_tokens
+    value = token_heads / w.H / dt  # full-layer tokens/s
+    return {"value": value, "unit": "tokens/s/layer", "cores": oracle.default_threads(), "kind": "oracle",
+            "sample": f"{sample_heads} of {w.H} heads x first {sample_tokens} of {w.total_tokens} tokens "
+                      f"(fp64, token by token), {dt:.2f} s wall incl. marshalling"}
+
+
+# -------------------------------------------------------------- reference
+def reference_main(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    from tests.kda_testlib import oracle_run
+    w = kda_synth.workload(3, device="cpu", lens=[2048])
+    heads = list(range(16))
+    sub_tokens = w.tokens
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle_run(w.params, sub_tokens, w.cu_seqlens, heads=heads)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    dt = statistics.mean(times)
+    value = len(heads) * w.total_tokens / w.H / dt
+    line = {
+        "impl": "reference", "metric": "KDA tokens/s/layer (chunked prefill)", "value": value,
+        "unit": "tokens/s/layer", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "K3 long prefill B=1 T=32768 H=96 d=128 bf16 inputs (oracle step: 16 heads x 2048 tokens)",
+                   "global_batch": 1, "seq_len": 32768, "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s/layer", "cores": oracle.default_threads(),
+                         "kind": "oracle", "sample": "16 of 96 heads x 2048 tokens per step"},
+        "e2e": {"value": value, "unit": "tokens/s/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--algo", default="auto", choices=["auto", "scan", "chunked"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_info()
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        reference_main(args, world, rank)
+        return
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from gated_delta_rule_04_gb300 import build as kbuild
+    kbuild.build()
+
+    hbm, tc, tc_sus, peak_kind = peaks()
+    r = prefill_arm(args, dev, world, rank)
+    w = r["w"]
+    H, T = w.H, w.total_tokens
+    value = T * world / (r["ms_max"] / 1e3)
+
+    # roofline of the dominant kernel (largest share of the step)
+    chunked = r["algo_resolved"] == "chunked"
+    names = ["prestage_kernel", "chunked_kernel" if chunked else "scan_kernel", "epilogue_kernel", "ring_update_kernel"]
+    srcs = ["kda_prestage.cu", "kda_chunk.cu" if chunked else "kda_scan.cu", "kda_epilogue.cu", "kda_prestage.cu"]
+    per_th = [prestage_bytes_per_token_head(2, 2 if chunked else 4),
+              recurrence_bytes_per_token_head(2 if chunked else 4),
+              epilogue_bytes_per_token_head(2), 0]
+    stage_ms = r["stage_ms"]
+    dom = max(range(3), key=lambda i: stage_ms[i])
+    alg_bytes = per_th[dom] * T * H
+    achieved = alg_bytes / (stage_ms[dom] / 1e3) / 1e9
+    src_path = os.path.join(ROOT, "gated_delta_rule_04_gb300", "csrc", srcs[dom])
+    roofline = {"bound": "hbm", "kernel": names[dom], "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_kind": f"{peak_kind} copy bandwidth",
+                "traffic": ncu_traffic(names[dom], src_path),
+                "algorithmic_bytes_per_launch": alg_bytes,
+                "bytes_per_token_head": per_th[dom], "ms_per_launch": stage_ms[dom],
+                "stage_ms": dict(zip(["prestage", "recurrence", "epilogue", "ring"], stage_ms))}
+
+    line = {
+        "metric": "KDA tokens/s/layer (chunked prefill)", "value": value, "unit": "tokens/s/layer",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_max"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "K3 long prefill: B=1, T=32768, H=96, d=128, bf16 I/O, fp32 state, zero initial state",
+                   "global_batch": world, "seq_len": T, "heads": H, "algo": r["algo_resolved"],
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs (4.0 GB) larger than L2 (129 MB); no flush"},
+        "roofline": roofline,
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+        "workspace_status": r["ws_status"],
+    }
+    if not args.no_decode:
+        dr = decode_arm(args, dev)
+        gbs = dr["bytes"] / (dr["ms"] / 1e3) / 1e9
+        line["decode"] = {
+            "workload": "batched decode: 256 sessions x H=32, d=128, one token each, bf16 I/O, fp32 state from 512 warm-up tokens",
+            "value": dr["sessions"] * world / (dr["ms"] / 1e3), "unit": "session*tokens/s",
+            "ms_per_step": dr["ms"], "steps": dr["steps"],
+            "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs / hbm, "peak_kind": f"{peak_kind} copy bandwidth",
+                         "traffic": ncu_traffic("decode_kernel", os.path.join(ROOT, "gated_delta_rule_04_gb300", "csrc", "kda_decode.cu")),
+                         "algorithmic_bytes_per_launch": dr["bytes"]},
+        }
+    if not args.no_e2e:
+        ms, h2d, d2h = e2e_arm(args, dev, w, r["kp"])
+        ms = allreduce_max(ms, world)
+        line["e2e"] = {"value": T * world / (ms / 1e3), "unit": "tokens/s/layer", "ms_per_step": ms,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

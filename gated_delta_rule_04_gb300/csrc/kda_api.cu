@@ -1,0 +1,293 @@
+// C ABI of the KDA mixer core: host-side validation, workspace layout and the
+// launch sequence of each entry point.  Every check happens here, before
+// anything is enqueued, so a rejected call writes nothing.
+#include <math.h>
+#include <string.h>
+
+#include <vector>
+
+#include "kda_common.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int CHUNK = 64;
+constexpr size_t WS_ALIGN = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t count_chunks(const int64_t* cu, int32_t n) {
+    int64_t c = 0;
+    for (int32_t i = 0; i < n; ++i) c += (cu[i + 1] - cu[i] + CHUNK - 1) / CHUNK;
+    return c;
+}
+
+// Which prefill algorithm a parameter set runs.
+enum class Algo { Scan, Chunked };
+
+bool chunked_available() { return chunked_kernel_built(); }
+
+kda_status resolve_algo(const kda_params* p, Algo* out) {
+    const bool bf16 = p->io_dtype == KDA_DTYPE_BF16;
+    const bool bound_ok = p->gate_lower_bound >= -5.5f;  // 16 * 5.5 = 88 < ln(FLT_MAX)
+    switch (p->algo) {
+        case KDA_ALGO_SCAN: *out = Algo::Scan; return KDA_OK;
+        case KDA_ALGO_CHUNKED:
+            if (!bf16 || !bound_ok || !chunked_available()) return KDA_ERR_UNSUPPORTED;
+            *out = Algo::Chunked;
+            return KDA_OK;
+        case KDA_ALGO_AUTO:
+            *out = (bf16 && bound_ok && chunked_available()) ? Algo::Chunked : Algo::Scan;
+            return KDA_OK;
+        default: return KDA_ERR_INVALID_ARG;
+    }
+}
+
+kda_status check_params(const kda_params* p) {
+    if (p == nullptr) return KDA_ERR_INVALID_ARG;
+    if (p->num_heads < 1 || p->num_heads > (1 << 16)) return KDA_ERR_INVALID_ARG;
+    if (p->head_dim != D || p->conv_kernel != CONV_K) return KDA_ERR_UNSUPPORTED;
+    if (p->io_dtype != KDA_DTYPE_F32 && p->io_dtype != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARG;
+    if (!(p->gate_lower_bound < 0.f) || !isfinite(p->gate_lower_bound)) return KDA_ERR_INVALID_ARG;
+    if (!(p->l2_eps >= 0.f) || !(p->norm_eps >= 0.f) || !isfinite(p->l2_eps) || !isfinite(p->norm_eps))
+        return KDA_ERR_INVALID_ARG;
+    if (!isfinite(p->q_scale)) return KDA_ERR_INVALID_ARG;
+    if (!p->conv_w || !p->A_log || !p->dt_bias || !p->norm_w) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(p->conv_w) || !aligned16(p->dt_bias) || !aligned16(p->norm_w)) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+
+float resolved_q_scale(const kda_params* p) {
+    return p->q_scale != 0.f ? p->q_scale : 1.0f / sqrtf((float)D);
+}
+
+struct WsLayout {
+    size_t status = 0, meta = 0, qh = 0, kh = 0, vh = 0, g = 0, beta = 0, ocore = 0, total = 0;
+    size_t meta_bytes = 0;
+};
+
+WsLayout layout(const kda_params* p, Algo algo, int32_t n_seqs, int64_t T, int64_t n_chunks) {
+    WsLayout L;
+    const size_t W = (size_t)p->num_heads * D;
+    const size_t op = (algo == Algo::Chunked) ? 2 : 4;  // bytes per q^/k^/v^ element
+    size_t off = 0;
+    L.status = off; off += WS_ALIGN;
+    L.meta = off;
+    L.meta_bytes = sizeof(int64_t) * (size_t)(n_seqs + 1) + sizeof(ChunkDesc) * (size_t)n_chunks;
+    off = align_up(off + L.meta_bytes, WS_ALIGN);
+    L.qh = off; off = align_up(off + op * (size_t)T * W, WS_ALIGN);
+    L.kh = off; off = align_up(off + op * (size_t)T * W, WS_ALIGN);
+    L.vh = off; off = align_up(off + op * (size_t)T * W, WS_ALIGN);
+    L.g = off; off = align_up(off + 4 * (size_t)T * W, WS_ALIGN);
+    L.beta = off; off = align_up(off + 4 * (size_t)T * p->num_heads, WS_ALIGN);
+    L.ocore = off; off = align_up(off + 4 * (size_t)T * W, WS_ALIGN);
+    L.total = off;
+    return L;
+}
+
+kda_status check_cu(const int64_t* cu, int32_t n, int64_t T) {
+    if (n < 0 || T < 0) return KDA_ERR_INVALID_ARG;
+    if (cu == nullptr) return KDA_ERR_INVALID_ARG;
+    if (cu[0] != 0 || cu[n] != T) return KDA_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n; ++i)
+        if (cu[i + 1] < cu[i]) return KDA_ERR_INVALID_ARG;
+    if (T > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;  // chunk table uses int32 token indices
+    return KDA_OK;
+}
+
+kda_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" {
+
+const char* kda_status_str(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_INVALID_ARG: return "invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case KDA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+        case KDA_ERR_CUDA: return "CUDA error";
+        case KDA_ERR_TIMEOUT: return "bounded in-kernel wait timed out";
+    }
+    return "unknown status";
+}
+
+int32_t kda_prefill_algo(const kda_params* p) {
+    if (check_params(p) != KDA_OK) return -1;
+    Algo algo;
+    if (resolve_algo(p, &algo) != KDA_OK) return -1;
+    return algo == Algo::Chunked ? KDA_ALGO_CHUNKED : KDA_ALGO_SCAN;
+}
+
+size_t kda_prefill_workspace_bytes(const kda_params* p, int32_t n_seqs, int64_t total_tokens) {
+    if (check_params(p) != KDA_OK || n_seqs < 0 || total_tokens < 0) return 0;
+    Algo algo;
+    if (resolve_algo(p, &algo) != KDA_OK) return 0;
+    if (n_seqs == 0 && total_tokens == 0) return 0;
+    // upper bound on the chunk count: every sequence may add one partial chunk
+    const int64_t n_chunks = total_tokens / CHUNK + n_seqs;
+    return layout(p, algo, n_seqs, total_tokens, n_chunks).total;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Records ev[i] (when given) on the stream; stage boundaries for profiling.
+cudaError_t mark(void* const* ev, int i, cudaStream_t s) {
+    if (ev == nullptr || ev[i] == nullptr) return cudaSuccess;
+    return cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s);
+}
+
+kda_status prefill_impl(const kda_params* p, const void* q, const void* k, const void* v,
+                        const void* z, const void* b, const void* gout,
+                        const int64_t* cu_seqlens_host, int32_t n_seqs, int64_t total_tokens,
+                        const float* S_in, float* S_out, const void* ring_in, void* ring_out,
+                        void* o, void* workspace, size_t workspace_bytes, void* stream_,
+                        void* const* ev) {
+    kda_status st = check_params(p);
+    if (st != KDA_OK) return st;
+    Algo algo;
+    st = resolve_algo(p, &algo);
+    if (st != KDA_OK) return st;
+    st = check_cu(cu_seqlens_host, n_seqs, total_tokens);
+    if (st != KDA_OK) return st;
+    if (n_seqs == 0) return KDA_OK;
+    if (total_tokens > 0) {
+        const void* tok[7] = {q, k, v, z, gout, o, nullptr};
+        for (int i = 0; i < 6; ++i)
+            if (tok[i] == nullptr || !aligned16(tok[i])) return KDA_ERR_INVALID_ARG;
+        if (b == nullptr) return KDA_ERR_INVALID_ARG;
+    }
+    if (S_out == nullptr || !aligned16(S_out) || (S_in && !aligned16(S_in))) return KDA_ERR_INVALID_ARG;
+    if ((ring_in && !aligned16(ring_in)) || (ring_out && !aligned16(ring_out))) return KDA_ERR_INVALID_ARG;
+
+    const int64_t n_chunks = count_chunks(cu_seqlens_host, n_seqs);
+    const size_t need = kda_prefill_workspace_bytes(p, n_seqs, total_tokens);
+    if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) % WS_ALIGN))
+        return KDA_ERR_WORKSPACE;
+    const WsLayout L = layout(p, algo, n_seqs, total_tokens, n_chunks);
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream_);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    const int H = p->num_heads, W = H * D;
+    const int io_bf16 = p->io_dtype == KDA_DTYPE_BF16;
+
+    // host-built metadata: cu_seqlens then the chunk table, one upload
+    std::vector<unsigned char> meta(L.meta_bytes);
+    memcpy(meta.data(), cu_seqlens_host, sizeof(int64_t) * (size_t)(n_seqs + 1));
+    ChunkDesc* cds = reinterpret_cast<ChunkDesc*>(meta.data() + sizeof(int64_t) * (size_t)(n_seqs + 1));
+    int64_t ci = 0;
+    for (int32_t n = 0; n < n_seqs; ++n)
+        for (int64_t t = cu_seqlens_host[n]; t < cu_seqlens_host[n + 1]; t += CHUNK) {
+            const int64_t len = cu_seqlens_host[n + 1] - t < CHUNK ? cu_seqlens_host[n + 1] - t : CHUNK;
+            cds[ci++] = ChunkDesc{n, (int32_t)t, (int32_t)len, (int32_t)(t - cu_seqlens_host[n])};
+        }
+    const int64_t* d_cu = reinterpret_cast<const int64_t*>(ws + L.meta);
+    const ChunkDesc* d_chunks = reinterpret_cast<const ChunkDesc*>(ws + L.meta + sizeof(int64_t) * (size_t)(n_seqs + 1));
+    // the status word reports bounded-wait timeouts of this call only
+    cudaError_t e = cudaMemsetAsync(ws + L.status, 0, WS_ALIGN, s);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    e = cudaMemcpyAsync(ws + L.meta, meta.data(), L.meta_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+
+    if (mark(ev, 0, s) != cudaSuccess) return KDA_ERR_CUDA;
+    const float qs = resolved_q_scale(p);
+    float* gbuf = reinterpret_cast<float*>(ws + L.g);
+    float* beta = reinterpret_cast<float*>(ws + L.beta);
+    float* ocore = reinterpret_cast<float*>(ws + L.ocore);
+
+    PrestageArgs pa{q, k, v, z, b, p->conv_w, p->A_log, p->dt_bias, ring_in, d_cu, d_chunks,
+                    (int32_t)n_chunks, H, p->gate_lower_bound, p->l2_eps, qs,
+                    ws + L.qh, ws + L.kh, ws + L.vh, gbuf, beta};
+    if (algo == Algo::Scan) {
+        e = launch_prestage(pa, io_bf16, /*out_bf16=*/0, /*cumsum=*/0, s);
+        if (e != cudaSuccess || mark(ev, 1, s) != cudaSuccess) return KDA_ERR_CUDA;
+        ScanArgs sa{reinterpret_cast<const float*>(ws + L.qh), reinterpret_cast<const float*>(ws + L.kh),
+                    reinterpret_cast<const float*>(ws + L.vh), gbuf, beta, S_in, S_out, ocore, d_cu,
+                    n_seqs, H};
+        e = launch_scan(sa, s);
+        if (e != cudaSuccess || mark(ev, 2, s) != cudaSuccess) return KDA_ERR_CUDA;
+    } else {
+        e = launch_prestage(pa, io_bf16, /*out_bf16=*/1, /*cumsum=*/1, s);
+        if (e != cudaSuccess || mark(ev, 1, s) != cudaSuccess) return KDA_ERR_CUDA;
+        ChunkedArgs ca{ws + L.qh, ws + L.kh, ws + L.vh, gbuf, beta, S_in, S_out, ocore, d_cu,
+                       reinterpret_cast<int32_t*>(ws + L.status), n_seqs, H};
+        e = launch_chunked(ca, s);
+        if (e != cudaSuccess || mark(ev, 2, s) != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    EpilogueArgs ea{ocore, gout, p->norm_w, o, total_tokens, H, p->norm_eps};
+    e = launch_epilogue(ea, io_bf16, s);
+    if (e != cudaSuccess || mark(ev, 3, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (ring_out) {
+        RingArgs ra{q, k, v, ring_in, ring_out, d_cu, n_seqs, W};
+        e = launch_ring_update(ra, io_bf16, s);
+        if (e != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    if (mark(ev, 4, s) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_prefill(const kda_params* p, const void* q, const void* k, const void* v,
+                       const void* z, const void* b, const void* gout,
+                       const int64_t* cu_seqlens_host, int32_t n_seqs, int64_t total_tokens,
+                       const float* S_in, float* S_out, const void* ring_in, void* ring_out,
+                       void* o, void* workspace, size_t workspace_bytes, void* stream) {
+    return prefill_impl(p, q, k, v, z, b, gout, cu_seqlens_host, n_seqs, total_tokens, S_in, S_out,
+                        ring_in, ring_out, o, workspace, workspace_bytes, stream, nullptr);
+}
+
+kda_status kda_prefill_with_events(const kda_params* p, const void* q, const void* k, const void* v,
+                                   const void* z, const void* b, const void* gout,
+                                   const int64_t* cu_seqlens_host, int32_t n_seqs,
+                                   int64_t total_tokens, const float* S_in, float* S_out,
+                                   const void* ring_in, void* ring_out, void* o, void* workspace,
+                                   size_t workspace_bytes, void* stream, void* const* stage_events) {
+    return prefill_impl(p, q, k, v, z, b, gout, cu_seqlens_host, n_seqs, total_tokens, S_in, S_out,
+                        ring_in, ring_out, o, workspace, workspace_bytes, stream, stage_events);
+}
+
+kda_status kda_decode(const kda_params* p, int32_t n_sessions, const void* q, const void* k,
+                      const void* v, const void* z, const void* b, const void* gout, float* S,
+                      void* ring, void* o, void* stream_) {
+    kda_status st = check_params(p);
+    if (st != KDA_OK) return st;
+    if (n_sessions < 0) return KDA_ERR_INVALID_ARG;
+    if (n_sessions == 0) return KDA_OK;
+    const void* ptrs[8] = {q, k, v, z, gout, o, S, ring};
+    for (int i = 0; i < 8; ++i)
+        if (ptrs[i] == nullptr || !aligned16(ptrs[i])) return KDA_ERR_INVALID_ARG;
+    if (b == nullptr) return KDA_ERR_INVALID_ARG;
+    if ((int64_t)n_sessions * p->num_heads > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    DecodeArgs da{q, k, v, z, b, gout, p->conv_w, p->A_log, p->dt_bias, p->norm_w, S, ring, o,
+                  n_sessions, p->num_heads, p->gate_lower_bound, p->l2_eps, p->norm_eps,
+                  resolved_q_scale(p)};
+    return cuda_status(launch_decode(da, p->io_dtype == KDA_DTYPE_BF16, static_cast<cudaStream_t>(stream_)));
+}
+
+kda_status kda_workspace_status(void* workspace, void* stream_) {
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) % WS_ALIGN)) return KDA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream_);
+    int32_t word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (word == ERR_NONE) return KDA_OK;
+    const int32_t zero = 0;
+    if (cudaMemcpyAsync(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return word == ERR_TIMEOUT ? KDA_ERR_TIMEOUT : KDA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,162 @@
+// Device helpers shared by the KDA kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+constexpr int D = 128;      // head_dim (the only width instantiated)
+constexpr int CONV_K = 4;   // short conv kernel size
+constexpr int RING = 3;     // conv ring slots = CONV_K - 1
+
+// Error words written to the workspace status slot by bounded waits.
+constexpr int32_t ERR_NONE = 0;
+constexpr int32_t ERR_TIMEOUT = 1;
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
+
+// ---- 8-channel vector I/O for fp32 and bf16 token tensors ------------------
+template <typename T> struct Vec8;
+
+template <> struct Vec8<float> {
+    static __device__ __forceinline__ void load(const float* p, float (&x)[8]) {
+        float4 a = __ldg(reinterpret_cast<const float4*>(p));
+        float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
+    static __device__ __forceinline__ void store(float* p, const float (&x)[8]) {
+        reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
+        reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
+    }
+};
+
+template <> struct Vec8<__nv_bfloat16> {
+    static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&x)[8]) {
+        uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 f = __bfloat1622float2(h[i]);
+            x[2 * i] = f.x; x[2 * i + 1] = f.y;
+        }
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&x)[8]) {
+        uint4 u;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+        *reinterpret_cast<uint4*>(p) = u;
+    }
+};
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Sum over the 16 lanes of a half warp (lanes 0-15 and 16-31 reduce apart).
+__device__ __forceinline__ float halfwarp_sum(float v) {
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// One unit of prefill work: `len` tokens of sequence `seq` starting at the
+// global token index `t0`; `pos` is t0's index inside its sequence.
+struct ChunkDesc {
+    int32_t seq;
+    int32_t t0;
+    int32_t len;
+    int32_t pos;
+};
+
+}  // namespace kda
+
+// ---- launch wrappers (defined in the per-kernel .cu files) -----------------
+namespace kda {
+
+struct PrestageArgs {
+    const void *q, *k, *v, *z, *b;
+    const float *conv_w, *A_log, *dt_bias;
+    const void* ring_in;
+    const int64_t* cu;        // device [n+1]
+    const ChunkDesc* chunks;  // device [n_chunks]
+    int32_t n_chunks, H;
+    float lb, l2_eps, q_scale;
+    void *qh, *kh, *vh;       // outputs, bf16 or fp32
+    float *gbuf, *beta;       // gate (raw g, or chunk-local cumulative sum) and beta
+};
+
+cudaError_t launch_prestage(const PrestageArgs& a, int io_bf16, int out_bf16, int cumsum,
+                            cudaStream_t s);
+
+struct RingArgs {
+    const void *q, *k, *v;
+    const void* ring_in;
+    void* ring_out;
+    const int64_t* cu;
+    int32_t n_seqs, W;
+};
+cudaError_t launch_ring_update(const RingArgs& a, int io_bf16, cudaStream_t s);
+
+struct ScanArgs {
+    const float *qh, *kh, *vh, *g, *beta;
+    const float* S_in;
+    float* S_out;
+    float* o_core;
+    const int64_t* cu;
+    int32_t n_seqs, H;
+};
+cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
+
+struct EpilogueArgs {
+    const float* o_core;
+    const void* gout;
+    const float* norm_w;
+    void* o;
+    int64_t T;
+    int32_t H;
+    float eps;
+};
+cudaError_t launch_epilogue(const EpilogueArgs& a, int io_bf16, cudaStream_t s);
+
+struct ChunkedArgs {
+    const void *qh, *kh, *vh;  // bf16 [T][H*128]
+    const float* gcum;         // chunk-local inclusive cumulative gate [T][H*128]
+    const float* beta;         // [T][H]
+    const float* S_in;
+    float* S_out;
+    float* o_core;             // fp32 [T][H*128]
+    const int64_t* cu;
+    int32_t* status;           // workspace error word
+    int32_t n_seqs, H;
+};
+bool chunked_kernel_built();
+cudaError_t launch_chunked(const ChunkedArgs& a, cudaStream_t s);
+
+struct DecodeArgs {
+    const void *q, *k, *v, *z, *b, *gout;
+    const float *conv_w, *A_log, *dt_bias, *norm_w;
+    float* S;
+    void* ring;
+    void* o;
+    int32_t n, H;
+    float lb, l2_eps, norm_eps, q_scale;
+};
+cudaError_t launch_decode(const DecodeArgs& a, int io_bf16, cudaStream_t s);
+
+}  // namespace kda

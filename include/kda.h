@@ -1,0 +1,163 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention (KDA) mixer core.
+ *
+ * What the library computes, per sequence n, head h and token t (channel
+ * c = h*128 + i, i < 128):
+ *
+ *   1. short causal conv + SiLU on each of the planes q, k, v
+ *        x~[c] = sum_{j<4} conv_w[p][c][j] * x_p[t-3+j][c],  a = x~ * sigmoid(x~)
+ *      inputs before the sequence start come from the conv ring (slot 0
+ *      oldest); "Kimi Delta Attention (KDA) -- analysis & C kernel plan",
+ *      section "The KDA layer, precisely" (q = SiLU(ShortConv_4(W_q x)) ...);
+ *      "ferrox-models 0.8.0, module kda" (depthwise causal Conv1d, padding
+ *      kernel_size-1, no bias; KdaState keeps the raw projected inputs).
+ *   2. q^ = a_q / sqrt(sum a_q^2 + l2_eps) * q_scale,  k^ = a_k / sqrt(sum a_k^2 + l2_eps),
+ *      v^ = a_v  ("ferrox-models 0.8.0, module kda": L2-normalise q and k with
+ *      eps 1e-6, then scale q by head_dim^-0.5).
+ *   3. g[c] = gate_lower_bound * sigmoid(exp(A_log[h]) * (z[t][c] + dt_bias[c]))
+ *      ("Kimi K3 - Retention gate - OpenModelAtlas", gate formula and the
+ *      gate.py excerpt naive_kda_lowerbound_gate);  beta = sigmoid(b[t][h]).
+ *   4. S' = Diag(exp(g)) S;  S = S' + beta k^ (v^ - S'^T k^)^T;  o_core = S^T q^
+ *      ("Kimi Delta Attention (KDA) -- analysis & C kernel plan", section
+ *      "Recurrence"); S is 128 x 128 fp32 per (sequence, head), rows = key.
+ *   5. o = o_core / sqrt(mean_i o_core^2 + norm_eps) * norm_w[i] * sigmoid(gout[t][c])
+ *      (same page, section "The KDA layer, precisely": RMSNormGated with a
+ *      sigmoid gate; "ferrox-models 0.8.0, module kda", fact 2).
+ *
+ * Conventions shared by every entry point
+ *   - The caller owns every buffer.  The library allocates no device memory,
+ *     holds no global state and never synchronises: all work is enqueued on
+ *     `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *   - Every pointer marked "device" must be a device (or managed) address
+ *     aligned to 16 bytes, except b which needs only element alignment.
+ *   - Token tensors are token-major: element (t, c) at t*(H*128) + c.
+ *   - Argument errors are detected on the host, before anything is enqueued,
+ *     and returned as a status; nothing is written in that case.  Launch
+ *     errors are reported as KDA_ERR_CUDA; asynchronous faults surface at the
+ *     caller's next synchronisation.  No kernel traps or asserts.
+ *   - Results are deterministic: repeated calls on the same inputs give the
+ *     same bytes (no atomics in any reduction).
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, bad cu_seqlens */
+    KDA_ERR_UNSUPPORTED = 2, /* head_dim != 128, conv_kernel != 4, algo/bound mismatch */
+    KDA_ERR_WORKSPACE = 3,   /* workspace missing, too small or misaligned */
+    KDA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+    KDA_ERR_TIMEOUT = 5      /* a bounded in-kernel wait gave up (read via kda_workspace_status) */
+} kda_status;
+
+typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
+
+/* Prefill algorithm.  AUTO picks CHUNKED for bf16 I/O with a gate bound
+ * >= -5.5 (the tensor-core form needs every 16-token rescaling factor below
+ * e^88) and SCAN otherwise.  SCAN is the fp32 sequential recurrence. */
+typedef enum { KDA_ALGO_AUTO = 0, KDA_ALGO_SCAN = 1, KDA_ALGO_CHUNKED = 2 } kda_algo;
+
+typedef struct {
+    int32_t num_heads;      /* H >= 1 */
+    int32_t head_dim;       /* must be 128 */
+    int32_t conv_kernel;    /* must be 4 */
+    int32_t io_dtype;       /* kda_dtype of q,k,v,z,b,gout,o and the ring */
+    int32_t algo;           /* kda_algo, prefill only */
+    float gate_lower_bound; /* lb < 0, -5 for Kimi K3 */
+    float l2_eps;           /* 1e-6 */
+    float norm_eps;         /* RMSNorm eps, 1e-5 */
+    float q_scale;          /* 0 selects head_dim^-0.5 */
+    const float* conv_w;    /* device [3][H*128][4] fp32, planes q,k,v; tap 3 = current token */
+    const float* A_log;     /* device [H] fp32 */
+    const float* dt_bias;   /* device [H*128] fp32 */
+    const float* norm_w;    /* device [128] fp32, shared by all heads */
+} kda_params;
+
+/* The prefill algorithm (KDA_ALGO_SCAN or KDA_ALGO_CHUNKED) that kda_prefill
+ * runs for these parameters, or -1 when it would reject them. */
+int32_t kda_prefill_algo(const kda_params* p);
+
+/* Bytes of device workspace kda_prefill needs for this problem (0 when
+ * total_tokens == 0 and n_seqs == 0).  Returns 0 as well for arguments
+ * kda_prefill would reject. */
+size_t kda_prefill_workspace_bytes(const kda_params* p, int32_t n_seqs, int64_t total_tokens);
+
+/*
+ * Stateful varlen prefill: steps 1-5 over n_seqs packed sequences.
+ *   q,k,v,z,gout : device [total_tokens][H*128] io_dtype, raw projections
+ *                  (z = decay-gate logits, gout = output-gate logits)
+ *   b            : device [total_tokens][H] io_dtype, beta logits
+ *   cu_seqlens_host : HOST [n_seqs+1] int64, cu[0] = 0, non-decreasing,
+ *                  cu[n_seqs] = total_tokens; sequence n is tokens [cu[n], cu[n+1])
+ *   S_in         : device [n_seqs][H][128][128] fp32 initial state or NULL (zero)
+ *   S_out        : device, same shape, final state; may equal S_in
+ *   ring_in      : device [n_seqs][3 planes q,k,v][3 slots][H*128] io_dtype or
+ *                  NULL (zero); slot 0 is the oldest raw input
+ *   ring_out     : device, same shape, the last three raw inputs of each
+ *                  sequence (older slots carried from ring_in when the
+ *                  sequence is shorter than three); may equal ring_in; may be
+ *                  NULL to skip
+ *   o            : device [total_tokens][H*128] io_dtype
+ *   workspace    : device, >= kda_prefill_workspace_bytes(), 256-byte aligned;
+ *                  owned by the caller, reused freely between calls that do
+ *                  not overlap on the GPU
+ * Zero-length sequences copy their state (and ring) through unchanged.
+ */
+kda_status kda_prefill(const kda_params* p,
+                       const void* q, const void* k, const void* v, const void* z,
+                       const void* b, const void* gout,
+                       const int64_t* cu_seqlens_host, int32_t n_seqs, int64_t total_tokens,
+                       const float* S_in, float* S_out,
+                       const void* ring_in, void* ring_out,
+                       void* o, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Same as kda_prefill, and records caller-created CUDA events on `stream` at
+ * the stage boundaries, for profiling: stage_events[0] before the pre-stage,
+ * [1] after the pre-stage (conv, norms, gate, beta), [2] after the
+ * recurrence (chunked or scan), [3] after the RMSNormGated epilogue, [4]
+ * after the conv-ring update.  stage_events holds KDA_PREFILL_EVENTS
+ * cudaEvent_t handles (any may be NULL to skip it) or is NULL. */
+#define KDA_PREFILL_EVENTS 5
+kda_status kda_prefill_with_events(const kda_params* p,
+                                   const void* q, const void* k, const void* v, const void* z,
+                                   const void* b, const void* gout,
+                                   const int64_t* cu_seqlens_host, int32_t n_seqs,
+                                   int64_t total_tokens, const float* S_in, float* S_out,
+                                   const void* ring_in, void* ring_out, void* o, void* workspace,
+                                   size_t workspace_bytes, void* stream, void* const* stage_events);
+
+/*
+ * Batched one-token decode for n_sessions independent sessions (one token
+ * each): steps 1-5 with the state and ring updated in place.
+ *   q,k,v,z,gout : device [n_sessions][H*128] io_dtype
+ *   b            : device [n_sessions][H] io_dtype
+ *   S            : device [n_sessions][H][128][128] fp32, read and overwritten
+ *   ring         : device [n_sessions][3][3][H*128] io_dtype, rolled in place
+ *   o            : device [n_sessions][H*128] io_dtype
+ * Equal, up to rounding, to kda_prefill with one token per sequence.
+ */
+kda_status kda_decode(const kda_params* p, int32_t n_sessions,
+                      const void* q, const void* k, const void* v, const void* z,
+                      const void* b, const void* gout,
+                      float* S, void* ring, void* o, void* stream);
+
+/* Synchronises `stream` and reads the error word the prefill kernels keep in
+ * `workspace`: KDA_OK, or KDA_ERR_TIMEOUT when a bounded in-kernel wait gave
+ * up during an earlier call on that workspace (the word is then cleared). */
+kda_status kda_workspace_status(void* workspace, void* stream);
+
+/* Static string naming a status. */
+const char* kda_status_str(kda_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,74 @@
+"""Shared helpers of the parity tests: run the CUDA path through the C ABI
+and the fp64 oracle on the same seeded inputs, and compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import kda_synth
+import oracle
+
+TOL_F32 = dict(rel=1e-4, maxabs=None)
+TOL_BF16 = dict(rel=2e-2, maxabs=5e-2)
+
+
+def tol_for(io: str):
+    return TOL_F32 if io == "f32" else TOL_BF16
+
+
+def rel_l2(got, want) -> float:
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    den = np.linalg.norm(want)
+    return float(np.linalg.norm(got - want) / (den if den > 0 else 1.0))
+
+
+def assert_close(name, got, want, tol):
+    got = got.double().cpu().numpy() if hasattr(got, "cpu") else np.asarray(got)
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    r = rel_l2(got, want)
+    assert r <= tol["rel"], f"{name}: rel-L2 {r:.3e} > {tol['rel']}"
+    if tol.get("maxabs") is not None:
+        m = float(np.max(np.abs(got - want))) if got.size else 0.0
+        assert m <= tol["maxabs"], f"{name}: max-abs {m:.3e} > {tol['maxabs']}"
+    return r
+
+
+def oracle_params(p: kda_synth.Params) -> oracle.Params:
+    return oracle.Params(p.num_heads, p.head_dim, p.conv_w.double().cpu().numpy(),
+                         p.A_log.double().cpu().numpy(), p.dt_bias.double().cpu().numpy(),
+                         p.norm_w.double().cpu().numpy(), p.gate_lower_bound, p.l2_eps, p.norm_eps,
+                         p.q_scale)
+
+
+def kda_params(p: kda_synth.Params, io: str, algo: str = "auto", device="cuda"):
+    import gated_delta_rule_04_gb300 as kda
+    return kda.make_params(p.conv_w.to(device), p.A_log.to(device), p.dt_bias.to(device),
+                           p.norm_w.to(device), io_dtype=io, algo=algo,
+                           gate_lower_bound=p.gate_lower_bound, l2_eps=p.l2_eps,
+                           norm_eps=p.norm_eps, q_scale=p.q_scale)
+
+
+def to_np(t):
+    return None if t is None else t.double().cpu().numpy()
+
+
+def oracle_run(p: kda_synth.Params, tokens: kda_synth.Tokens, cu, S_in=None, ring_in=None,
+               heads=None, intermediates=False):
+    """Oracle on all heads, or on the subset ``heads`` (heads are independent).
+    S_in / ring_in are full-width tensors (or None)."""
+    if heads is not None:
+        p = p.head_slice(heads)
+        tokens = tokens.head_slice(heads)
+        idx = torch.tensor(heads, dtype=torch.long)
+        if S_in is not None:
+            S_in = S_in[:, idx.to(S_in.device)]
+        if ring_in is not None:
+            ch = (idx[:, None] * 128 + torch.arange(128)[None, :]).reshape(-1).to(ring_in.device)
+            ring_in = ring_in[..., ch]
+    return oracle.mixer(oracle_params(p), cu, *[to_np(t) for t in tokens.fields()],
+                        S_in=to_np(S_in), ring_in=to_np(ring_in), intermediates=intermediates)
+
+
+def head_cols(heads):
+    return torch.tensor([h * 128 + i for h in heads for i in range(128)], dtype=torch.long)

@@ -1,0 +1,159 @@
+"""The C ABI on the host: the library loads without a GPU, exports every
+function include/kda.h declares, and rejects bad arguments before it
+enqueues anything (every case here fails validation, so no kernel runs)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_delta_rule_04_gb300 as kda
+from gated_delta_rule_04_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+FAKE = 0x10000  # aligned non-null address; never dereferenced on these paths
+
+
+@pytest.fixture(scope="module")
+def L():
+    kbuild.build()
+    return kda.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert {"kda_prefill", "kda_decode", "kda_prefill_workspace_bytes", "kda_status_str",
+            "kda_workspace_status"} <= set(names)
+    for name in names:
+        assert hasattr(L, name), f"libkda.so does not export {name}"
+
+
+def test_status_strings(L):
+    for s in range(6):
+        assert kda.kda_status_str(s)
+    assert kda.kda_status_str(99) == "unknown status"
+
+
+def params(**kw):
+    d = dict(num_heads=2, head_dim=128, conv_kernel=4, io_dtype=kda.KDA_DTYPE_BF16,
+             algo=kda.KDA_ALGO_AUTO, gate_lower_bound=-5.0, l2_eps=1e-6, norm_eps=1e-5, q_scale=0.0,
+             conv_w=FAKE, A_log=FAKE, dt_bias=FAKE, norm_w=FAKE)
+    d.update(kw)
+    return kda.kda_params(**d)
+
+
+def prefill(L, p, cu, T=None, ws_bytes=1 << 40, ws=FAKE, **ptrs):
+    arr = (ctypes.c_int64 * len(cu))(*cu)
+    n = len(cu) - 1
+    T = cu[-1] if T is None else T
+    a = dict(q=FAKE, k=FAKE, v=FAKE, z=FAKE, b=FAKE, gout=FAKE, S_in=None, S_out=FAKE,
+             ring_in=None, ring_out=FAKE, o=FAKE)
+    a.update(ptrs)
+    return L.kda_prefill(ctypes.byref(p), a["q"], a["k"], a["v"], a["z"], a["b"], a["gout"], arr, n, T,
+                         a["S_in"], a["S_out"], a["ring_in"], a["ring_out"], a["o"], ws, ws_bytes, None)
+
+
+def test_algo_query(L):
+    assert L.kda_prefill_algo(ctypes.byref(params(algo=kda.KDA_ALGO_SCAN))) == kda.KDA_ALGO_SCAN
+    assert L.kda_prefill_algo(ctypes.byref(params(io_dtype=kda.KDA_DTYPE_F32))) == kda.KDA_ALGO_SCAN
+    assert L.kda_prefill_algo(ctypes.byref(params(head_dim=64))) == -1
+    assert L.kda_prefill_algo(None) == -1
+
+
+def test_workspace_query(L):
+    p = params()
+    small = L.kda_prefill_workspace_bytes(ctypes.byref(p), 1, 64)
+    big = L.kda_prefill_workspace_bytes(ctypes.byref(p), 1, 64 * 1000)
+    assert 0 < small < big
+    assert L.kda_prefill_workspace_bytes(ctypes.byref(p), 0, 0) == 0
+    assert L.kda_prefill_workspace_bytes(None, 1, 64) == 0
+    assert L.kda_prefill_workspace_bytes(ctypes.byref(params(head_dim=64)), 1, 64) == 0
+    assert L.kda_prefill_workspace_bytes(ctypes.byref(p), -1, 64) == 0
+
+
+@pytest.mark.parametrize("kw, want", [
+    (dict(head_dim=64), kda.KDA_ERR_UNSUPPORTED),
+    (dict(conv_kernel=3), kda.KDA_ERR_UNSUPPORTED),
+    (dict(num_heads=0), kda.KDA_ERR_INVALID_ARG),
+    (dict(io_dtype=7), kda.KDA_ERR_INVALID_ARG),
+    (dict(algo=9), kda.KDA_ERR_INVALID_ARG),
+    (dict(gate_lower_bound=0.5), kda.KDA_ERR_INVALID_ARG),
+    (dict(gate_lower_bound=float("nan")), kda.KDA_ERR_INVALID_ARG),
+    (dict(l2_eps=-1.0), kda.KDA_ERR_INVALID_ARG),
+    (dict(conv_w=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(dt_bias=FAKE + 4), kda.KDA_ERR_INVALID_ARG),
+    (dict(algo=kda.KDA_ALGO_CHUNKED, io_dtype=kda.KDA_DTYPE_F32), kda.KDA_ERR_UNSUPPORTED),
+    (dict(algo=kda.KDA_ALGO_CHUNKED, gate_lower_bound=-8.0), kda.KDA_ERR_UNSUPPORTED),
+])
+def test_bad_params(L, kw, want):
+    assert prefill(L, params(**kw), [0, 64]) == want
+
+
+@pytest.mark.parametrize("cu, T", [
+    ([1, 64], 64),        # cu[0] != 0
+    ([0, 64, 32], 32),    # decreasing
+    ([0, 64], 65),        # cu[n] != total
+    ([0, 10], -1),
+])
+def test_bad_cu_seqlens(L, cu, T):
+    assert prefill(L, params(), cu, T=T) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_null_cu_seqlens(L):
+    p = params()
+    assert L.kda_prefill(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 64, None,
+                         FAKE, None, FAKE, FAKE, FAKE, 1 << 40, None) == kda.KDA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name", ["q", "k", "v", "z", "gout", "o", "b", "S_out"])
+def test_null_token_pointers(L, name):
+    assert prefill(L, params(), [0, 64], **{name: None}) == kda.KDA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name", ["q", "o", "S_out", "S_in", "ring_in", "ring_out"])
+def test_misaligned_pointers(L, name):
+    assert prefill(L, params(), [0, 64], **{name: FAKE + 8}) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_workspace_errors(L):
+    p = params()
+    need = L.kda_prefill_workspace_bytes(ctypes.byref(p), 1, 64)
+    assert prefill(L, p, [0, 64], ws_bytes=need - 1) == kda.KDA_ERR_WORKSPACE
+    assert prefill(L, p, [0, 64], ws=None) == kda.KDA_ERR_WORKSPACE
+    assert prefill(L, p, [0, 64], ws=FAKE + 16) == kda.KDA_ERR_WORKSPACE
+
+
+def test_empty_batch_is_a_no_op(L):
+    assert prefill(L, params(), [0], T=0) == kda.KDA_OK
+
+
+def test_decode_validation(L):
+    p = params()
+    f = FAKE
+    assert L.kda_decode(ctypes.byref(p), 0, f, f, f, f, f, f, f, f, f, None) == kda.KDA_OK
+    assert L.kda_decode(ctypes.byref(p), -1, f, f, f, f, f, f, f, f, f, None) == kda.KDA_ERR_INVALID_ARG
+    assert L.kda_decode(ctypes.byref(p), 4, f, f, f, f, f, f, None, f, f, None) == kda.KDA_ERR_INVALID_ARG
+    assert L.kda_decode(ctypes.byref(p), 4, f, f, f, f, None, f, f, f, f, None) == kda.KDA_ERR_INVALID_ARG
+    assert L.kda_decode(ctypes.byref(p), 4, f + 2, f, f, f, f, f, f, f, f, None) == kda.KDA_ERR_INVALID_ARG
+    bad = params(head_dim=96)
+    assert L.kda_decode(ctypes.byref(bad), 4, f, f, f, f, f, f, f, f, f, None) == kda.KDA_ERR_UNSUPPORTED
+
+
+def test_workspace_status_rejects_bad_pointer(L):
+    assert L.kda_workspace_status(None, None) == kda.KDA_ERR_WORKSPACE
+    assert L.kda_workspace_status(FAKE + 16, None) == kda.KDA_ERR_WORKSPACE
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(kda, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(kda, "_lib", None)
+    with pytest.raises(kda.KdaLibraryMissing):
+        kda.lib()
