@@ -6,7 +6,10 @@
 
 #include <vector>
 
-#include "kda_common.cuh"
+#include <algorithm>
+#include <numeric>
+
+#include "kda_chunk_layout.cuh"
 
 namespace kda {
 namespace {
@@ -63,19 +66,24 @@ float resolved_q_scale(const kda_params* p) {
     return p->q_scale != 0.f ? p->q_scale : 1.0f / sqrtf((float)D);
 }
 
+// Workspace regions.  meta = cu_seqlens (int64 [n+1]) | first chunk of each
+// sequence (int64 [n+1]) | sequence order (int32 [n], padded) | chunk table.
 struct WsLayout {
-    size_t status = 0, meta = 0, qh = 0, kh = 0, vh = 0, g = 0, beta = 0, ocore = 0, total = 0;
-    size_t meta_bytes = 0;
+    size_t status = 0, meta = 0, qh = 0, kh = 0, vh = 0, g = 0, beta = 0, ocore = 0, rec = 0, total = 0;
+    size_t meta_bytes = 0, off_chunk_off = 0, off_order = 0, off_chunks = 0;
 };
 
 WsLayout layout(const kda_params* p, Algo algo, int32_t n_seqs, int64_t T, int64_t n_chunks) {
     WsLayout L;
     const size_t W = (size_t)p->num_heads * D;
-    const size_t op = (algo == Algo::Chunked) ? 2 : 4;  // bytes per q^/k^/v^ element
+    const size_t op = (algo == Algo::Chunked) ? 2 : 4;  // q^/k^/v^: fp16 (chunked) or fp32 (scan)
     size_t off = 0;
     L.status = off; off += WS_ALIGN;
     L.meta = off;
-    L.meta_bytes = sizeof(int64_t) * (size_t)(n_seqs + 1) + sizeof(ChunkDesc) * (size_t)n_chunks;
+    L.off_chunk_off = sizeof(int64_t) * (size_t)(n_seqs + 1);
+    L.off_order = L.off_chunk_off + sizeof(int64_t) * (size_t)(n_seqs + 1);
+    L.off_chunks = align_up(L.off_order + sizeof(int32_t) * (size_t)n_seqs, 16);
+    L.meta_bytes = L.off_chunks + sizeof(ChunkDesc) * (size_t)n_chunks;
     off = align_up(off + L.meta_bytes, WS_ALIGN);
     L.qh = off; off = align_up(off + op * (size_t)T * W, WS_ALIGN);
     L.kh = off; off = align_up(off + op * (size_t)T * W, WS_ALIGN);
@@ -83,6 +91,8 @@ WsLayout layout(const kda_params* p, Algo algo, int32_t n_seqs, int64_t T, int64
     L.g = off; off = align_up(off + 4 * (size_t)T * W, WS_ALIGN);
     L.beta = off; off = align_up(off + 4 * (size_t)T * p->num_heads, WS_ALIGN);
     L.ocore = off; off = align_up(off + 4 * (size_t)T * W, WS_ALIGN);
+    L.rec = off;
+    if (algo == Algo::Chunked) off = align_up(off + (size_t)REC_BYTES * (size_t)n_chunks * p->num_heads, WS_ALIGN);
     L.total = off;
     return L;
 }
@@ -179,18 +189,30 @@ kda_status prefill_impl(const kda_params* p, const void* q, const void* k, const
     const int H = p->num_heads, W = H * D;
     const int io_bf16 = p->io_dtype == KDA_DTYPE_BF16;
 
-    // host-built metadata: cu_seqlens then the chunk table, one upload
-    std::vector<unsigned char> meta(L.meta_bytes);
+    // host-built metadata, one upload
+    std::vector<unsigned char> meta(L.meta_bytes, 0);
     memcpy(meta.data(), cu_seqlens_host, sizeof(int64_t) * (size_t)(n_seqs + 1));
-    ChunkDesc* cds = reinterpret_cast<ChunkDesc*>(meta.data() + sizeof(int64_t) * (size_t)(n_seqs + 1));
+    int64_t* coff = reinterpret_cast<int64_t*>(meta.data() + L.off_chunk_off);
+    int32_t* order = reinterpret_cast<int32_t*>(meta.data() + L.off_order);
+    ChunkDesc* cds = reinterpret_cast<ChunkDesc*>(meta.data() + L.off_chunks);
     int64_t ci = 0;
-    for (int32_t n = 0; n < n_seqs; ++n)
+    for (int32_t n = 0; n < n_seqs; ++n) {
+        coff[n] = ci;
         for (int64_t t = cu_seqlens_host[n]; t < cu_seqlens_host[n + 1]; t += CHUNK) {
             const int64_t len = cu_seqlens_host[n + 1] - t < CHUNK ? cu_seqlens_host[n + 1] - t : CHUNK;
             cds[ci++] = ChunkDesc{n, (int32_t)t, (int32_t)len, (int32_t)(t - cu_seqlens_host[n])};
         }
+    }
+    coff[n_seqs] = ci;
+    // longest sequences first, so the sequential chunk walks start early
+    std::iota(order, order + n_seqs, 0);
+    std::stable_sort(order, order + n_seqs, [&](int32_t x, int32_t y) {
+        return cu_seqlens_host[x + 1] - cu_seqlens_host[x] > cu_seqlens_host[y + 1] - cu_seqlens_host[y];
+    });
     const int64_t* d_cu = reinterpret_cast<const int64_t*>(ws + L.meta);
-    const ChunkDesc* d_chunks = reinterpret_cast<const ChunkDesc*>(ws + L.meta + sizeof(int64_t) * (size_t)(n_seqs + 1));
+    const int64_t* d_coff = reinterpret_cast<const int64_t*>(ws + L.meta + L.off_chunk_off);
+    const int32_t* d_order = reinterpret_cast<const int32_t*>(ws + L.meta + L.off_order);
+    const ChunkDesc* d_chunks = reinterpret_cast<const ChunkDesc*>(ws + L.meta + L.off_chunks);
     // the status word reports bounded-wait timeouts of this call only
     cudaError_t e = cudaMemsetAsync(ws + L.status, 0, WS_ALIGN, s);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
@@ -207,7 +229,7 @@ kda_status prefill_impl(const kda_params* p, const void* q, const void* k, const
                     (int32_t)n_chunks, H, p->gate_lower_bound, p->l2_eps, qs,
                     ws + L.qh, ws + L.kh, ws + L.vh, gbuf, beta};
     if (algo == Algo::Scan) {
-        e = launch_prestage(pa, io_bf16, /*out_bf16=*/0, /*cumsum=*/0, s);
+        e = launch_prestage(pa, io_bf16, /*out_fp16=*/0, /*cumsum=*/0, s);
         if (e != cudaSuccess || mark(ev, 1, s) != cudaSuccess) return KDA_ERR_CUDA;
         ScanArgs sa{reinterpret_cast<const float*>(ws + L.qh), reinterpret_cast<const float*>(ws + L.kh),
                     reinterpret_cast<const float*>(ws + L.vh), gbuf, beta, S_in, S_out, ocore, d_cu,
@@ -215,11 +237,14 @@ kda_status prefill_impl(const kda_params* p, const void* q, const void* k, const
         e = launch_scan(sa, s);
         if (e != cudaSuccess || mark(ev, 2, s) != cudaSuccess) return KDA_ERR_CUDA;
     } else {
-        e = launch_prestage(pa, io_bf16, /*out_bf16=*/1, /*cumsum=*/1, s);
+        e = launch_prestage(pa, io_bf16, /*out_fp16=*/1, /*cumsum=*/1, s);
         if (e != cudaSuccess || mark(ev, 1, s) != cudaSuccess) return KDA_ERR_CUDA;
-        ChunkedArgs ca{ws + L.qh, ws + L.kh, ws + L.vh, gbuf, beta, S_in, S_out, ocore, d_cu,
-                       reinterpret_cast<int32_t*>(ws + L.status), n_seqs, H};
-        e = launch_chunked(ca, s);
+        PrepArgs pr{ws + L.qh, ws + L.kh, ws + L.vh, gbuf, beta, d_chunks, (int32_t)n_chunks, H, ws + L.rec};
+        e = launch_chunk_prep(pr, s);
+        if (e != cudaSuccess) return KDA_ERR_CUDA;
+        ChunkRecArgs ca{ws + L.rec, S_in, S_out, ocore, d_cu, d_coff, d_order,
+                        reinterpret_cast<int32_t*>(ws + L.status), n_seqs, H};
+        e = launch_chunk_recurrence(ca, s);
         if (e != cudaSuccess || mark(ev, 2, s) != cudaSuccess) return KDA_ERR_CUDA;
     }
     EpilogueArgs ea{ocore, gout, p->norm_w, o, total_tokens, H, p->norm_eps};

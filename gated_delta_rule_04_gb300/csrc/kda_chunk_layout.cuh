@@ -1,0 +1,59 @@
+// Layout shared by the chunk-preparation kernel (producer) and the tcgen05
+// chunk-recurrence kernel (consumer): one record per (chunk, head) holding
+// that chunk's operand tiles as the byte image of the consumer's shared
+// memory, so one bulk copy moves a whole record.
+#pragma once
+
+#include "kda_common.cuh"
+
+namespace kda {
+
+constexpr int CHUNK_T = 64;  // tokens per chunk
+
+// Record layout (bytes).  Every tile is fp16, K-major with the 128-byte
+// swizzle, and starts on a 1024-byte boundary.  fp16 rather than bf16: every
+// operand here is bounded (unit-norm keys and queries scaled by decays <= 1,
+// values of order 1-10, the UT-solve products), so the 3 extra mantissa bits
+// cut the operand rounding error 8x at the same tensor-core rate.
+constexpr int REC_W = 0;          // W     [64 tok rows][128 key]  2 panels x 64 rows x 128 B
+constexpr int REC_Q = 16384;      // Q+    [64 tok rows][128 key]  2 panels
+constexpr int REC_KT = 32768;     // Kt^T  [128 key rows][64 tok]  1 panel x 128 rows
+constexpr int REC_UT = 49152;     // U0^T  [128 val rows][64 tok]  1 panel x 128 rows
+constexpr int REC_P = 65536;      // P     [64 r rows][64 s]       1 panel x 64 rows
+constexpr int REC_DECAY = 73728;  // decay [128] fp32 = e^{G_last}
+constexpr int REC_BYTES = 74240;
+
+// Byte offset of 16-bit element (row, k) in a K-major tile with the 128-byte
+// swizzle: 64 elements of K per 128-byte row, panels of `rows` rows for each
+// further 64 elements of K, 8-row groups 1024 bytes apart.
+__host__ __device__ __forceinline__ uint32_t sw128_off(int row, int k, int rows) {
+    const int panel = k >> 6, kk = k & 63;
+    const int chunk = kk >> 3, within = kk & 7;
+    return (uint32_t)(panel * rows * 128 + row * 128 + (((chunk ^ (row & 7)) & 7) << 4) + within * 2);
+}
+
+struct PrepArgs {
+    const void *qh, *kh, *vh;  // fp16 [T][H*128]
+    const float* gcum;         // [T][H*128] chunk-local inclusive cumulative gate
+    const float* beta;         // [T][H]
+    const ChunkDesc* chunks;
+    int32_t n_chunks, H;
+    void* records;             // [n_chunks][H][REC_BYTES]
+};
+cudaError_t launch_chunk_prep(const PrepArgs& a, cudaStream_t s);
+size_t chunk_prep_smem_bytes();
+
+struct ChunkRecArgs {
+    const void* records;
+    const float* S_in;
+    float* S_out;
+    float* o_core;
+    const int64_t* cu;         // [n+1] token offsets
+    const int64_t* chunk_off;  // [n+1] first chunk of each sequence
+    const int32_t* seq_order;  // [n] sequences by decreasing length (CTA order), or NULL
+    int32_t* status;
+    int32_t n_seqs, H;
+};
+cudaError_t launch_chunk_recurrence(const ChunkRecArgs& a, cudaStream_t s);
+
+}  // namespace kda

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -54,7 +55,27 @@ template <> struct Vec8<__nv_bfloat16> {
     }
 };
 
+template <> struct Vec8<__half> {
+    static __device__ __forceinline__ void load(const __half* p, float (&x)[8]) {
+        uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+        const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 f = __half22float2(h[i]);
+            x[2 * i] = f.x; x[2 * i + 1] = f.y;
+        }
+    }
+    static __device__ __forceinline__ void store(__half* p, const float (&x)[8]) {
+        uint4 u;
+        __half2* h = reinterpret_cast<__half2*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+        *reinterpret_cast<uint4*>(p) = u;
+    }
+};
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
@@ -97,11 +118,11 @@ struct PrestageArgs {
     const ChunkDesc* chunks;  // device [n_chunks]
     int32_t n_chunks, H;
     float lb, l2_eps, q_scale;
-    void *qh, *kh, *vh;       // outputs, bf16 or fp32
+    void *qh, *kh, *vh;       // outputs, fp16 (chunked path) or fp32 (scan path)
     float *gbuf, *beta;       // gate (raw g, or chunk-local cumulative sum) and beta
 };
 
-cudaError_t launch_prestage(const PrestageArgs& a, int io_bf16, int out_bf16, int cumsum,
+cudaError_t launch_prestage(const PrestageArgs& a, int io_bf16, int out_fp16, int cumsum,
                             cudaStream_t s);
 
 struct RingArgs {
@@ -134,19 +155,7 @@ struct EpilogueArgs {
 };
 cudaError_t launch_epilogue(const EpilogueArgs& a, int io_bf16, cudaStream_t s);
 
-struct ChunkedArgs {
-    const void *qh, *kh, *vh;  // bf16 [T][H*128]
-    const float* gcum;         // chunk-local inclusive cumulative gate [T][H*128]
-    const float* beta;         // [T][H]
-    const float* S_in;
-    float* S_out;
-    float* o_core;             // fp32 [T][H*128]
-    const int64_t* cu;
-    int32_t* status;           // workspace error word
-    int32_t n_seqs, H;
-};
 bool chunked_kernel_built();
-cudaError_t launch_chunked(const ChunkedArgs& a, cudaStream_t s);
 
 struct DecodeArgs {
     const void *q, *k, *v, *z, *b, *gout;

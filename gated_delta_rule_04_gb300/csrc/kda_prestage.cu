@@ -229,13 +229,13 @@ cudaError_t launch_prestage_t(const PrestageArgs& a, int cumsum, cudaStream_t s)
 
 }  // namespace
 
-cudaError_t launch_prestage(const PrestageArgs& a, int io_bf16, int out_bf16, int cumsum,
+cudaError_t launch_prestage(const PrestageArgs& a, int io_bf16, int out_fp16, int cumsum,
                             cudaStream_t s) {
     if (io_bf16) {
-        return out_bf16 ? launch_prestage_t<__nv_bfloat16, __nv_bfloat16>(a, cumsum, s)
+        return out_fp16 ? launch_prestage_t<__nv_bfloat16, __half>(a, cumsum, s)
                         : launch_prestage_t<__nv_bfloat16, float>(a, cumsum, s);
     }
-    return out_bf16 ? launch_prestage_t<float, __nv_bfloat16>(a, cumsum, s)
+    return out_fp16 ? launch_prestage_t<float, __half>(a, cumsum, s)
                     : launch_prestage_t<float, float>(a, cumsum, s);
 }
 
