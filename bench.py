@@ -172,24 +172,32 @@ def decode_bytes_per_session_head(io_bytes):
 
 
 # ------------------------------------------------------------------- arms
+PREFILL_WORKLOADS = {"long": 3, "prefill": 2, "varlen": 4}
+
+
 def prefill_arm(args, dev, world, rank):
     import gated_delta_rule_04_gb300 as kda
-    w = kda_synth.workload(3, device=dev)
+    w = kda_synth.workload(PREFILL_WORKLOADS[args.workload], device=dev)
     H, T, W = w.H, w.total_tokens, w.H * D
     kp = kda.make_params(w.params.conv_w, w.params.A_log, w.params.dt_bias, w.params.norm_w,
                          io_dtype=w.io, algo=args.algo)
     toks = list(w.tokens.fields())
-    o = torch.empty(T, W, dtype=torch.bfloat16, device=dev)
-    S_out = torch.empty(1, H, D, D, device=dev)
-    ring_out = torch.empty(1, 3, 3, W, dtype=torch.bfloat16, device=dev)
-    ws_bytes = kda.kda_prefill_workspace_bytes(kp, 1, T)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    n = w.n_seqs
     cu = w.cu_seqlens
+    S_in = ring_in = None
+    if w.warmup_tokens is not None:
+        # continuing sessions: state and ring after the warm-up tokens (timing input)
+        _, S_in, ring_in = kda.kda_prefill(kp, *w.warmup_tokens.fields(), w.warmup_cu)
+    o = torch.empty(T, W, dtype=torch.bfloat16, device=dev)
+    S_out = torch.empty(n, H, D, D, device=dev)
+    ring_out = torch.empty(n, 3, 3, W, dtype=torch.bfloat16, device=dev)
+    ws_bytes = kda.kda_prefill_workspace_bytes(kp, n, T)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def step(evs=None):
-        kda.kda_prefill(kp, *toks, cu, S_out=S_out, ring_out=ring_out, o=o, workspace=ws,
-                        stream=stream, stage_events=evs)
+        kda.kda_prefill(kp, *toks, cu, S_in=S_in, S_out=S_out, ring_in=ring_in, ring_out=ring_out, o=o,
+                        workspace=ws, stream=stream, stage_events=evs)
 
     for _ in range(args.warmup):
         step()
@@ -334,6 +342,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--algo", default="auto", choices=["auto", "scan", "chunked"])
+    ap.add_argument("--workload", default="long", choices=sorted(PREFILL_WORKLOADS),
+                    help="prefill workload of the headline line: long (T=32768, H=96; the default), "
+                         "prefill (T=4096, H=32) or varlen (8 sequences, H=64); the others are for profiling")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -383,10 +394,10 @@ def main():
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_max"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "K3 long prefill: B=1, T=32768, H=96, d=128, bf16 I/O, fp32 state, zero initial state",
-                   "global_batch": world, "seq_len": T, "heads": H, "algo": r["algo_resolved"],
+        "config": {"workload": kda_synth.describe(w.idx) + ", fp32 state",
+                   "global_batch": world * w.n_seqs, "seq_len": T, "heads": H, "algo": r["algo_resolved"],
                    "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "inputs (4.0 GB) larger than L2 (129 MB); no flush"},
+                   "l2": f"inputs ({sum(t.numel() * t.element_size() for t in w.tokens.fields()) / 1e9:.2f} GB) larger than L2 (129 MB); no flush"},
         "roofline": roofline,
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],

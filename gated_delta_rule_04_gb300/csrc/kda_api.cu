@@ -239,7 +239,8 @@ kda_status prefill_impl(const kda_params* p, const void* q, const void* k, const
     } else {
         e = launch_prestage(pa, io_bf16, /*out_fp16=*/1, /*cumsum=*/1, s);
         if (e != cudaSuccess || mark(ev, 1, s) != cudaSuccess) return KDA_ERR_CUDA;
-        PrepArgs pr{ws + L.qh, ws + L.kh, ws + L.vh, gbuf, beta, d_chunks, (int32_t)n_chunks, H, ws + L.rec};
+        PrepArgs pr{ws + L.qh, ws + L.kh, ws + L.vh, gbuf, beta, d_chunks, (int32_t)n_chunks, H, ws + L.rec,
+                    reinterpret_cast<int32_t*>(ws + L.status)};
         e = launch_chunk_prep(pr, s);
         if (e != cudaSuccess) return KDA_ERR_CUDA;
         ChunkRecArgs ca{ws + L.rec, S_in, S_out, ocore, d_cu, d_coff, d_order,

@@ -39,6 +39,7 @@ struct PrepArgs {
     const ChunkDesc* chunks;
     int32_t n_chunks, H;
     void* records;             // [n_chunks][H][REC_BYTES]
+    int32_t* status;           // workspace error word
 };
 cudaError_t launch_chunk_prep(const PrepArgs& a, cudaStream_t s);
 size_t chunk_prep_smem_bytes();

@@ -30,6 +30,13 @@ template <> struct Vec8<float> {
         x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
         x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
     }
+    // shared-memory (or any generic, 16-byte aligned) load without the read-only path
+    static __device__ __forceinline__ void lds(const float* p, float (&x)[8]) {
+        const float4 a = reinterpret_cast<const float4*>(p)[0];
+        const float4 b = reinterpret_cast<const float4*>(p)[1];
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
     static __device__ __forceinline__ void store(float* p, const float (&x)[8]) {
         reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
         reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);

@@ -30,12 +30,13 @@ __device__ __forceinline__ void cp_async_wait_all() {
 }
 
 template <typename TI, typename TO>
-__global__ void __launch_bounds__(PS_THREADS) prestage_kernel(PrestageArgs a, int cumsum) {
+__global__ void __launch_bounds__(PS_THREADS, 2) prestage_kernel(PrestageArgs a, int cumsum) {
     constexpr int VEC = 16 / sizeof(TI);          // elements per 16-byte vector
     constexpr int VPR = D / VEC;                  // vectors per 128-channel row
     extern __shared__ __align__(16) unsigned char smem_raw[];
     TI* xs = reinterpret_cast<TI*>(smem_raw);     // [3][PS_ROWS][D]
     float* tot = reinterpret_cast<float*>(smem_raw + sizeof(TI) * 3 * PS_ROWS * D);  // [16][D]
+    float* cw = tot + 16 * D;                     // [3][D][4] conv weights of this head
 
     const int item = blockIdx.x;
     const int H = a.H, W = H * D;
@@ -63,6 +64,11 @@ __global__ void __launch_bounds__(PS_THREADS) prestage_kernel(PrestageArgs a, in
         } else {
             *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
         }
+    }
+
+    for (int idx = tid; idx < 3 * D; idx += PS_THREADS) {  // conv weights: one 16-byte row per channel
+        const int p = idx / D, c = idx % D;
+        cp_async16(cw + 4 * idx, a.conv_w + ((size_t)p * W + h * D + c) * CONV_K);
     }
 
     // gate inputs and per-lane constants, loaded while the copies fly
@@ -96,7 +102,7 @@ __global__ void __launch_bounds__(PS_THREADS) prestage_kernel(PrestageArgs a, in
         float wt[8][4];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const float4 w4 = __ldg(reinterpret_cast<const float4*>(a.conv_w + ((size_t)p * W + h * D + cb + e) * CONV_K));
+            const float4 w4 = *reinterpret_cast<const float4*>(cw + 4 * (p * D + cb + e));
             wt[e][0] = w4.x; wt[e][1] = w4.y; wt[e][2] = w4.z; wt[e][3] = w4.w;
         }
         float win[7][8];  // smem rows hw*4 .. hw*4+6 = tokens hw*4-3 .. hw*4+3
@@ -217,7 +223,7 @@ __global__ void ring_update_kernel(RingArgs a) {
 
 template <typename TI, typename TO>
 cudaError_t launch_prestage_t(const PrestageArgs& a, int cumsum, cudaStream_t s) {
-    const size_t smem = sizeof(TI) * 3 * PS_ROWS * D + sizeof(float) * 16 * D;
+    const size_t smem = sizeof(TI) * 3 * PS_ROWS * D + sizeof(float) * 16 * D + sizeof(float) * 3 * D * CONV_K;
     cudaError_t e = cudaFuncSetAttribute(prestage_kernel<TI, TO>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
