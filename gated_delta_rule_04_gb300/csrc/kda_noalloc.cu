@@ -1,0 +1,197 @@
+// kda_prefill_noalloc: the prefill for callers that may not allocate memory.
+//
+// kda_prefill asks its caller for a workspace.  Some callers cannot provide
+// one on demand: code whose device memory is fully planned up front (a plugin
+// inside an inference engine that owns every byte, a serving loop whose
+// memory plan is fixed at start-up) and code that must not call cudaMalloc or
+// cudaFree, which can synchronise the whole device and stall every other
+// stream.  This entry point takes the same inputs and outputs as kda_prefill
+// but no workspace: its scratch is a fixed array in device memory that every
+// GPU which loads this library holds until the process exits.  It calls no
+// memory-allocating routine, on the device or on the host.
+//
+// Set-up: the first call on each device looks up the array's device address
+// with cudaGetSymbolAddress (with that device current) and caches it; make
+// that first call before any stream capture.
+// Sharing: every call uses the same array and leaves its contents behind.
+// The only part that must start at zero (the error word) is cleared by each
+// call; every other byte is written before it is read.  Calls whose work can
+// overlap on the GPU (concurrent streams, or host threads on one device)
+// race on the array: order them on one stream.
+#include <string.h>
+
+#include <atomic>
+
+#include "kda_chunk_layout.cuh"
+
+namespace kda {
+namespace {
+
+constexpr size_t NA_ALIGN = 256;
+constexpr int NA_CHUNK = CHUNK_T;
+constexpr int NA_MAX_DEVICES = 64;
+constexpr int NA_MAX_SEQS = 512;           // sequences per call
+constexpr size_t NA_META_MAX = 32768;      // host-side metadata built on the stack
+
+// The scratch array.  In host code this name is only a handle for
+// cudaGetSymbolAddress, never an address to pass to a kernel.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
+
+std::atomic<void*> g_scratch_addr[NA_MAX_DEVICES];
+
+size_t up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct NaLayout {
+    size_t status, meta, meta_bytes, off_coff, off_order, off_chunks;
+    size_t qh, kh, vh, g, beta, ocore, rec, total;
+};
+
+// Same region order as the caller-provided workspace of kda_prefill.
+NaLayout na_layout(int H, bool chunked, int32_t n, int64_t T, int64_t nc) {
+    NaLayout L{};
+    const size_t W = (size_t)H * D, op = chunked ? 2 : 4;
+    size_t off = 0;
+    L.status = off; off += NA_ALIGN;
+    L.meta = off;
+    L.off_coff = sizeof(int64_t) * (size_t)(n + 1);
+    L.off_order = L.off_coff + sizeof(int64_t) * (size_t)(n + 1);
+    L.off_chunks = up(L.off_order + sizeof(int32_t) * (size_t)n, 16);
+    L.meta_bytes = L.off_chunks + sizeof(ChunkDesc) * (size_t)nc;
+    off = up(off + L.meta_bytes, NA_ALIGN);
+    L.qh = off; off = up(off + op * (size_t)T * W, NA_ALIGN);
+    L.kh = off; off = up(off + op * (size_t)T * W, NA_ALIGN);
+    L.vh = off; off = up(off + op * (size_t)T * W, NA_ALIGN);
+    L.g = off; off = up(off + 4 * (size_t)T * W, NA_ALIGN);
+    L.beta = off; off = up(off + 4 * (size_t)T * H, NA_ALIGN);
+    L.ocore = off; off = up(off + 4 * (size_t)T * W, NA_ALIGN);
+    L.rec = off;
+    if (chunked) off = up(off + (size_t)REC_BYTES * (size_t)nc * H, NA_ALIGN);
+    L.total = off;
+    return L;
+}
+
+// Device address of the scratch array on the current device (set up once).
+cudaError_t scratch_address(unsigned char** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= NA_MAX_DEVICES) return cudaErrorInvalidDevice;
+    void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev].store(p, std::memory_order_release);
+    }
+    *out = static_cast<unsigned char*>(p);
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" kda_status kda_prefill_noalloc(const kda_params* p, const void* q, const void* k, const void* v,
+                                          const void* z, const void* b, const void* gout,
+                                          const int64_t* cu, int32_t n_seqs, int64_t total_tokens,
+                                          const float* S_in, float* S_out, const void* ring_in, void* ring_out,
+                                          void* o, void* stream_) {
+    // the parameter checks and the algorithm choice of kda_prefill
+    const int32_t algo = kda_prefill_algo(p);
+    if (algo < 0) {
+        if (p && (p->head_dim != D || p->conv_kernel != CONV_K)) return KDA_ERR_UNSUPPORTED;
+        if (p && p->algo == KDA_ALGO_CHUNKED) return KDA_ERR_UNSUPPORTED;
+        return KDA_ERR_INVALID_ARG;
+    }
+    const bool chunked = algo == KDA_ALGO_CHUNKED;
+    if (n_seqs < 0 || total_tokens < 0 || cu == nullptr) return KDA_ERR_INVALID_ARG;
+    if (cu[0] != 0 || cu[n_seqs] != total_tokens) return KDA_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n_seqs; ++i)
+        if (cu[i + 1] < cu[i]) return KDA_ERR_INVALID_ARG;
+    if (n_seqs == 0) return KDA_OK;
+    if (total_tokens > 0) {
+        const void* tok[6] = {q, k, v, z, gout, o};
+        for (int i = 0; i < 6; ++i)
+            if (tok[i] == nullptr || !al16(tok[i])) return KDA_ERR_INVALID_ARG;
+        if (b == nullptr) return KDA_ERR_INVALID_ARG;
+    }
+    if (S_out == nullptr || !al16(S_out) || (S_in && !al16(S_in))) return KDA_ERR_INVALID_ARG;
+    if ((ring_in && !al16(ring_in)) || (ring_out && !al16(ring_out))) return KDA_ERR_INVALID_ARG;
+
+    // size limits of the fixed scratch and of the on-stack metadata
+    int64_t nc = 0;
+    for (int32_t i = 0; i < n_seqs; ++i) nc += (cu[i + 1] - cu[i] + NA_CHUNK - 1) / NA_CHUNK;
+    const int H = p->num_heads, W = H * D;
+    if (n_seqs > NA_MAX_SEQS) return KDA_ERR_UNSUPPORTED;
+    const NaLayout L = na_layout(H, chunked, n_seqs, total_tokens, nc);
+    if (L.meta_bytes > NA_META_MAX) return KDA_ERR_UNSUPPORTED;
+    if (L.total > KDA_NOALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
+
+    unsigned char* ws = nullptr;
+    if (scratch_address(&ws) != cudaSuccess) return KDA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream_);
+
+    // metadata on the stack: cu_seqlens, first chunk per sequence, order, chunks
+    alignas(16) unsigned char meta[NA_META_MAX];
+    memcpy(meta, cu, sizeof(int64_t) * (size_t)(n_seqs + 1));
+    int64_t* coff = reinterpret_cast<int64_t*>(meta + L.off_coff);
+    int32_t* order = reinterpret_cast<int32_t*>(meta + L.off_order);
+    ChunkDesc* cds = reinterpret_cast<ChunkDesc*>(meta + L.off_chunks);
+    int64_t ci = 0;
+    for (int32_t n = 0; n < n_seqs; ++n) {
+        coff[n] = ci;
+        order[n] = n;
+        for (int64_t t = cu[n]; t < cu[n + 1]; t += NA_CHUNK) {
+            const int64_t len = cu[n + 1] - t < NA_CHUNK ? cu[n + 1] - t : NA_CHUNK;
+            cds[ci++] = ChunkDesc{n, (int32_t)t, (int32_t)len, (int32_t)(t - cu[n])};
+        }
+    }
+    coff[n_seqs] = ci;
+    // longest sequences first (insertion sort: stable, no allocation)
+    for (int32_t i = 1; i < n_seqs; ++i) {
+        const int32_t x = order[i];
+        const int64_t lx = cu[x + 1] - cu[x];
+        int32_t j = i - 1;
+        while (j >= 0 && cu[order[j] + 1] - cu[order[j]] < lx) { order[j + 1] = order[j]; --j; }
+        order[j + 1] = x;
+    }
+    const int64_t* d_cu = reinterpret_cast<const int64_t*>(ws + L.meta);
+    const int64_t* d_coff = reinterpret_cast<const int64_t*>(ws + L.meta + L.off_coff);
+    const int32_t* d_order = reinterpret_cast<const int32_t*>(ws + L.meta + L.off_order);
+    const ChunkDesc* d_chunks = reinterpret_cast<const ChunkDesc*>(ws + L.meta + L.off_chunks);
+    cudaError_t e = cudaMemsetAsync(ws + L.status, 0, NA_ALIGN, s);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    e = cudaMemcpyAsync(ws + L.meta, meta, L.meta_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+
+    const int io_bf16 = p->io_dtype == KDA_DTYPE_BF16;
+    const float qs = p->q_scale != 0.f ? p->q_scale : 1.0f / sqrtf((float)D);
+    float* gbuf = reinterpret_cast<float*>(ws + L.g);
+    float* beta = reinterpret_cast<float*>(ws + L.beta);
+    float* ocore = reinterpret_cast<float*>(ws + L.ocore);
+    int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
+    PrestageArgs pa{q, k, v, z, b, p->conv_w, p->A_log, p->dt_bias, ring_in, d_cu, d_chunks,
+                    (int32_t)nc, H, p->gate_lower_bound, p->l2_eps, qs,
+                    ws + L.qh, ws + L.kh, ws + L.vh, gbuf, beta};
+    if (!chunked) {
+        if (launch_prestage(pa, io_bf16, 0, 0, s) != cudaSuccess) return KDA_ERR_CUDA;
+        ScanArgs sa{reinterpret_cast<const float*>(ws + L.qh), reinterpret_cast<const float*>(ws + L.kh),
+                    reinterpret_cast<const float*>(ws + L.vh), gbuf, beta, S_in, S_out, ocore, d_cu,
+                    n_seqs, H};
+        if (launch_scan(sa, s) != cudaSuccess) return KDA_ERR_CUDA;
+    } else {
+        if (launch_prestage(pa, io_bf16, 1, 1, s) != cudaSuccess) return KDA_ERR_CUDA;
+        PrepArgs pr{ws + L.qh, ws + L.kh, ws + L.vh, gbuf, beta, d_chunks, (int32_t)nc, H, ws + L.rec, status};
+        if (launch_chunk_prep(pr, s) != cudaSuccess) return KDA_ERR_CUDA;
+        ChunkRecArgs ca{ws + L.rec, S_in, S_out, ocore, d_cu, d_coff, d_order, status, n_seqs, H};
+        if (launch_chunk_recurrence(ca, s) != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    EpilogueArgs ea{ocore, gout, p->norm_w, o, total_tokens, H, p->norm_eps};
+    if (launch_epilogue(ea, io_bf16, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (ring_out) {
+        RingArgs ra{q, k, v, ring_in, ring_out, d_cu, n_seqs, W};
+        if (launch_ring_update(ra, io_bf16, s) != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}

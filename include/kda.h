@@ -148,6 +148,32 @@ kda_status kda_decode(const kda_params* p, int32_t n_sessions,
                       const void* b, const void* gout,
                       float* S, void* ring, void* o, void* stream);
 
+/*
+ * kda_prefill without a workspace, for callers that cannot allocate device
+ * memory when they run: a plugin inside an engine that owns every byte of
+ * device memory, or a serving loop that must not call cudaMalloc/cudaFree
+ * because they can synchronise the whole device.  The sources describe no
+ * counterpart; this is an interface addition of this library.
+ * Same arguments and results as kda_prefill, minus the workspace.  The
+ * scratch is a fixed device array of KDA_NOALLOC_SCRATCH_BYTES, held by every
+ * GPU that loads the library until the process exits.  The first call on a
+ * device looks up that array's address (cudaGetSymbolAddress) and caches it:
+ * make it before any stream capture.  Every call shares the array, so calls
+ * that can overlap on the GPU race: issue them in order on one stream.
+ * Returns KDA_ERR_WORKSPACE when the problem needs more scratch than the
+ * array holds (kda_prefill_workspace_bytes reports the need), and
+ * KDA_ERR_UNSUPPORTED for more than 512 sequences in one call.  Bounded-wait
+ * timeouts inside this call are not reported (the error word is private).
+ * Calls no memory-allocating routine.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+kda_status kda_prefill_noalloc(const kda_params* p,
+                               const void* q, const void* k, const void* v, const void* z,
+                               const void* b, const void* gout,
+                               const int64_t* cu_seqlens_host, int32_t n_seqs, int64_t total_tokens,
+                               const float* S_in, float* S_out,
+                               const void* ring_in, void* ring_out, void* o, void* stream);
+
 /* Synchronises `stream` and reads the error word the prefill kernels keep in
  * `workspace`: KDA_OK, or KDA_ERR_TIMEOUT when a bounded in-kernel wait gave
  * up during an earlier call on that workspace (the word is then cleared). */
