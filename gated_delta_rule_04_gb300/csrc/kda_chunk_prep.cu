@@ -4,7 +4,7 @@
 // per-channel cumulative log gate described on "memra-engine 0.124.0, module
 // kda" (PREFILL DISPATCH) and the 16-token tile bound of "Kimi K3 - Retention
 // gate - OpenModelAtlas" (section "Why": with g >= -5 every rescaling over a
-// 16-token tile stays below e^80).
+// 16-token tile stays below e^80, inside bf16's range).
 //
 // With G_r the inclusive cumulative gate inside the chunk (per key channel):
 //   A[r][s] = beta_r sum_i k_ri k_si e^{G_ri - G_si}   (s < r)
@@ -15,20 +15,24 @@
 // The sequential kernel then needs only U = U0 - W S, O = Q+ S + P U and
 // S' = Diag(decay) S + Kt^T U per chunk.
 //
-// Range.  e^{G_r - G_s} is split at the 16-token sub-tile boundaries.  With
-// st(a)/en(a) the first/last token of sub-tile a, Y_s = e^{G_en(b) - G_s} <= 1
-// for s in sub-tile b, and for r in sub-tile a:
-//   a > b:  e^{G_r - G_s} = [e^{G_r - G_st(a)} e^{G_st(a) - G_en(b)}] * Y_s
-//           both brackets <= 1: these six off-diagonal 16 x 16 blocks run on
-//           the tensor cores with fp16 operands (two M=128 MMAs, rows =
-//           (block pair, r) for k and for q, columns = all 64 s);
-//   a = b:  e^{G_r - G_s} = (1 / Y_r) * Y_s with 1/Y_r <= e^{75}: the four
-//           diagonal blocks stay in fp32 on the CUDA cores (fp16 cannot hold
-//           e^{75}, and bf16 operands there triple the end-to-end error).
+// Range.  For s in 16-token sub-tile b the reference point is the last token
+// of that sub-tile, en(b):  e^{G_r - G_s} = e^{G_r - G_en(b)} * Y_s with
+// Y_s = e^{G_en(b) - G_s} <= 1.  The left factor is <= 1 when r lies in a
+// later sub-tile and at most e^{75} inside the diagonal sub-tile, which bf16
+// holds.  All of A and the off-diagonal blocks of P therefore run on the
+// tensor cores as two bf16 MMAs (M = 128, N = 64 = every s, K = 128 keys):
+// 256 left rows = (A rows grouped by column sub-tile b: 64+48+32+16) +
+// (off-diagonal P rows: 48+32+16).  The diagonal blocks of P stay in fp32 on
+// the CUDA cores: P reaches the output directly, and bf16 there would triple
+// the end-to-end error, while bf16 in A changes it by under 5%.
+// Left factors for a later sub-tile a > b are formed as a product of two
+// factors <= 1, e^{G_r - G_st(a)} e^{G_st(a) - G_en(b)}, so nothing
+// overflows or loses precision to fp32 subnormals.
+//
 // The unit lower-triangular solve is blockwise: the four 16 x 16 diagonal
 // inverses by forward substitution, then the off-diagonal blocks of the
 // inverse by 16 x 16 products, diagonal by diagonal.  W^T = (k e^G)^T T^T and
-// U0^T = v^T T^T run as two M=128 tensor-core MMAs.
+// U0^T = v^T T^T run as two fp16 M=128 MMAs.
 //
 // Output: one record per (chunk, head) holding the operand tiles in the exact
 // shared-memory image the tcgen05 recurrence kernel consumes (fp16, K-major,
@@ -39,31 +43,46 @@
 namespace kda {
 namespace {
 
-constexpr int PT = 256;        // threads (8 warps)
+constexpr int PT = 512;        // threads (16 warps: four per scheduler to hide latency)
 constexpr int C = CHUNK_T;     // 64 tokens
 constexpr int LDS = 65;        // padded fp32 row stride of the 64 x 64 matrices
-constexpr uint32_t TMEM_COLS = 256;  // [0,64) A-rows D, [64,128) P-rows D, [128,192) W^T, [192,256) U0^T
+constexpr int LDY = 132;       // padded fp32 row stride of Y
+constexpr uint32_t TMEM_COLS = 256;  // [0,64) left tile 0, [64,128) left tile 1, [128,192) W^T, [192,256) U0^T
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
 // shared-memory map (bytes, from a 1 KiB aligned base)
-constexpr uint32_t S_G = 0;                    // fp32 [64][128] G (rows past the chunk repeat the last)
-constexpr uint32_t S_Y = S_G + 32768;          // fp32 [64][128] Y, later X = (I+A)^{-1} fp32 [64][65]
-constexpr uint32_t S_KH = S_Y + 32768;         // fp16 [64][128] k^ (plain row-major)
-constexpr uint32_t S_QH = S_KH + 16384;        // fp16 [64][128] q^
-constexpr uint32_t S_LOFF = S_QH + 16384;      // fp16 2 tiles x [128 rows][128 keys] (swizzled), later KPT/VT/TT
-constexpr uint32_t S_KPT = S_LOFF;             //   fp16 [128 key][64 tok]  (k e^G)^T
-constexpr uint32_t S_VT = S_LOFF + 16384;      //   fp16 [128 val][64 tok]  v^T
-constexpr uint32_t S_TT = S_LOFF + 32768;      //   fp16 [64 r][64 s]       T
-constexpr uint32_t S_RT = S_LOFF + 65536;      // fp16 [64 s][128 keys] (swizzled) k Y
-constexpr uint32_t S_AM = S_RT + 16384;        // fp32 [64][65] A (with beta)
-constexpr uint32_t S_PM = S_AM + 64 * LDS * 4; // fp32 [64][65] P
-constexpr uint32_t S_MT = S_PM + 64 * LDS * 4; // fp32 [6 pairs][128] e^{G_st(a) - G_en(b)}; [4][128] e^{G_en(a)-G_st(a)}; [4][128] e^{G_st(a)}
-constexpr uint32_t S_BT = S_MT + 14 * 128 * 4; // fp32 [64] beta
-constexpr uint32_t S_BAR = S_BT + 256;         // mbarrier + TMEM slot
+constexpr uint32_t S_G = 0;                      // fp32 [64][128] G (rows past the chunk repeat the last)
+constexpr uint32_t S_Y = S_G + 32768;            // fp32 [64][132] Y; later X = (I+A)^{-1} fp32 [64][65]
+constexpr uint32_t S_KH = S_Y + 33792;           // fp16 [64][128] k^ (plain row-major)
+constexpr uint32_t S_QH = S_KH + 16384;          // fp16 [64][128] q^
+constexpr uint32_t S_LAP = S_QH + 16384;         // bf16 2 tiles x [128 rows][128 keys] (swizzled); later KPT/VT/TT
+constexpr uint32_t S_KPT = S_LAP;                //   fp16 [128 key][64 tok]  (k e^G)^T
+constexpr uint32_t S_VT = S_LAP + 16384;         //   fp16 [128 val][64 tok]  v^T
+constexpr uint32_t S_TT = S_LAP + 32768;         //   fp16 [64 r][64 s]       T
+constexpr uint32_t S_RT = S_LAP + 65536;         // bf16 [64 s][128 keys] k Y (swizzled); later v^ rows, then W
+constexpr uint32_t S_AM = S_RT + 16384;          // fp32 [64][65] A (with beta)
+constexpr uint32_t S_PM = S_AM + 64 * LDS * 4;   // fp32 [64][65] P
+constexpr uint32_t S_MT = S_PM + 64 * LDS * 4;   // fp32 [6][128] e^{G_st(a) - G_en(b)} per pair a > b; [4][128] e^{G_en(a) - G_st(a)}
+constexpr uint32_t S_BT = S_MT + 10 * 128 * 4;   // fp32 [64] beta
+constexpr uint32_t S_BAR = S_BT + 256;           // mbarrier, TMEM slot, flag
 constexpr uint32_t SMEM_BYTES = S_BAR + 64 + 1024;
 
+// sub-tile pairs a > b in the order of the factor table
 __constant__ int8_t kPairA[6] = {1, 2, 3, 2, 3, 3};
 __constant__ int8_t kPairB[6] = {0, 0, 0, 1, 1, 2};
+__device__ __forceinline__ int pair_of(int a, int b) { return b == 0 ? a - 1 : (b == 1 ? a + 1 : 5); }
+
+// Row groups of the 256 left rows: (is_P, column sub-tile b, first r, first row)
+__constant__ int16_t kGroup[7][4] = {
+    {0, 0, 0, 0}, {0, 1, 16, 64}, {0, 2, 32, 112}, {0, 3, 48, 144},
+    {1, 0, 16, 160}, {1, 1, 32, 208}, {1, 2, 48, 240}};
+__device__ __forceinline__ int group_of(int row) {
+    int g = 0;
+#pragma unroll
+    for (int j = 1; j < 7; ++j)
+        if (row >= kGroup[j][3]) g = j;
+    return g;
+}
 
 __device__ __forceinline__ uint4 pack8_f16(const float* v) {
     uint4 u;
@@ -72,8 +91,15 @@ __device__ __forceinline__ uint4 pack8_f16(const float* v) {
     for (int e = 0; e < 4; ++e) p[e] = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
     return u;
 }
+__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+    uint4 u;
+    __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) p[e] = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+    return u;
+}
 
-// eight fp16 values from shared memory (16-byte aligned) as fp32
+// eight fp16 / fp32 values from shared memory (16-byte aligned) as fp32
 __device__ __forceinline__ void lds_h8(const __half* p, float (&x)[8]) {
     const uint4 u = *reinterpret_cast<const uint4*>(p);
     const __half2* h = reinterpret_cast<const __half2*>(&u);
@@ -83,6 +109,24 @@ __device__ __forceinline__ void lds_h8(const __half* p, float (&x)[8]) {
         x[2 * i] = f.x;
         x[2 * i + 1] = f.y;
     }
+}
+__device__ __forceinline__ void lds_f8(const float* p, float (&x)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0];
+    const float4 b = reinterpret_cast<const float4*>(p)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void sts_f8(float* p, const float (&x)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
+}
+
+// One-instruction reciprocal (max error 1 ulp); every argument here is a
+// normal number in [e^-75, 1].
+__device__ __forceinline__ float rcp_approx(float y) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+    return r;
 }
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
@@ -114,7 +158,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
     float* Xm = reinterpret_cast<float*>(sb + S_Y);
     const __half* KH = reinterpret_cast<const __half*>(sb + S_KH);
     const __half* QH = reinterpret_cast<const __half*>(sb + S_QH);
-    const __half* VH = reinterpret_cast<const __half*>(sb + S_RT);  // v^ rows, after the off-diagonal MMAs
+    const __half* VH = reinterpret_cast<const __half*>(sb + S_RT);  // v^ rows, once the A/P MMAs are done
     float* Am = reinterpret_cast<float*>(sb + S_AM);
     float* Pm = reinterpret_cast<float*>(sb + S_PM);
     float* Mt = reinterpret_cast<float*>(sb + S_MT);
@@ -144,13 +188,13 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
         ptx::fence_mbar_init();
     }
 
-    // ---- 1. G, beta, k^, q^ into shared memory (16-byte cp.async copies, all in flight at once)
-    for (int idx = tid; idx < C * 32; idx += PT) {          // G: 64 rows x 32 x 16 B
+    // ---- 1. G, k^, q^ into shared memory: 16-byte cp.async copies, all in flight at once
+    for (int idx = tid; idx < C * 32; idx += PT) {
         const int r = idx >> 5, v4 = idx & 31;
         const int rr = r < L ? r : L - 1;
         cp_async16(sb + S_G + 16 * idx, a.gcum + gidx(rr, 4 * v4));
     }
-    for (int idx = tid; idx < C * 16; idx += PT) {          // k^, q^: 64 rows x 16 x 16 B
+    for (int idx = tid; idx < C * 16; idx += PT) {
         const int r = idx >> 4, v8 = idx & 15;
         if (r < L) {
             cp_async16(sb + S_KH + 16 * idx, kh + gidx(r, 8 * v8));
@@ -160,126 +204,116 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
             reinterpret_cast<uint4*>(sb + S_QH)[idx] = make_uint4(0, 0, 0, 0);
         }
     }
-    cp_async_wait_all();
     if (tid < C) bt[tid] = tid < L ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
+    cp_async_wait_all();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // ---- 2. Y, per-tile factors, right operand R = k Y (fp16 swizzled)
-    for (int idx = tid; idx < C * D; idx += PT) {
-        const int r = idx >> 7, i = idx & 127;
+    // ---- 2. Y_s = e^{G_en(b) - G_s} and the per-sub-tile factors (8 channels per step)
+    for (int idx = tid; idx < C * 16; idx += PT) {
+        const int r = idx >> 4, ch = idx & 15;
         const int en = min((r & ~15) + 15, L - 1);
-        Y[idx] = __expf(G[en * D + i] - G[idx]);
+        float g[8], ge[8], y[8];
+        lds_f8(G + r * D + 8 * ch, g);
+        lds_f8(G + en * D + 8 * ch, ge);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = __expf(ge[e] - g[e]);
+        sts_f8(Y + r * LDY + 8 * ch, y);
     }
-    for (int idx = tid; idx < 14 * D; idx += PT) {
+    for (int idx = tid; idx < 10 * D; idx += PT) {
         const int m = idx >> 7, i = idx & 127;
-        float val;
-        if (m < 6) {          // e^{G_st(a) - G_en(b)}, a > b
-            const int st = min(16 * kPairA[m], L - 1), en = min(16 * kPairB[m] + 15, L - 1);
-            val = expf(G[st * D + i] - G[en * D + i]);
-        } else if (m < 10) {  // e^{G_en(a) - G_st(a)}
-            const int ta = m - 6;
-            const int st = min(16 * ta, L - 1), en = min(16 * ta + 15, L - 1);
-            val = expf(G[en * D + i] - G[st * D + i]);
-        } else {              // e^{G_st(a)}
-            const int st = min(16 * (m - 10), L - 1);
-            val = expf(G[st * D + i]);
-        }
-        Mt[idx] = val;
+        int st, en;
+        if (m < 6) { st = min(16 * kPairA[m], L - 1); en = min(16 * kPairB[m] + 15, L - 1); }
+        else { st = min(16 * (m - 6) + 15, L - 1); en = min(16 * (m - 6), L - 1); }  // e^{G_en(a) - G_st(a)}
+        Mt[idx] = __expf(G[st * D + i] - G[en * D + i]);
     }
     __syncthreads();
-    for (int idx = tid; idx < C * 16; idx += PT) {           // R: 64 rows x 16 chunks of 8 keys
+
+    // ---- 3. right operand R_s = k_s Y_s and the 256 left rows (bf16, swizzled)
+    for (int idx = tid; idx < C * 16; idx += PT) {
         const int s = idx >> 4, ch = idx & 15;
-        float v[8];
+        float k8[8], y8[8], v[8];
+        lds_h8(KH + s * D + 8 * ch, k8);
+        lds_f8(Y + s * LDY + 8 * ch, y8);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int i = ch * 8 + e;
-            v[e] = __half2float(KH[s * D + i]) * Y[s * D + i];
-        }
-        *reinterpret_cast<uint4*>(sb + S_RT + sw128_off(s, ch * 8, C)) = pack8_f16(v);
+        for (int e = 0; e < 8; ++e) v[e] = k8[e] * y8[e];
+        *reinterpret_cast<uint4*>(sb + S_RT + sw128_off(s, 8 * ch, C)) = pack8_bf16(v);
     }
-    // left operand of the off-diagonal blocks: row (pair p, r_local) =
-    //   k_r e^{G_r - G_st(a)} e^{G_st(a) - G_en(b)}, with
-    //   e^{G_r - G_st(a)} = e^{G_en(a) - G_st(a)} / Y_r   (both <= 1 after the division)
-    // tile 0 holds the k rows, tile 1 the q rows; rows 96..127 are zero.
-    for (int idx = tid; idx < 2 * 128 * 16; idx += PT) {
-        const int tile = idx >> 11, rem = idx & 2047;
-        const int row = rem >> 4, ch = rem & 15;
-        float v[8];
-        if (row < 96) {
-            const int p = row >> 4, rl = row & 15;
-            const int ta = kPairA[p];
-            const int r = 16 * ta + rl;
-            const __half* src = tile == 0 ? KH : QH;
+    for (int idx = tid; idx < 256 * 16; idx += PT) {
+        const int row = idx >> 4, ch = idx & 15;
+        const int g = group_of(row);
+        const int isP = kGroup[g][0], b = kGroup[g][1];
+        const int r = kGroup[g][2] + (row - kGroup[g][3]);
+        const int ta = r >> 4;
+        float x8[8], y8[8], v[8];
+        lds_h8((isP ? QH : KH) + r * D + 8 * ch, x8);
+        lds_f8(Y + r * LDY + 8 * ch, y8);
+        if (ta == b) {        // e^{G_r - G_en(b)} = 1 / Y_r
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int i = ch * 8 + e;
-                const float x = Mt[(6 + ta) * D + i] * __frcp_rn(Y[r * D + i]);
-                v[e] = __half2float(src[r * D + i]) * x * Mt[p * D + i];
-            }
-        } else {
+            for (int e = 0; e < 8; ++e) v[e] = x8[e] * rcp_approx(y8[e]);
+        } else {              // e^{G_r - G_st(a)} e^{G_st(a) - G_en(b)}, with e^{G_r - G_st(a)} = e^{G_en(a) - G_st(a)} / Y_r
+            float va[8], cab[8];
+            lds_f8(Mt + (6 + ta) * D + 8 * ch, va);
+            lds_f8(Mt + pair_of(ta, b) * D + 8 * ch, cab);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = 0.f;
+            for (int e = 0; e < 8; ++e) v[e] = x8[e] * (va[e] * rcp_approx(y8[e])) * cab[e];
         }
-        *reinterpret_cast<uint4*>(sb + S_LOFF + tile * 32768 + sw128_off(row, ch * 8, 128)) = pack8_f16(v);
+        *reinterpret_cast<uint4*>(sb + S_LAP + (row >> 7) * 32768 + sw128_off(row & 127, 8 * ch, 128)) =
+            pack8_bf16(v);
     }
     ptx::fence_async_smem();
     ptx::tc_fence_before();
     __syncthreads();
 
-    // ---- 3. off-diagonal blocks on the tensor cores: D[row][s] for all 64 s
-    constexpr uint32_t IDESC_N64 = ptx::idesc_f16_f32(128, 64);
+    // ---- 4. A and the off-diagonal P blocks on the tensor cores
+    constexpr uint32_t IDESC_BF16_N64 = ptx::idesc_bf16_f32(128, 64);
+    constexpr uint32_t IDESC_F16_N64 = ptx::idesc_f16_f32(128, 64);
     if (tid == 0) {
         ptx::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             const uint32_t koff = (kk & 3) * 32;
             const uint64_t bR = ptx::sdesc_sw128(base + S_RT + (kk >> 2) * 8192 + koff);
-            const uint64_t aK = ptx::sdesc_sw128(base + S_LOFF + (kk >> 2) * 16384 + koff);
-            const uint64_t aQ = ptx::sdesc_sw128(base + S_LOFF + 32768 + (kk >> 2) * 16384 + koff);
-            ptx::mma_f16(tmem, aK, bR, IDESC_N64, kk > 0);
-            ptx::mma_f16(tmem + 64, aQ, bR, IDESC_N64, kk > 0);
+            const uint64_t a0 = ptx::sdesc_sw128(base + S_LAP + (kk >> 2) * 16384 + koff);
+            const uint64_t a1 = ptx::sdesc_sw128(base + S_LAP + 32768 + (kk >> 2) * 16384 + koff);
+            ptx::mma_f16(tmem, a0, bR, IDESC_BF16_N64, kk > 0);
+            ptx::mma_f16(tmem + 64, a1, bR, IDESC_BF16_N64, kk > 0);
         }
         ptx::mma_commit(bar);
     }
 
-    // ---- 4. diagonal blocks in fp32 while the MMAs run: e^{G_r - G_s} = Y_s / Y_r.
-    // Thread (tile a, 4 rows x 4 cols block, K quarter); partial sums reduced in
-    // shared memory.  Blocks above the diagonal of a tile are skipped.
+    // ---- 5. diagonal blocks of P in fp32 while the MMAs run: e^{G_r - G_s} = Y_s / Y_r.
+    // Thread = (sub-tile, 4x4 block, K quarter); the quarters interleave 8-channel
+    // chunks so that neighbouring lanes read different banks.
+    for (int idx = tid; idx < C * LDS; idx += PT) { Am[idx] = 0.f; Pm[idx] = 0.f; }
+    __syncthreads();
     {
-        // zero A and P (the off-diagonal blocks are filled from TMEM later)
-        for (int idx = tid; idx < C * LDS; idx += PT) { Am[idx] = 0.f; Pm[idx] = 0.f; }
-        __syncthreads();
-        const int ta = tid >> 6;            // tile
-        const int rem = tid & 63;
-        const int blk = rem >> 2, kq = rem & 3;
-        const int br = blk >> 2, bc = blk & 3;  // 4x4 sub-blocks of the 16x16 tile
-        float accA[4][4], accP[4][4];
+        const int ta = tid >> 7, rem = tid & 127;
+        const int blk = rem >> 3, kq = rem & 7;   // 16 blocks of 4x4 x 8 interleaved K slices
+        const int br = blk >> 2, bc = blk & 3;
+        float acc[4][4];
 #pragma unroll
         for (int x = 0; x < 4; ++x)
 #pragma unroll
-            for (int y = 0; y < 4; ++y) { accA[x][y] = 0.f; accP[x][y] = 0.f; }
+            for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+        const int r0 = 16 * ta + 4 * br, s0 = 16 * ta + 4 * bc;
         if (bc <= br) {
-            const int r0 = 16 * ta + 4 * br, s0 = 16 * ta + 4 * bc;
 #pragma unroll 1
-            for (int i0 = 32 * kq; i0 < 32 * kq + 32; i0 += 8) {
-                float lk[4][8], lq[4][8], rr[4][8];
+            for (int c8 = kq; c8 < 16; c8 += 8) {
+                float lq[4][8], rr[4][8];
 #pragma unroll
                 for (int x = 0; x < 4; ++x) {
-                    float y8[8], k8[8], q8[8], ys8[8], ks8[8];
-                    Vec8<float>::lds(Y + (r0 + x) * D + i0, y8);
-                    Vec8<float>::lds(Y + (s0 + x) * D + i0, ys8);
-                    lds_h8(KH + (r0 + x) * D + i0, k8);
-                    lds_h8(QH + (r0 + x) * D + i0, q8);
-                    lds_h8(KH + (s0 + x) * D + i0, ks8);
+                    float q8[8], yr[8], k8[8], ys[8];
+                    lds_h8(QH + (r0 + x) * D + 8 * c8, q8);
+                    lds_f8(Y + (r0 + x) * LDY + 8 * c8, yr);
+                    lds_h8(KH + (s0 + x) * D + 8 * c8, k8);
+                    lds_f8(Y + (s0 + x) * LDY + 8 * c8, ys);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const float inv = __frcp_rn(y8[e]);
-                        lk[x][e] = k8[e] * inv;
-                        lq[x][e] = q8[e] * inv;
-                        rr[x][e] = ks8[e] * ys8[e];
+                        lq[x][e] = q8[e] * rcp_approx(yr[e]);
+                        rr[x][e] = k8[e] * ys[e];
                     }
                 }
 #pragma unroll
@@ -287,74 +321,51 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
 #pragma unroll
                     for (int x = 0; x < 4; ++x)
 #pragma unroll
-                        for (int y = 0; y < 4; ++y) {
-                            accA[x][y] = fmaf(lk[x][e], rr[y][e], accA[x][y]);
-                            accP[x][y] = fmaf(lq[x][e], rr[y][e], accP[x][y]);
-                        }
+                        for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(lq[x][e], rr[y][e], acc[x][y]);
             }
         }
-        // reduce the four K quarters with shuffles (lanes kq = 0..3 are adjacent)
 #pragma unroll
         for (int x = 0; x < 4; ++x)
 #pragma unroll
             for (int y = 0; y < 4; ++y) {
-                float va = accA[x][y], vp = accP[x][y];
-                va += __shfl_xor_sync(0xffffffffu, va, 1);
-                va += __shfl_xor_sync(0xffffffffu, va, 2);
-                vp += __shfl_xor_sync(0xffffffffu, vp, 1);
-                vp += __shfl_xor_sync(0xffffffffu, vp, 2);
-                accA[x][y] = va;
-                accP[x][y] = vp;
+                float v = acc[x][y];
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                acc[x][y] = v;
             }
         if (kq == 0 && bc <= br) {
-            const int r0 = 16 * ta + 4 * br, s0 = 16 * ta + 4 * bc;
 #pragma unroll
             for (int x = 0; x < 4; ++x)
 #pragma unroll
-                for (int y = 0; y < 4; ++y) {
-                    const int r = r0 + x, s = s0 + y;
-                    if (s < r) Am[r * LDS + s] = bt[r] * accA[x][y];
-                    if (s <= r) Pm[r * LDS + s] = accP[x][y];
-                }
+                for (int y = 0; y < 4; ++y)
+                    if (s0 + y <= r0 + x) Pm[(r0 + x) * LDS + s0 + y] = acc[x][y];
         }
     }
 
-    // ---- 5. off-diagonal blocks out of TMEM (warps 0-3: k rows -> A, 4-7: q rows -> P)
+    // ---- 6. A and off-diagonal P out of TMEM (warps 0-3: left tile 0, 4-7: tile 1)
     if (!ptx::mbar_wait(bar, 0, WAIT_LIMIT_NS)) *abort_flag = 1;
     ptx::tc_fence_after();
-    {
-        const int lane_row = 32 * (warp & 3) + (tid & 31);  // TMEM lane = tile row
+    if (warp < 8) {
+        const int lane_row = 32 * (warp & 3) + (tid & 31);
+        const int row = (warp < 4 ? 0 : 128) + lane_row;
         const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (warp < 4 ? 0 : 64);
-        float v[64];
+        const int g = group_of(row);
+        const int isP = kGroup[g][0], b = kGroup[g][1];
+        const int r = kGroup[g][2] + (row - kGroup[g][3]);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-            float part[16];
-            tmem_ld16(taddr + 16 * q4, part);
+            float v[16];
+            tmem_ld16(taddr + 16 * q4, v);  // columns s = 16 q4 .. 16 q4 + 15
+            if (q4 == b && !*abort_flag) {
+                if (isP) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[16 * q4 + j] = part[j];
-        }
-        if (lane_row < 96 && !*abort_flag) {
-            const int p = lane_row >> 4, rl = lane_row & 15;
-            const int r = 16 * kPairA[p] + rl, sb0 = 16 * kPairB[p];
-            if (warp < 4) {
-                const float be = bt[r];
+                    for (int j = 0; j < 16; ++j) Pm[r * LDS + 16 * b + j] = v[j];
+                } else {
+                    const float be = bt[r];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    // the pair's columns sit at [16 b, 16 b + 16) of the 64
-                    float val = 0.f;
-#pragma unroll
-                    for (int bb = 0; bb < 3; ++bb)
-                        if (kPairB[p] == bb) val = v[16 * bb + j];
-                    Am[r * LDS + sb0 + j] = be * val;
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    float val = 0.f;
-#pragma unroll
-                    for (int bb = 0; bb < 3; ++bb)
-                        if (kPairB[p] == bb) val = v[16 * bb + j];
-                    Pm[r * LDS + sb0 + j] = val;
+                    for (int j = 0; j < 16; ++j)
+                        if (16 * b + j < r) Am[r * LDS + 16 * b + j] = be * v[j];
                 }
             }
         }
@@ -369,7 +380,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
         else reinterpret_cast<uint4*>(sb + S_RT)[idx] = make_uint4(0, 0, 0, 0);
     }
 
-    // ---- 6. X = (I + A)^{-1}: diagonal 16 x 16 inverses by forward substitution
+    // ---- 7. X = (I + A)^{-1}: diagonal 16 x 16 inverses by forward substitution
     for (int idx = tid; idx < C * LDS; idx += PT) Xm[idx] = 0.f;
     __syncthreads();
     if (tid < 64) {
@@ -387,27 +398,23 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
         for (int r = 0; r < 16; ++r) Xm[(o + r) * LDS + o + j] = x[r];
     }
     __syncthreads();
-    // off-diagonal blocks, one diagonal at a time:
-    //   X_ab = -X_aa * sum_{k=b}^{a-1} A_ak X_kb
-    // Am's upper-right 16x16 blocks are zero and unused by the solve; they
-    // hold the temporaries M_ab = sum_k A_ak X_kb at block (b, a).
+    // off-diagonal blocks, one diagonal at a time: X_ab = -X_aa sum_{k=b}^{a-1} A_ak X_kb.
+    // The temporaries M_ab live in A's unused upper-right block (b, a).
     for (int d = 1; d < 4; ++d) {
         const int nblk = 4 - d;
         for (int idx = tid; idx < nblk * 256; idx += PT) {
-            const int bidx = idx >> 8, e = idx & 255;
-            const int b = bidx, ab = bidx + d;
+            const int b = idx >> 8, e = idx & 255, ab = b + d;
             const int r = e >> 4, cc = e & 15;
             float acc = 0.f;
             for (int kb = b; kb < ab; ++kb)
 #pragma unroll
                 for (int s = 0; s < 16; ++s)
                     acc = fmaf(Am[(16 * ab + r) * LDS + 16 * kb + s], Xm[(16 * kb + s) * LDS + 16 * b + cc], acc);
-            Am[(16 * b + r) * LDS + 16 * ab + cc] = acc;  // temporary in the unused upper block
+            Am[(16 * b + r) * LDS + 16 * ab + cc] = acc;
         }
         __syncthreads();
         for (int idx = tid; idx < nblk * 256; idx += PT) {
-            const int bidx = idx >> 8, e = idx & 255;
-            const int b = bidx, ab = bidx + d;
+            const int b = idx >> 8, e = idx & 255, ab = b + d;
             const int r = e >> 4, cc = e & 15;
             float acc = 0.f;
 #pragma unroll
@@ -417,33 +424,29 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
         }
         __syncthreads();
     }
-
     cp_async_wait_all();
     __syncthreads();
 
-    // ---- 7. operands of W^T and U0^T (the left tiles are dead: reuse their space)
+    // ---- 8. operands of W^T and U0^T (fp16; the left tiles are dead, reuse their space)
     //   TT[r][s] = X[r][s] beta_s ; KPT[key][s] = k_s e^{G_s} ; VT[val][s] = v_s
-    for (int idx = tid; idx < C * 8; idx += PT) {           // TT: 64 rows x 8 chunks
+    for (int idx = tid; idx < C * 8; idx += PT) {
         const int r = idx >> 3, ch = idx & 7;
         float v[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int s = ch * 8 + e;
-            v[e] = Xm[r * LDS + s] * bt[s];
-        }
-        *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, ch * 8, C)) = pack8_f16(v);
+        for (int e = 0; e < 8; ++e) v[e] = Xm[r * LDS + 8 * ch + e] * bt[8 * ch + e];
+        *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 8 * ch, C)) = pack8_f16(v);
     }
-    for (int idx = tid; idx < D * 8; idx += PT) {           // KPT, VT: 128 rows x 8 chunks of 8 tokens
+    for (int idx = tid; idx < D * 8; idx += PT) {
         const int row = idx & 127, ch = idx >> 7;
         float vk[8], vv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const int s = ch * 8 + e;
+            const int s = 8 * ch + e;
             vk[e] = __half2float(KH[s * D + row]) * __expf(G[s * D + row]);
             vv[e] = __half2float(VH[s * D + row]);
         }
-        *reinterpret_cast<uint4*>(sb + S_KPT + sw128_off(row, ch * 8, 128)) = pack8_f16(vk);
-        *reinterpret_cast<uint4*>(sb + S_VT + sw128_off(row, ch * 8, 128)) = pack8_f16(vv);
+        *reinterpret_cast<uint4*>(sb + S_KPT + sw128_off(row, 8 * ch, 128)) = pack8_f16(vk);
+        *reinterpret_cast<uint4*>(sb + S_VT + sw128_off(row, 8 * ch, 128)) = pack8_f16(vv);
     }
     ptx::fence_async_smem();
     ptx::tc_fence_before();
@@ -455,24 +458,23 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
             const uint64_t bT = ptx::sdesc_sw128(base + S_TT + kk * 32);
             const uint64_t aK = ptx::sdesc_sw128(base + S_KPT + kk * 32);
             const uint64_t aV = ptx::sdesc_sw128(base + S_VT + kk * 32);
-            ptx::mma_f16(tmem + 128, aK, bT, IDESC_N64, kk > 0);
-            ptx::mma_f16(tmem + 192, aV, bT, IDESC_N64, kk > 0);
+            ptx::mma_f16(tmem + 128, aK, bT, IDESC_F16_N64, kk > 0);
+            ptx::mma_f16(tmem + 192, aV, bT, IDESC_F16_N64, kk > 0);
         }
         ptx::mma_commit(bar);
     }
 
     unsigned char* rec = static_cast<unsigned char*>(a.records) + ((size_t)chunk * H + h) * REC_BYTES;
 
-    // ---- 8. tiles that need no MMA: Q+ [tok][key], Kt^T [key][tok], P [r][s], decay
+    // ---- 9. tiles that need no MMA, straight to the record: Q+ [tok][key], Kt^T [key][tok], P, decay
     for (int idx = tid; idx < C * 16; idx += PT) {
         const int r = idx >> 4, ch = idx & 15;
-        float v[8];
+        float q8[8], g8[8], v[8];
+        lds_h8(QH + r * D + 8 * ch, q8);
+        lds_f8(G + r * D + 8 * ch, g8);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int i = ch * 8 + e;
-            v[e] = __half2float(QH[r * D + i]) * __expf(G[r * D + i]);
-        }
-        *reinterpret_cast<uint4*>(rec + REC_Q + sw128_off(r, ch * 8, C)) = pack8_f16(v);
+        for (int e = 0; e < 8; ++e) v[e] = q8[e] * __expf(g8[e]);
+        *reinterpret_cast<uint4*>(rec + REC_Q + sw128_off(r, 8 * ch, C)) = pack8_f16(v);
     }
     for (int idx = tid; idx < D * 8; idx += PT) {
         const int key = idx & 127, ch = idx >> 7;
@@ -480,44 +482,48 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
         float v[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const int s = ch * 8 + e;
+            const int s = 8 * ch + e;
             v[e] = __half2float(KH[s * D + key]) * __expf(glast - G[s * D + key]);
         }
-        *reinterpret_cast<uint4*>(rec + REC_KT + sw128_off(key, ch * 8, 128)) = pack8_f16(v);
+        *reinterpret_cast<uint4*>(rec + REC_KT + sw128_off(key, 8 * ch, 128)) = pack8_f16(v);
     }
     for (int idx = tid; idx < C * 8; idx += PT) {
         const int r = idx >> 3, ch = idx & 7;
         float v[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = Pm[r * LDS + ch * 8 + e];
-        *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, ch * 8, C)) = pack8_f16(v);
+        for (int e = 0; e < 8; ++e) v[e] = Pm[r * LDS + 8 * ch + e];
+        *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 8 * ch, C)) = pack8_f16(v);
     }
     if (tid < D) reinterpret_cast<float*>(rec + REC_DECAY)[tid] = expf(G[(C - 1) * D + tid]);
 
-    // ---- 9. W and U0^T out of TMEM: warps 0-3 hold W^T (lane = key), 4-7 U0^T (lane = value)
+    // ---- 10. W^T (warps 0-3, lane = key) through a shared-memory W tile; U0^T (warps 4-7, lane = value) direct
     if (!ptx::mbar_wait(bar, 1, WAIT_LIMIT_NS)) *abort_flag = 1;
     ptx::tc_fence_after();
-    {
+    if (warp < 8) {
         const int row = 32 * (warp & 3) + (tid & 31);
         const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (warp < 4 ? 128 : 192);
 #pragma unroll 1
         for (int q4 = 0; q4 < 4; ++q4) {
             float v[16];
             tmem_ld16(taddr + 16 * q4, v);
-            if (*abort_flag) continue;
             if (warp < 4) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    *reinterpret_cast<__half*>(rec + REC_W + sw128_off(16 * q4 + j, row, C)) = __float2half_rn(v[j]);
-            } else {
+                    *reinterpret_cast<__half*>(sb + S_RT + sw128_off(16 * q4 + j, row, C)) = __float2half_rn(v[j]);
+            } else if (!*abort_flag) {
                 *reinterpret_cast<uint4*>(rec + REC_UT + sw128_off(row, 16 * q4, 128)) = pack8_f16(v);
                 *reinterpret_cast<uint4*>(rec + REC_UT + sw128_off(row, 16 * q4 + 8, 128)) = pack8_f16(v + 8);
             }
         }
     }
-    if (tid == 0 && *abort_flag) atomicExch(a.status, ERR_TIMEOUT);
     ptx::tc_fence_before();
     __syncthreads();
+    if (!*abort_flag) {
+        for (int idx = tid; idx < 1024; idx += PT)  // the 16 KiB W image, 16 bytes per thread step
+            reinterpret_cast<uint4*>(rec + REC_W)[idx] = reinterpret_cast<const uint4*>(sb + S_RT)[idx];
+    } else if (tid == 0) {
+        atomicExch(a.status, ERR_TIMEOUT);
+    }
     if (warp == 0) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
