@@ -90,7 +90,8 @@ WsLayout layout(const kda_params* p, Algo algo, int32_t n_seqs, int64_t T, int64
     L.vh = off; off = align_up(off + op * (size_t)T * W, WS_ALIGN);
     L.g = off; off = align_up(off + 4 * (size_t)T * W, WS_ALIGN);
     L.beta = off; off = align_up(off + 4 * (size_t)T * p->num_heads, WS_ALIGN);
-    L.ocore = off; off = align_up(off + 4 * (size_t)T * W, WS_ALIGN);
+    L.ocore = off;  // o_core: only the scan path has a separate output stage
+    if (algo == Algo::Scan) off = align_up(off + 4 * (size_t)T * W, WS_ALIGN);
     L.rec = off;
     if (algo == Algo::Chunked) off = align_up(off + (size_t)REC_BYTES * (size_t)n_chunks * p->num_heads, WS_ALIGN);
     L.total = off;
@@ -243,14 +244,18 @@ kda_status prefill_impl(const kda_params* p, const void* q, const void* k, const
                     reinterpret_cast<int32_t*>(ws + L.status)};
         e = launch_chunk_prep(pr, s);
         if (e != cudaSuccess) return KDA_ERR_CUDA;
-        ChunkRecArgs ca{ws + L.rec, S_in, S_out, ocore, d_cu, d_coff, d_order,
+        // the recurrence kernel applies the output norm itself
+        ChunkRecArgs ca{ws + L.rec, S_in, S_out, gout, p->norm_w, o, p->norm_eps, d_cu, d_coff, d_order,
                         reinterpret_cast<int32_t*>(ws + L.status), n_seqs, H};
         e = launch_chunk_recurrence(ca, s);
         if (e != cudaSuccess || mark(ev, 2, s) != cudaSuccess) return KDA_ERR_CUDA;
     }
-    EpilogueArgs ea{ocore, gout, p->norm_w, o, total_tokens, H, p->norm_eps};
-    e = launch_epilogue(ea, io_bf16, s);
-    if (e != cudaSuccess || mark(ev, 3, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (algo == Algo::Scan) {
+        EpilogueArgs ea{ocore, gout, p->norm_w, o, total_tokens, H, p->norm_eps};
+        e = launch_epilogue(ea, io_bf16, s);
+        if (e != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    if (mark(ev, 3, s) != cudaSuccess) return KDA_ERR_CUDA;
     if (ring_out) {
         RingArgs ra{q, k, v, ring_in, ring_out, d_cu, n_seqs, W};
         e = launch_ring_update(ra, io_bf16, s);

@@ -1,7 +1,7 @@
 // Chunk recurrence of the chunked prefill on the 5th-generation tensor cores
-// (tcgen05, accumulators in tensor memory).  One CTA per (sequence, head)
-// walks the sequence's 64-token chunks in order; the 128 x 128 fp32 state
-// never leaves the SM.
+// (tcgen05, accumulators in tensor memory), with the RMSNormGated output stage
+// fused in.  One CTA per (sequence, head) walks the sequence's 64-token chunks
+// in order; the 128 x 128 fp32 state never leaves the SM.
 //
 // Per chunk, with the operands prepared by the chunk-preparation kernel
 // (W, Q+, Kt, U0, P, decay; see kda_chunk_prep.cu) and S the state at the
@@ -10,31 +10,46 @@
 //   U   = U0 - W S
 //   O   = Q+ S + P U
 //   S'  = Diag(decay) S + Kt^T U
+// and then o = O / sqrt(mean_i O^2 + eps) * w * sigmoid(gout) per token
+// ("Kimi Delta Attention (KDA) -- analysis & C kernel plan", section "The
+// KDA layer, precisely": RMSNormGated with a sigmoid gate).
+//
 // Everything is computed transposed so that every MMA has M = 128 (the value
 // dimension) and the state lives in TMEM as S^T (lane = value index, column
 // = key index):
-//   MMA1  D[:, 0:64]   = S^T W^T           (A = S^T fp16 copy, B = W)
-//         D[:, 64:128] = S^T Q+^T          (B = Q+)
-//   SIMT  U^T = U0^T - D[:, 0:64]  -> fp16 tile
-//   MMA2  S^T += U^T Kt                     (onto the decayed state, B = Kt^T tile)
-//   MMA3  D[:, 64:128] += U^T P^T           (B = P)
-//   SIMT  O^T = D[:, 64:128] -> o_core ; S^T -> fp16 copy, scaled by next decay
-// Each chunk's record arrives with one bulk copy into a two-stage ring, two
-// chunks ahead of use.  Every wait is bounded; on timeout the kernel records
-// KDA timeout in the workspace status word, drains its own copies and
-// returns after freeing its tensor memory.
+//   MMA1  D[b][:, 0:64]   = S^T W^T          (A = S^T fp16 copy, B = W)
+//         D[b][:, 64:128] = S^T Q+^T         (B = Q+)
+//   SIMT  U^T = U0^T - D[b][:, 0:64]  -> fp16 tile
+//   MMA2  S^T += U^T Kt                    (onto the decayed state, B = Kt^T tile)
+//   MMA3  D[b][:, 64:128] += U^T P^T       (B = P)
+//   SIMT  S^T -> fp16 copy, S^T *= next decay
+// Warp roles: warps 0-7 run this serial chain (each step split over two warps
+// per TMEM lane quarter); warps 8-15 (two per lane quarter, 32 tokens each)
+// take O^T of the chunk out of TMEM buffer b and apply the output norm while
+// the chain moves on (three D buffers: the chain may run two chunks ahead).
+// O passes through a shared-memory tile, 32 tokens at a time, so that each
+// token row is normalised by the 8 threads holding it and the gate logits
+// are read and the output written as whole 16-byte row segments.  Each chunk's record arrives with one bulk
+// copy into a two-stage ring, two chunks ahead of use.  Every wait is
+// bounded; on timeout the kernel records the timeout in the workspace status
+// word, drains its own copies and MMAs and returns after freeing its tensor
+// memory.
 #include "kda_chunk_layout.cuh"
 #include "tc_ptx.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int NT = 128;                 // 4 warps: thread t <-> TMEM lane t <-> value index t
-constexpr uint32_t TMEM_COLS = 256;     // [0,128) state S^T, [128,256) D
-constexpr uint32_t STAGE_STRIDE = 75776;  // REC_BYTES rounded up to 1 KiB
+constexpr int NT = 512;                    // 16 warps: 8 state-chain warps + 8 output warps
+constexpr int NSTATE = 256;                // threads of the state chain
+constexpr uint32_t TMEM_COLS = 512;        // [0,128) S^T, then D[0], D[1], D[2] (128 columns each)
+constexpr int NBUF = 3;                    // D buffers: the chain may run two chunks ahead of the output
+constexpr uint32_t STAGE_STRIDE = 75776;   // REC_BYTES rounded up to 1 KiB
 constexpr uint32_t OFF_ST = 2 * STAGE_STRIDE;      // S^T fp16, 2 panels x 128 rows x 128 B
 constexpr uint32_t OFF_UT = OFF_ST + 32768;        // U^T fp16, 1 panel x 128 rows x 128 B
-constexpr uint32_t OFF_BAR = OFF_UT + 16384;       // 3 mbarriers + TMEM slot + flags
+constexpr int LDYS = 132;                          // padded row stride of the output tile
+constexpr uint32_t OFF_Y = OFF_UT + 16384;         // fp32 [32 tok][132] output of half a chunk
+constexpr uint32_t OFF_BAR = OFF_Y + 32 * LDYS * 4; // mbarriers + TMEM slot + flags
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 128 + 1024;  // + slack for 1 KiB alignment
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 
@@ -49,18 +64,40 @@ __device__ __forceinline__ uint4 pack8_f16(const float* v) {
     return u;
 }
 
+// named barrier over `count` threads (ids 1 and 2; id 0 is __syncthreads)
+__device__ __forceinline__ void bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+template <typename TO>
 __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char* sb = smem_raw + (base - raw);
-    const uint32_t bar_load[2] = {base + OFF_BAR, base + OFF_BAR + 8};
-    const uint32_t bar_mma = base + OFF_BAR + 16;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sb + OFF_BAR + 32);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sb + OFF_BAR + 36);
-    int* pend = reinterpret_cast<int*>(sb + OFF_BAR + 40);  // [0],[1] load pending per stage, [2] mma pending
+    const uint32_t bar_load0 = base + OFF_BAR;           // + 8 * stage
+    const uint32_t bar_mma1 = base + OFF_BAR + 16;       // MMA1 of a chunk finished
+    // MMA2/3 of a chunk finished, one barrier per D buffer: the output warps
+    // can then lag the chain by a chunk without two phases of one barrier
+    // completing between their waits
+    const uint32_t bar_mma23_0 = base + OFF_BAR + 24;    // + 8 * buffer (3)
+    const uint32_t bar_ofree0 = base + OFF_BAR + 48;     // + 8 * buffer (3): D[b] read by the output warps
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sb + OFF_BAR + 72);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sb + OFF_BAR + 76);
+    // in-flight bookkeeping for the drain after a timeout (thread 0 only):
+    // [0],[1] load pending per stage and [2],[3] its parity; [4] MMA commit pending
+    // (barrier address), [5] its parity
+    int* pend = reinterpret_cast<int*>(sb + OFF_BAR + 80);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, W = H * D;
     const int n = a.seq_order ? a.seq_order[blockIdx.x / H] : (int)(blockIdx.x / H);
     const int h = blockIdx.x % H;
@@ -73,173 +110,248 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
         ptx::tmem_relinquish();
     }
     if (tid == 0) {
-        ptx::mbar_init(bar_load[0], 1);
-        ptx::mbar_init(bar_load[1], 1);
-        ptx::mbar_init(bar_mma, 1);
+        ptx::mbar_init(bar_load0, 1);
+        ptx::mbar_init(bar_load0 + 8, 1);
+        ptx::mbar_init(bar_mma1, 1);
+        for (int b = 0; b < NBUF; ++b) {
+            ptx::mbar_init(bar_mma23_0 + 8 * b, 1);
+            ptx::mbar_init(bar_ofree0 + 8 * b, 1);
+        }
         *abort_flag = 0;
-        pend[0] = pend[1] = pend[2] = 0;
+        for (int i = 0; i < 6; ++i) pend[i] = 0;
         ptx::fence_mbar_init();
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane = (uint32_t)(warp * 32) << 16;
-    const uint32_t tS = tmem + lane;         // this warp's lanes, state columns
-    const uint32_t tD = tmem + lane + 128;   // this warp's lanes, D columns
+    const int quarter = warp & 3;                        // TMEM lane quarter of this warp
+    const int vrow = 32 * quarter + lane;                // value index = TMEM lane
+    const uint32_t tlane = tmem + ((uint32_t)(32 * quarter) << 16);
 
     const unsigned char* recs = static_cast<const unsigned char*>(a.records);
     auto issue_load = [&](int64_t c) {
         const int s = (int)(c & 1);
-        ptx::mbar_expect_tx(bar_load[s], REC_BYTES);
+        ptx::mbar_expect_tx(bar_load0 + 8 * s, REC_BYTES);
         ptx::bulk_g2s(base + s * STAGE_STRIDE, recs + ((size_t)(c0 + c) * H + h) * REC_BYTES, REC_BYTES,
-                      bar_load[s]);
+                      bar_load0 + 8 * s);
         pend[s] = 1;
+        pend[2 + s] = (int)((c >> 1) & 1);
     };
-    if (tid == 0) {
-        for (int64_t c = 0; c < nc && c < 2; ++c) issue_load(c);
-    }
-
-    // initial state: S^T into TMEM (thread t holds value column t, all keys)
     const size_t soff = ((size_t)n * H + h) * D * D;
-#pragma unroll 1
-    for (int j = 0; j < 4; ++j) {
-        float v[32];
-#pragma unroll
-        for (int x = 0; x < 32; ++x) v[x] = a.S_in ? a.S_in[soff + (size_t)(32 * j + x) * D + tid] : 0.f;
-        ptx::tmem_st32(tS + 32 * j, v);
-    }
 
-    uint32_t mma_phase = 0;
-    uint32_t load_phase[2] = {0, 0};
-    float* o_core = a.o_core;
-#pragma unroll 1
-    for (int64_t c = 0; c < nc; ++c) {
-        const int s = (int)(c & 1);
-        const uint32_t stg = base + s * STAGE_STRIDE;
-        const unsigned char* sp = sb + s * STAGE_STRIDE;
-        const int64_t rem = L - (int64_t)CHUNK_T * c;
-        const int Lc = rem < CHUNK_T ? (int)rem : CHUNK_T;
-
-        if (!ptx::mbar_wait(bar_load[s], load_phase[s], WAIT_LIMIT_NS)) *abort_flag = 1;
-        __syncthreads();
-        if (*abort_flag) break;
-        load_phase[s] ^= 1;
-        if (tid == 0) pend[s] = 0;
-
-        // ---- state transition: fp16 copy of S^T for MMA1, then S^T *= decay (per key column)
-        const float* decay = reinterpret_cast<const float*>(sp + REC_DECAY);
-#pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
-            float v[32];
-            ptx::tmem_ld32(tS + 32 * j, v);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4*>(sb + OFF_ST + sw128_off(tid, 32 * j + 8 * q, 128)) = pack8_f16(v + 8 * q);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) v[x] *= decay[32 * j + x];
-            ptx::tmem_st32(tS + 32 * j, v);
-        }
-        ptx::fence_async_smem();
-        ptx::tc_fence_before();
-        __syncthreads();
+    if (warp < 8) {
+        // ============================ state chain ============================
+        const int half = warp >> 2;  // which half of the columns this warp handles
         if (tid == 0) {
-            ptx::tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t koff = (kk & 3) * 32;  // 16 fp16 of K inside the 128-byte row
-                const uint64_t ad = ptx::sdesc_sw128(base + OFF_ST + (kk >> 2) * 16384 + koff);
-                const uint64_t bw = ptx::sdesc_sw128(stg + REC_W + (kk >> 2) * 8192 + koff);
-                const uint64_t bq = ptx::sdesc_sw128(stg + REC_Q + (kk >> 2) * 8192 + koff);
-                ptx::mma_f16(tmem + 128, ad, bw, IDESC_N64, kk > 0);
-                ptx::mma_f16(tmem + 192, ad, bq, IDESC_N64, kk > 0);
-            }
-            ptx::mma_commit(bar_mma);
-            pend[2] = 1;
+            for (int64_t c = 0; c < nc && c < 2; ++c) issue_load(c);
         }
-        if (!ptx::mbar_wait(bar_mma, mma_phase, WAIT_LIMIT_NS)) *abort_flag = 1;
-        __syncthreads();
-        if (*abort_flag) break;
-        mma_phase ^= 1;
-        if (tid == 0) pend[2] = 0;
-        ptx::tc_fence_after();
-
-        // ---- U^T = U0^T - (W S)^T, as the fp16 A operand of MMA2 / MMA3
+        // initial state: S^T into TMEM (thread holds value column vrow, keys of its half)
 #pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 2 * half; j < 2 * half + 2; ++j) {
             float v[32];
-            ptx::tmem_ld32(tD + 32 * j, v);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint32_t off = sw128_off(tid, 32 * j + 8 * q, 128);
-                const uint4 u0 = *reinterpret_cast<const uint4*>(sp + REC_UT + off);
-                const __half2* p = reinterpret_cast<const __half2*>(&u0);
-                float u[8];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __half22float2(p[e]);
-                    u[2 * e] = f.x - v[8 * q + 2 * e];
-                    u[2 * e + 1] = f.y - v[8 * q + 2 * e + 1];
-                }
-                *reinterpret_cast<uint4*>(sb + OFF_UT + off) = pack8_f16(u);
-            }
+            for (int x = 0; x < 32; ++x) v[x] = a.S_in ? a.S_in[soff + (size_t)(32 * j + x) * D + vrow] : 0.f;
+            ptx::tmem_st32(tlane + 32 * j, v);
         }
-        ptx::fence_async_smem();
-        ptx::tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            ptx::tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t au = ptx::sdesc_sw128(base + OFF_UT + kk * 32);
-                const uint64_t bk = ptx::sdesc_sw128(stg + REC_KT + kk * 32);
-                const uint64_t bp = ptx::sdesc_sw128(stg + REC_P + kk * 32);
-                ptx::mma_f16(tmem, au, bk, IDESC_N128, 1);
-                ptx::mma_f16(tmem + 192, au, bp, IDESC_N64, 1);
-            }
-            ptx::mma_commit(bar_mma);
-            pend[2] = 1;
-        }
-        if (!ptx::mbar_wait(bar_mma, mma_phase, WAIT_LIMIT_NS)) *abort_flag = 1;
-        __syncthreads();
-        if (*abort_flag) break;
-        mma_phase ^= 1;
-        if (tid == 0) pend[2] = 0;
-        ptx::tc_fence_after();
-
-        // ---- O^T -> o_core (lanes are consecutive value columns: coalesced)
-        float* orow = o_core + (size_t)(bos + CHUNK_T * c) * W + (size_t)h * D + tid;
 #pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-            float v[32];
-            ptx::tmem_ld32(tD + 64 + 32 * j, v);
+        for (int64_t c = 0; c < nc; ++c) {
+            const int s = (int)(c & 1);
+            const int buf = (int)(c % NBUF);
+            const uint32_t use = (uint32_t)((c / NBUF) & 1);  // parity of this use of D[buf]
+            const uint32_t stg = base + s * STAGE_STRIDE;
+            const unsigned char* sp = sb + s * STAGE_STRIDE;
+            const uint32_t dcol = 128 + 128 * buf;       // D[buf] column offset
+
+            // stage s is used by chunks s, s+2, ...: this is its use number c >> 1
+            if (!ptx::mbar_wait(bar_load0 + 8 * s, (uint32_t)((c >> 1) & 1), WAIT_LIMIT_NS)) *abort_flag = 1;
+            bar_sync(1, NSTATE);
+            if (*abort_flag) break;
+            if (tid == 0) pend[s] = 0;
+
+            // ---- state transition: fp16 copy of S^T for MMA1, then S^T *= decay (per key column)
+            const float* decay = reinterpret_cast<const float*>(sp + REC_DECAY);
+#pragma unroll 1
+            for (int j = 2 * half; j < 2 * half + 2; ++j) {
+                float v[32];
+                ptx::tmem_ld32(tlane + 32 * j, v);
 #pragma unroll
-            for (int x = 0; x < 32; ++x)
-                if (32 * j + x < Lc) orow[(size_t)(32 * j + x) * W] = v[x];
-        }
-        ptx::tc_fence_before();
-        __syncthreads();
-        if (tid == 0 && c + 2 < nc) {
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4*>(sb + OFF_ST + sw128_off(vrow, 32 * j + 8 * q, 128)) = pack8_f16(v + 8 * q);
+#pragma unroll
+                for (int x = 0; x < 32; ++x) v[x] *= decay[32 * j + x];
+                ptx::tmem_st32(tlane + 32 * j, v);
+            }
             ptx::fence_async_smem();
-            issue_load(c + 2);
+            ptx::tc_fence_before();
+            bar_sync(1, NSTATE);
+            if (tid == 0) {
+                // D[buf] must have been read out by the output warps (chunk c - NBUF)
+                bool ok = true;
+                if (c >= NBUF) ok = ptx::mbar_wait(bar_ofree0 + 8 * buf, use ^ 1u, WAIT_LIMIT_NS);
+                if (!ok) {
+                    *abort_flag = 1;
+                } else {
+                    ptx::tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t koff = (kk & 3) * 32;  // 16 fp16 of K inside the 128-byte row
+                        const uint64_t ad = ptx::sdesc_sw128(base + OFF_ST + (kk >> 2) * 16384 + koff);
+                        const uint64_t bw = ptx::sdesc_sw128(stg + REC_W + (kk >> 2) * 8192 + koff);
+                        const uint64_t bq = ptx::sdesc_sw128(stg + REC_Q + (kk >> 2) * 8192 + koff);
+                        ptx::mma_f16(tmem + dcol, ad, bw, IDESC_N64, kk > 0);
+                        ptx::mma_f16(tmem + dcol + 64, ad, bq, IDESC_N64, kk > 0);
+                    }
+                    ptx::mma_commit(bar_mma1);
+                    pend[4] = (int)bar_mma1;
+                    pend[5] = (int)(c & 1);
+                }
+            }
+            // the abort flag (set by thread 0 above) is checked after this wait and barrier
+            if (!*abort_flag && !ptx::mbar_wait(bar_mma1, (uint32_t)(c & 1), WAIT_LIMIT_NS)) *abort_flag = 1;
+            bar_sync(1, NSTATE);
+            if (*abort_flag) break;
+            if (tid == 0) pend[4] = 0;
+            ptx::tc_fence_after();
+
+            // ---- U^T = U0^T - (W S)^T as the fp16 A operand of MMA2 / MMA3 (this warp: 32 tokens)
+            {
+                float v[32];
+                ptx::tmem_ld32(tlane + dcol + 32 * half, v);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t off = sw128_off(vrow, 32 * half + 8 * q, 128);
+                    const uint4 u0 = *reinterpret_cast<const uint4*>(sp + REC_UT + off);
+                    const __half2* p = reinterpret_cast<const __half2*>(&u0);
+                    float u[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __half22float2(p[e]);
+                        u[2 * e] = f.x - v[8 * q + 2 * e];
+                        u[2 * e + 1] = f.y - v[8 * q + 2 * e + 1];
+                    }
+                    *reinterpret_cast<uint4*>(sb + OFF_UT + off) = pack8_f16(u);
+                }
+            }
+            ptx::fence_async_smem();
+            ptx::tc_fence_before();
+            bar_sync(1, NSTATE);
+            if (tid == 0) {
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t au = ptx::sdesc_sw128(base + OFF_UT + kk * 32);
+                    const uint64_t bk = ptx::sdesc_sw128(stg + REC_KT + kk * 32);
+                    const uint64_t bp = ptx::sdesc_sw128(stg + REC_P + kk * 32);
+                    ptx::mma_f16(tmem, au, bk, IDESC_N128, 1);
+                    ptx::mma_f16(tmem + dcol + 64, au, bp, IDESC_N64, 1);
+                }
+                ptx::mma_commit(bar_mma23_0 + 8 * buf);
+                pend[4] = (int)(bar_mma23_0 + 8 * buf);
+                pend[5] = (int)use;
+            }
+            if (!ptx::mbar_wait(bar_mma23_0 + 8 * buf, use, WAIT_LIMIT_NS)) *abort_flag = 1;
+            bar_sync(1, NSTATE);
+            if (*abort_flag) break;
+            ptx::tc_fence_after();
+            if (tid == 0) {
+                pend[4] = 0;
+                if (c + 2 < nc) {
+                    ptx::fence_async_smem();
+                    issue_load(c + 2);
+                }
+            }
+        }
+        if (!*abort_flag) {
+            // final state: S_out[key][value] = S^T[value][key]
+#pragma unroll 1
+            for (int j = 2 * half; j < 2 * half + 2; ++j) {
+                float v[32];
+                ptx::tmem_ld32(tlane + 32 * j, v);
+#pragma unroll
+                for (int x = 0; x < 32; ++x) a.S_out[soff + (size_t)(32 * j + x) * D + vrow] = v[x];
+            }
+        }
+    } else {
+        // ============================ output warps ===========================
+        // Per chunk: O^T (lane = value) -> fp32 tile [32 tokens][128 values],
+        // one token half at a time; then 8 threads per token row: sum of O^2
+        // (3 shuffles), o = O * rsqrt(mean + eps) * w * sigmoid(gout).
+        const int ow = warp - 8;                       // 0..7
+        const int th = ow >> 2;                        // the token half this warp's TMEM columns hold
+        const int otid = tid - NSTATE;                 // 0..255
+        const int rt = otid >> 3, rseg = otid & 7;     // row pass: token rt of the half, values 16 rseg .. +15
+        const TO* gout = static_cast<const TO*>(a.gout);
+        TO* out = static_cast<TO*>(a.o);
+        float* ys = reinterpret_cast<float*>(sb + OFF_Y);
+        float wv[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) wv[e] = a.norm_w[16 * rseg + e];
+#pragma unroll 1
+        for (int64_t c = 0; c < nc; ++c) {
+            const int buf = (int)(c % NBUF);
+            const uint32_t use = (uint32_t)((c / NBUF) & 1);
+            const int64_t rem = L - (int64_t)CHUNK_T * c;
+            const int Lc = rem < CHUNK_T ? (int)rem : CHUNK_T;
+            const size_t row0 = (size_t)(bos + (int64_t)CHUNK_T * c);
+            if (!ptx::mbar_wait(bar_mma23_0 + 8 * buf, use, WAIT_LIMIT_NS)) *abort_flag = 1;
+            bar_sync(2, 256);
+            if (*abort_flag) break;
+            ptx::tc_fence_after();
+            float o[32];
+            ptx::tmem_ld32(tlane + 128 + 128 * buf + 64 + 32 * th, o);
+            // D[buf] is no longer needed: MMA1 of chunk c + NBUF may overwrite it
+            ptx::tc_fence_before();
+            bar_sync(2, 256);
+            if (otid == 0) mbar_arrive(bar_ofree0 + 8 * buf);
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                const int t = 32 * half + rt;          // token of this thread's row pass
+                uint4 g2[2];
+                const size_t roff = (row0 + t) * W + (size_t)h * D + 16 * rseg;
+                if (t < Lc) {
+                    g2[0] = __ldg(reinterpret_cast<const uint4*>(gout + roff));
+                    g2[1] = __ldg(reinterpret_cast<const uint4*>(gout + roff) + 1);
+                }
+                if (th == half) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ys[j * LDYS + vrow] = o[j];
+                }
+                bar_sync(2, 256);
+                float y[16];
+                lds8(ys + rt * LDYS + 16 * rseg, *reinterpret_cast<float(*)[8]>(y));
+                lds8(ys + rt * LDYS + 16 * rseg + 8, *reinterpret_cast<float(*)[8]>(y + 8));
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) ss = fmaf(y[e], y[e], ss);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+                const float rs = rsqrtf(ss * (1.0f / D) + a.eps);
+                if (t < Lc) {
+                    float g16[16], r[16];
+                    const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(g2);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float2 gf = __bfloat1622float2(gh[e]);
+                        g16[2 * e] = gf.x; g16[2 * e + 1] = gf.y;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r[e] = y[e] * rs * wv[e] * sigmoid_fast(g16[e]);
+                    Vec8<TO>::store(out + roff, *reinterpret_cast<float(*)[8]>(r));
+                    Vec8<TO>::store(out + roff + 8, *reinterpret_cast<float(*)[8]>(r + 8));
+                }
+                bar_sync(2, 256);  // the tile is read before the next half overwrites it
+            }
         }
     }
 
-    if (!*abort_flag) {
-        // final state: S_out[key][value] = S^T[value][key]
-#pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
-            float v[32];
-            ptx::tmem_ld32(tS + 32 * j, v);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) a.S_out[soff + (size_t)(32 * j + x) * D + tid] = v[x];
-        }
-    } else if (tid == 0) {
+    if (*abort_flag && tid == 0) {
         // record the timeout, then let this CTA's own copies and MMAs land
         atomicExch(a.status, ERR_TIMEOUT);
         for (int s = 0; s < 2; ++s)
-            if (pend[s]) ptx::mbar_wait(bar_load[s], load_phase[s], WAIT_LIMIT_NS);
-        if (pend[2]) ptx::mbar_wait(bar_mma, mma_phase, WAIT_LIMIT_NS);
+            if (pend[s]) ptx::mbar_wait(bar_load0 + 8 * s, (uint32_t)pend[2 + s], WAIT_LIMIT_NS);
+        if (pend[4]) ptx::mbar_wait((uint32_t)pend[4], (uint32_t)pend[5], WAIT_LIMIT_NS);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -254,12 +366,12 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
 bool chunked_kernel_built() { return true; }
 
 cudaError_t launch_chunk_recurrence(const ChunkRecArgs& a, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(chunk_recurrence_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+    auto k = chunk_recurrence_kernel<__nv_bfloat16>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int64_t blocks = (int64_t)a.n_seqs * a.H;
     if (blocks == 0) return cudaSuccess;
-    chunk_recurrence_kernel<<<(unsigned)blocks, NT, SMEM_BYTES, s>>>(a);
+    k<<<(unsigned)blocks, NT, SMEM_BYTES, s>>>(a);
     return cudaGetLastError();
 }
 

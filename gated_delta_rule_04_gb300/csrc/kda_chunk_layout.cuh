@@ -48,7 +48,10 @@ struct ChunkRecArgs {
     const void* records;
     const float* S_in;
     float* S_out;
-    float* o_core;
+    const void* gout;          // bf16 [T][H*128] output-gate logits
+    const float* norm_w;       // [128]
+    void* o;                   // bf16 [T][H*128]
+    float eps;                 // RMSNorm eps
     const int64_t* cu;         // [n+1] token offsets
     const int64_t* chunk_off;  // [n+1] first chunk of each sequence
     const int32_t* seq_order;  // [n] sequences by decreasing length (CTA order), or NULL

@@ -64,7 +64,8 @@ NaLayout na_layout(int H, bool chunked, int32_t n, int64_t T, int64_t nc) {
     L.vh = off; off = up(off + op * (size_t)T * W, NA_ALIGN);
     L.g = off; off = up(off + 4 * (size_t)T * W, NA_ALIGN);
     L.beta = off; off = up(off + 4 * (size_t)T * H, NA_ALIGN);
-    L.ocore = off; off = up(off + 4 * (size_t)T * W, NA_ALIGN);
+    L.ocore = off;
+    if (!chunked) off = up(off + 4 * (size_t)T * W, NA_ALIGN);
     L.rec = off;
     if (chunked) off = up(off + (size_t)REC_BYTES * (size_t)nc * H, NA_ALIGN);
     L.total = off;
@@ -184,11 +185,14 @@ extern "C" kda_status kda_prefill_noalloc(const kda_params* p, const void* q, co
         if (launch_prestage(pa, io_bf16, 1, 1, s) != cudaSuccess) return KDA_ERR_CUDA;
         PrepArgs pr{ws + L.qh, ws + L.kh, ws + L.vh, gbuf, beta, d_chunks, (int32_t)nc, H, ws + L.rec, status};
         if (launch_chunk_prep(pr, s) != cudaSuccess) return KDA_ERR_CUDA;
-        ChunkRecArgs ca{ws + L.rec, S_in, S_out, ocore, d_cu, d_coff, d_order, status, n_seqs, H};
+        ChunkRecArgs ca{ws + L.rec, S_in, S_out, gout, p->norm_w, o, p->norm_eps, d_cu, d_coff, d_order, status,
+                        n_seqs, H};
         if (launch_chunk_recurrence(ca, s) != cudaSuccess) return KDA_ERR_CUDA;
     }
-    EpilogueArgs ea{ocore, gout, p->norm_w, o, total_tokens, H, p->norm_eps};
-    if (launch_epilogue(ea, io_bf16, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (!chunked) {
+        EpilogueArgs ea{ocore, gout, p->norm_w, o, total_tokens, H, p->norm_eps};
+        if (launch_epilogue(ea, io_bf16, s) != cudaSuccess) return KDA_ERR_CUDA;
+    }
     if (ring_out) {
         RingArgs ra{q, k, v, ring_in, ring_out, d_cu, n_seqs, W};
         if (launch_ring_update(ra, io_bf16, s) != cudaSuccess) return KDA_ERR_CUDA;

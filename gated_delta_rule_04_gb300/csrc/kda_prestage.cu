@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(PS_THREADS, 2) prestage_kernel(PrestageArgs a,
     TI* xs = reinterpret_cast<TI*>(smem_raw);     // [3][PS_ROWS][D]
     float* tot = reinterpret_cast<float*>(smem_raw + sizeof(TI) * 3 * PS_ROWS * D);  // [16][D]
     float* cw = tot + 16 * D;                     // [3][D][4] conv weights of this head
+    TI* zs = reinterpret_cast<TI*>(cw + 3 * D * CONV_K);  // [PS_MAXLEN][D] gate inputs
 
     const int item = blockIdx.x;
     const int H = a.H, W = H * D;
@@ -71,19 +72,13 @@ __global__ void __launch_bounds__(PS_THREADS, 2) prestage_kernel(PrestageArgs a,
         cp_async16(cw + 4 * idx, a.conv_w + ((size_t)p * W + h * D + c) * CONV_K);
     }
 
-    // gate inputs and per-lane constants, loaded while the copies fly
+    // gate inputs of the chunk's tokens, staged with the same copies
+    for (int idx = tid; idx < len * VPR; idx += PS_THREADS) {
+        const int r = idx / VPR, vv = idx - r * VPR;
+        cp_async16(zs + (size_t)r * D + vv * VEC, static_cast<const TI*>(a.z) + (size_t)(cd.t0 + r) * W + h * D + vv * VEC);
+    }
     const int hw = tid >> 4, l16 = tid & 15;
     const int cb = l16 * 8;                       // first channel (inside the head)
-    float zt[4][8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int tau = hw * 4 + j;
-        if (tau < len) Vec8<TI>::load(static_cast<const TI*>(a.z) + (size_t)(cd.t0 + tau) * W + h * D + cb, zt[j]);
-        else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) zt[j][e] = 0.f;
-        }
-    }
     float dtb[8];
     Vec8<float>::load(a.dt_bias + h * D + cb, dtb);
     const float eA = expf(a.A_log[h]);
@@ -110,9 +105,7 @@ __global__ void __launch_bounds__(PS_THREADS, 2) prestage_kernel(PrestageArgs a,
         for (int r = 0; r < 7; ++r) {
             const int row = hw * 4 + r;
             if (row < rows) {
-                const TI* src = xs + ((size_t)p * PS_ROWS + row) * D + cb;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) win[r][e] = to_f32(src[e]);
+                lds8(xs + ((size_t)p * PS_ROWS + row) * D + cb, win[r]);
             } else {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) win[r][e] = 0.f;
@@ -129,7 +122,7 @@ __global__ void __launch_bounds__(PS_THREADS, 2) prestage_kernel(PrestageArgs a,
                 acc = fmaf(wt[e][1], win[j + 1][e], acc);
                 acc = fmaf(wt[e][2], win[j + 2][e], acc);
                 acc = fmaf(wt[e][3], win[j + 3][e], acc);
-                y[e] = acc / (1.0f + expf(-acc));
+                y[e] = silu_fast(acc);
                 ss = fmaf(y[e], y[e], ss);
             }
             if (p < 2) {
@@ -152,10 +145,11 @@ __global__ void __launch_bounds__(PS_THREADS, 2) prestage_kernel(PrestageArgs a,
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int tau = hw * 4 + j;
+        float z8[8];
+        if (tau < len) lds8(zs + (size_t)tau * D + cb, z8);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            float g = a.lb / (1.0f + expf(-eA * (zt[j][e] + dtb[e])));
-            if (tau >= len) g = 0.f;
+            float g = tau < len ? a.lb * sigmoid_fast(eA * (z8[e] + dtb[e])) : 0.f;
             run[e] += g;
             gv[j][e] = cumsum ? run[e] : g;
         }
@@ -223,7 +217,8 @@ __global__ void ring_update_kernel(RingArgs a) {
 
 template <typename TI, typename TO>
 cudaError_t launch_prestage_t(const PrestageArgs& a, int cumsum, cudaStream_t s) {
-    const size_t smem = sizeof(TI) * 3 * PS_ROWS * D + sizeof(float) * 16 * D + sizeof(float) * 3 * D * CONV_K;
+    const size_t smem = sizeof(TI) * 3 * PS_ROWS * D + sizeof(float) * 16 * D + sizeof(float) * 3 * D * CONV_K +
+                        sizeof(TI) * PS_MAXLEN * D;
     cudaError_t e = cudaFuncSetAttribute(prestage_kernel<TI, TO>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
