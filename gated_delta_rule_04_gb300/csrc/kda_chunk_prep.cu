@@ -55,14 +55,15 @@ constexpr uint32_t S_G = 0;                      // fp32 [64][128] G (rows past 
 constexpr uint32_t S_Y = S_G + 32768;            // fp32 [64][132] Y; later X = (I+A)^{-1} fp32 [64][65]
 constexpr uint32_t S_KH = S_Y + 33792;           // fp16 [64][128] k^ (plain row-major)
 constexpr uint32_t S_QH = S_KH + 16384;          // fp16 [64][128] q^
-constexpr uint32_t S_LAP = S_QH + 16384;         // bf16 2 tiles x [128 rows][128 keys] (swizzled); later KPT/VT/TT
+constexpr uint32_t S_VH = S_QH + 16384;          // fp16 [64][128] v^
+constexpr uint32_t S_LAP = S_VH + 16384;         // bf16 2 tiles x [128 rows][128 keys] (swizzled); later KPT/VT/TT
 constexpr uint32_t S_KPT = S_LAP;                //   fp16 [128 key][64 tok]  (k e^G)^T
 constexpr uint32_t S_VT = S_LAP + 16384;         //   fp16 [128 val][64 tok]  v^T
 constexpr uint32_t S_TT = S_LAP + 32768;         //   fp16 [64 r][64 s]       T
-constexpr uint32_t S_RT = S_LAP + 65536;         // bf16 [64 s][128 keys] k Y (swizzled); later v^ rows, then W
+constexpr uint32_t S_RT = S_LAP + 65536;         // bf16 [64 s][128 keys] k Y (swizzled); later the W tile
 constexpr uint32_t S_AM = S_RT + 16384;          // fp32 [64][65] A (with beta)
-constexpr uint32_t S_PM = S_AM + 64 * LDS * 4;   // fp32 [64][65] P
-constexpr uint32_t S_MT = S_PM + 64 * LDS * 4;   // fp32 [6][128] e^{G_st(a) - G_en(b)} per pair a > b; [4][128] e^{G_en(a) - G_st(a)}
+constexpr uint32_t S_PT = S_AM + 64 * LDS * 4;   // fp16 [64 r][64 s] P, in the record's swizzled layout
+constexpr uint32_t S_MT = S_PT + 8192;           // fp32 [6][128] e^{G_st(a) - G_en(b)} per pair a > b; [4][128] e^{G_en(a) - G_st(a)}
 constexpr uint32_t S_BT = S_MT + 10 * 128 * 4;   // fp32 [64] beta
 constexpr uint32_t S_BAR = S_BT + 256;           // mbarrier, TMEM slot, flag
 constexpr uint32_t SMEM_BYTES = S_BAR + 64 + 1024;
@@ -133,7 +134,9 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(smem));
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gmem) : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
@@ -148,6 +151,35 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// One diagonal of the blockwise inverse (block pairs (b + d, b)), with the
+// inner products unrolled so every load is issued ahead of its FMA.
+template <int Dg>
+__device__ __forceinline__ void solve_level(float* Am, float* Xm, int tid) {
+    constexpr int nblk = 4 - Dg;
+    for (int idx = tid; idx < nblk * 256; idx += PT) {
+        const int b = idx >> 8, e = idx & 255, ab = b + Dg;
+        const int r = e >> 4, cc = e & 15;
+        float acc = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < Dg; ++kk)
+#pragma unroll
+            for (int s = 0; s < 16; ++s)
+                acc = fmaf(Am[(16 * ab + r) * LDS + 16 * (b + kk) + s], Xm[(16 * (b + kk) + s) * LDS + 16 * b + cc], acc);
+        Am[(16 * b + r) * LDS + 16 * ab + cc] = acc;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < nblk * 256; idx += PT) {
+        const int b = idx >> 8, e = idx & 255, ab = b + Dg;
+        const int r = e >> 4, cc = e & 15;
+        float acc = 0.f;
+#pragma unroll
+        for (int s = 0; s < 16; ++s)
+            acc = fmaf(Xm[(16 * ab + r) * LDS + 16 * ab + s], Am[(16 * b + s) * LDS + 16 * ab + cc], acc);
+        Xm[(16 * ab + r) * LDS + 16 * b + cc] = -acc;
+    }
+    __syncthreads();
+}
+
 __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -158,9 +190,9 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
     float* Xm = reinterpret_cast<float*>(sb + S_Y);
     const __half* KH = reinterpret_cast<const __half*>(sb + S_KH);
     const __half* QH = reinterpret_cast<const __half*>(sb + S_QH);
-    const __half* VH = reinterpret_cast<const __half*>(sb + S_RT);  // v^ rows, once the A/P MMAs are done
+    const __half* VH = reinterpret_cast<const __half*>(sb + S_VH);
     float* Am = reinterpret_cast<float*>(sb + S_AM);
-    float* Pm = reinterpret_cast<float*>(sb + S_PM);
+    unsigned char* ptile = sb + S_PT;
     float* Mt = reinterpret_cast<float*>(sb + S_MT);
     float* bt = reinterpret_cast<float*>(sb + S_BT);
     const uint32_t bar = base + S_BAR;
@@ -188,12 +220,14 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
         ptx::fence_mbar_init();
     }
 
-    // ---- 1. G, k^, q^ into shared memory: 16-byte cp.async copies, all in flight at once
+    // ---- 1. G, k^, q^, v^ into shared memory: three cp.async groups, all in
+    // flight at once, each awaited where it is first needed
     for (int idx = tid; idx < C * 32; idx += PT) {
         const int r = idx >> 5, v4 = idx & 31;
         const int rr = r < L ? r : L - 1;
         cp_async16(sb + S_G + 16 * idx, a.gcum + gidx(rr, 4 * v4));
     }
+    cp_async_commit();
     for (int idx = tid; idx < C * 16; idx += PT) {
         const int r = idx >> 4, v8 = idx & 15;
         if (r < L) {
@@ -204,8 +238,16 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
             reinterpret_cast<uint4*>(sb + S_QH)[idx] = make_uint4(0, 0, 0, 0);
         }
     }
+    cp_async_commit();
+    for (int idx = tid; idx < C * 16; idx += PT) {
+        const int r = idx >> 4, v8 = idx & 15;
+        if (r < L) cp_async16(sb + S_VH + 16 * idx, vh + gidx(r, 8 * v8));
+        else reinterpret_cast<uint4*>(sb + S_VH)[idx] = make_uint4(0, 0, 0, 0);
+    }
+    cp_async_commit();
     if (tid < C) bt[tid] = tid < L ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
-    cp_async_wait_all();
+    for (int idx = tid; idx < 512; idx += PT) reinterpret_cast<uint4*>(ptile)[idx] = make_uint4(0, 0, 0, 0);
+    cp_async_wait_group<2>();  // G
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -231,37 +273,51 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
     }
     __syncthreads();
 
-    // ---- 3. right operand R_s = k_s Y_s and the 256 left rows (bf16, swizzled)
+    // ---- 3. right operand R_s = k_s Y_s and the 256 left rows (bf16, swizzled).
+    // One item = (token r, 8 channels): the reciprocal 1/Y_r is formed once and
+    // every left row that token appears in (A rows for b <= a, P rows for
+    // b < a) is written from it.
+    cp_async_wait_group<1>();  // k^, q^
+    __syncthreads();
     for (int idx = tid; idx < C * 16; idx += PT) {
-        const int s = idx >> 4, ch = idx & 15;
-        float k8[8], y8[8], v[8];
-        lds_h8(KH + s * D + 8 * ch, k8);
-        lds_f8(Y + s * LDY + 8 * ch, y8);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = k8[e] * y8[e];
-        *reinterpret_cast<uint4*>(sb + S_RT + sw128_off(s, 8 * ch, C)) = pack8_bf16(v);
-    }
-    for (int idx = tid; idx < 256 * 16; idx += PT) {
-        const int row = idx >> 4, ch = idx & 15;
-        const int g = group_of(row);
-        const int isP = kGroup[g][0], b = kGroup[g][1];
-        const int r = kGroup[g][2] + (row - kGroup[g][3]);
+        const int r = idx >> 4, ch = idx & 15;
         const int ta = r >> 4;
-        float x8[8], y8[8], v[8];
-        lds_h8((isP ? QH : KH) + r * D + 8 * ch, x8);
+        float k8[8], q8[8], y8[8], iy[8], v[8];
+        lds_h8(KH + r * D + 8 * ch, k8);
+        lds_h8(QH + r * D + 8 * ch, q8);
         lds_f8(Y + r * LDY + 8 * ch, y8);
-        if (ta == b) {        // e^{G_r - G_en(b)} = 1 / Y_r
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = x8[e] * rcp_approx(y8[e]);
-        } else {              // e^{G_r - G_st(a)} e^{G_st(a) - G_en(b)}, with e^{G_r - G_st(a)} = e^{G_en(a) - G_st(a)} / Y_r
-            float va[8], cab[8];
-            lds_f8(Mt + (6 + ta) * D + 8 * ch, va);
-            lds_f8(Mt + pair_of(ta, b) * D + 8 * ch, cab);
+        for (int e = 0; e < 8; ++e) { v[e] = k8[e] * y8[e]; iy[e] = rcp_approx(y8[e]); }
+        *reinterpret_cast<uint4*>(sb + S_RT + sw128_off(r, 8 * ch, C)) = pack8_bf16(v);
+        float va[8];
+        lds_f8(Mt + (6 + ta) * D + 8 * ch, va);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = x8[e] * (va[e] * rcp_approx(y8[e])) * cab[e];
+        for (int e = 0; e < 8; ++e) va[e] *= iy[e];  // e^{G_r - G_st(a)} = e^{G_en(a) - G_st(a)} / Y_r
+        for (int b = 0; b <= ta; ++b) {
+            // A row of (column sub-tile b, r)
+            const int arow = kGroup[b][3] + (r - kGroup[b][2]);
+            float f[8];
+            if (b == ta) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = iy[e];
+            } else {
+                float cab[8];
+                lds_f8(Mt + pair_of(ta, b) * D + 8 * ch, cab);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = va[e] * cab[e];
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = k8[e] * f[e];
+            *reinterpret_cast<uint4*>(sb + S_LAP + (arow >> 7) * 32768 + sw128_off(arow & 127, 8 * ch, 128)) =
+                pack8_bf16(v);
+            if (b < ta) {  // off-diagonal P row of (b, r)
+                const int prow = kGroup[4 + b][3] + (r - kGroup[4 + b][2]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = q8[e] * f[e];
+                *reinterpret_cast<uint4*>(sb + S_LAP + (prow >> 7) * 32768 + sw128_off(prow & 127, 8 * ch, 128)) =
+                    pack8_bf16(v);
+            }
         }
-        *reinterpret_cast<uint4*>(sb + S_LAP + (row >> 7) * 32768 + sw128_off(row & 127, 8 * ch, 128)) =
-            pack8_bf16(v);
     }
     ptx::fence_async_smem();
     ptx::tc_fence_before();
@@ -287,7 +343,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
     // ---- 5. diagonal blocks of P in fp32 while the MMAs run: e^{G_r - G_s} = Y_s / Y_r.
     // Thread = (sub-tile, 4x4 block, K quarter); the quarters interleave 8-channel
     // chunks so that neighbouring lanes read different banks.
-    for (int idx = tid; idx < C * LDS; idx += PT) { Am[idx] = 0.f; Pm[idx] = 0.f; }
+    for (int idx = tid; idx < C * LDS; idx += PT) Am[idx] = 0.f;
     __syncthreads();
     {
         const int ta = tid >> 7, rem = tid & 127;
@@ -339,7 +395,8 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
             for (int x = 0; x < 4; ++x)
 #pragma unroll
                 for (int y = 0; y < 4; ++y)
-                    if (s0 + y <= r0 + x) Pm[(r0 + x) * LDS + s0 + y] = acc[x][y];
+                    if (s0 + y <= r0 + x)
+                        *reinterpret_cast<__half*>(ptile + sw128_off(r0 + x, s0 + y, C)) = __float2half_rn(acc[x][y]);
         }
     }
 
@@ -359,8 +416,8 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
             tmem_ld16(taddr + 16 * q4, v);  // columns s = 16 q4 .. 16 q4 + 15
             if (q4 == b && !*abort_flag) {
                 if (isP) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) Pm[r * LDS + 16 * b + j] = v[j];
+                    *reinterpret_cast<uint4*>(ptile + sw128_off(r, 16 * b, C)) = pack8_f16(v);
+                    *reinterpret_cast<uint4*>(ptile + sw128_off(r, 16 * b + 8, C)) = pack8_f16(v + 8);
                 } else {
                     const float be = bt[r];
 #pragma unroll
@@ -372,13 +429,6 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
     }
     ptx::tc_fence_before();
     __syncthreads();
-
-    // v^ rows into the (now free) right-operand space, landing during the solve
-    for (int idx = tid; idx < C * 16; idx += PT) {
-        const int r = idx >> 4, v8 = idx & 15;
-        if (r < L) cp_async16(sb + S_RT + 16 * idx, vh + gidx(r, 8 * v8));
-        else reinterpret_cast<uint4*>(sb + S_RT)[idx] = make_uint4(0, 0, 0, 0);
-    }
 
     // ---- 7. X = (I + A)^{-1}: diagonal 16 x 16 inverses by forward substitution
     for (int idx = tid; idx < C * LDS; idx += PT) Xm[idx] = 0.f;
@@ -400,31 +450,10 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
     __syncthreads();
     // off-diagonal blocks, one diagonal at a time: X_ab = -X_aa sum_{k=b}^{a-1} A_ak X_kb.
     // The temporaries M_ab live in A's unused upper-right block (b, a).
-    for (int d = 1; d < 4; ++d) {
-        const int nblk = 4 - d;
-        for (int idx = tid; idx < nblk * 256; idx += PT) {
-            const int b = idx >> 8, e = idx & 255, ab = b + d;
-            const int r = e >> 4, cc = e & 15;
-            float acc = 0.f;
-            for (int kb = b; kb < ab; ++kb)
-#pragma unroll
-                for (int s = 0; s < 16; ++s)
-                    acc = fmaf(Am[(16 * ab + r) * LDS + 16 * kb + s], Xm[(16 * kb + s) * LDS + 16 * b + cc], acc);
-            Am[(16 * b + r) * LDS + 16 * ab + cc] = acc;
-        }
-        __syncthreads();
-        for (int idx = tid; idx < nblk * 256; idx += PT) {
-            const int b = idx >> 8, e = idx & 255, ab = b + d;
-            const int r = e >> 4, cc = e & 15;
-            float acc = 0.f;
-#pragma unroll
-            for (int s = 0; s < 16; ++s)
-                acc = fmaf(Xm[(16 * ab + r) * LDS + 16 * ab + s], Am[(16 * b + s) * LDS + 16 * ab + cc], acc);
-            Xm[(16 * ab + r) * LDS + 16 * b + cc] = -acc;
-        }
-        __syncthreads();
-    }
-    cp_async_wait_all();
+    solve_level<1>(Am, Xm, tid);
+    solve_level<2>(Am, Xm, tid);
+    solve_level<3>(Am, Xm, tid);
+    cp_async_wait_group<0>();  // v^
     __syncthreads();
 
     // ---- 8. operands of W^T and U0^T (fp16; the left tiles are dead, reuse their space)
@@ -487,13 +516,8 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
         }
         *reinterpret_cast<uint4*>(rec + REC_KT + sw128_off(key, 8 * ch, 128)) = pack8_f16(v);
     }
-    for (int idx = tid; idx < C * 8; idx += PT) {
-        const int r = idx >> 3, ch = idx & 7;
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = Pm[r * LDS + 8 * ch + e];
-        *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 8 * ch, C)) = pack8_f16(v);
-    }
+    for (int idx = tid; idx < 512; idx += PT)  // the 8 KiB P image
+        reinterpret_cast<uint4*>(rec + REC_P)[idx] = reinterpret_cast<const uint4*>(ptile)[idx];
     if (tid < D) reinterpret_cast<float*>(rec + REC_DECAY)[tid] = expf(G[(C - 1) * D + tid]);
 
     // ---- 10. W^T (warps 0-3, lane = key) through a shared-memory W tile; U0^T (warps 4-7, lane = value) direct
