@@ -77,19 +77,29 @@ def ncu_traffic(kernel: str, src: str):
 
 
 class Clocks:
-    """nvidia-smi sampler running during the timed region."""
+    """nvidia-smi sampler for the timed region: started (and its first sample
+    awaited) before the region opens; the samples taken while it is open, or
+    the one nearest to it when the region is shorter than the period, are
+    summarised."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 100
 
     def __init__(self, device_index):
         self.proc = None
         self.dev = device_index
+        self.lines = []  # (arrival time, line)
+        self.t_open = self.t_close = None
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.monotonic(), line))
 
     def __enter__(self):
+        import threading
         try:
-            uuid = None
             try:
                 uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
                 if not uuid.startswith("GPU-"):
@@ -99,49 +109,72 @@ class Clocks:
             sel = uuid or os.environ.get("CUDA_VISIBLE_DEVICES", str(self.dev)).split(",")[self.dev]
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", sel], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.PERIOD_MS), "-i", sel],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._reader, daemon=True).start()
+            deadline = time.monotonic() + 5.0
+            while not self.lines and time.monotonic() < deadline and self.proc.poll() is None:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
+        self.t_open = time.monotonic()
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
+        self.t_close = time.monotonic()
         if self.proc is not None:
+            time.sleep(self.PERIOD_MS / 1000 * 1.5)  # the sample that covers the region's end
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
         return False
 
+    @staticmethod
+    def _parse(line):
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 7:
+            return None
+        try:
+            return float(parts[0]), float(parts[1]), parts[3:7]
+        except ValueError:
+            return None
+
     def summary(self):
-        sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in (self.out or "").strip().splitlines():
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 7:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx = float(parts[1])
-            except ValueError:
-                continue
-            for nm, val in zip(names, parts[3:7]):
+        parsed = [(t, self._parse(l)) for t, l in self.lines]
+        parsed = [(t, p) for t, p in parsed if p is not None]
+        if not parsed or self.t_open is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        # a sample arriving up to one period after the region closed still covers it
+        inside = [p for t, p in parsed if self.t_open <= t <= self.t_close + self.PERIOD_MS / 1000]
+        if not inside:
+            inside = [min(parsed, key=lambda tp: abs(tp[0] - self.t_open))[1]]
+        reasons = set()
+        for _, _, flags in inside:
+            for nm, val in zip(names, flags):
                 if val.lower() == "active":
                     reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(p[0] for p in inside), "sm_max_mhz": inside[-1][1],
+                "reasons": sorted(reasons), "samples": len(inside), "period_ms": self.PERIOD_MS}
 
 
 def allreduce_max(x: float, world: int) -> float:
+    """Maximum of `x` over the ranks (the slowest replica sets the step time)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_value(units_per_rank: float, ms_max: float, world: int) -> float:
+    """Throughput of the whole job: every rank processes its own copy of the
+    workload (replicas), timed by the slowest rank."""
+    return units_per_rank * world / (ms_max / 1e3)
 
 
 def barrier(world):
@@ -156,9 +189,22 @@ def prestage_bytes_per_token_head(io_bytes, out_bytes):
     return 4 * D * io_bytes + io_bytes + 3 * D * out_bytes + 4 * D + 4
 
 
-def recurrence_bytes_per_token_head(op_bytes):
-    # reads q^,k^,v^ + gate (fp32) + beta; writes o_core (fp32)
-    return 3 * D * op_bytes + 4 * D + 4 + 4 * D
+def scan_bytes_per_token_head():
+    # reads q^,k^,v^, gate (fp32) + beta; writes o_core (fp32)
+    return 3 * D * 4 + 4 * D + 4 + 4 * D
+
+
+REC_BYTES = 74240  # one chunk-head record of operand tiles (kda_chunk_layout.cuh)
+
+
+def prep_bytes_per_token_head():
+    # reads q^,k^,v^ (fp16) + cumulative gate (fp32) + beta; writes the record
+    return 3 * D * 2 + 4 * D + 4 + REC_BYTES / 64
+
+
+def chunk_recurrence_bytes_per_token_head(io_bytes):
+    # reads the record + gout; writes o
+    return REC_BYTES / 64 + 2 * D * io_bytes
 
 
 def epilogue_bytes_per_token_head(io_bytes):
@@ -219,7 +265,8 @@ def prefill_arm(args, dev, world, rank):
         torch.cuda.synchronize()
     barrier(world)
     ms = start.elapsed_time(end) / args.steps
-    stage_ms = [statistics.mean(evs[i].elapsed_time(evs[i + 1]) for evs in evsets) for i in range(4)]
+    stage_ms = [statistics.mean(evs[i].elapsed_time(evs[i + 1]) for evs in evsets)
+                for i in range(kda.KDA_PREFILL_EVENTS - 1)]
     ms_max = allreduce_max(ms, world)
     ws_status = kda.kda_workspace_status(ws, stream)
     return dict(w=w, ms=ms, ms_max=ms_max, stage_ms=stage_ms, clocks=clk.summary(), kp=kp,
@@ -285,7 +332,7 @@ def decode_arm(args, dev):
     return dict(ms=ms, sessions=w.n_seqs, H=w.H, bytes=n_units * decode_bytes_per_session_head(2) , steps=steps)
 
 
-def cpu_baseline(args, sample_heads=32, sample_tokens=16384):
+def cpu_baseline(args, sample_heads=48, sample_tokens=32768):
     """The fp64 oracle, as it stands, on a bounded sample of the long
     workload: `sample_heads` heads x the first `sample_tokens` tokens."""
     import oracle
@@ -304,31 +351,35 @@ def cpu_baseline(args, sample_heads=32, sample_tokens=16384):
 
 
 # -------------------------------------------------------------- reference
+REFERENCE_STEP = dict(tokens=2048, heads=16)  # one oracle step: the first heads x tokens of the long workload
+
+
 def reference_main(args, world, rank):
     if rank != 0:
         return
     import oracle
     from tests.kda_testlib import oracle_run
-    w = kda_synth.workload(3, device="cpu", lens=[2048])
-    heads = list(range(16))
-    sub_tokens = w.tokens
+    n_tok, n_heads = REFERENCE_STEP["tokens"], REFERENCE_STEP["heads"]
+    w = kda_synth.workload(3, device="cpu", lens=[n_tok])
+    heads = list(range(n_heads))
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        oracle_run(w.params, sub_tokens, w.cu_seqlens, heads=heads)
+        oracle_run(w.params, w.tokens, w.cu_seqlens, heads=heads)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     dt = statistics.mean(times)
     value = len(heads) * w.total_tokens / w.H / dt
+    sample = f"{n_heads} of {w.H} heads x {n_tok} tokens per step"
     line = {
         "impl": "reference", "metric": "KDA tokens/s/layer (chunked prefill)", "value": value,
         "unit": "tokens/s/layer", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "K3 long prefill B=1 T=32768 H=96 d=128 bf16 inputs (oracle step: 16 heads x 2048 tokens)",
+        "config": {"workload": f"long prefill B=1 T=32768 H=96 d=128 bf16 inputs (oracle step: {sample})",
                    "global_batch": 1, "seq_len": 32768, "parallelism": "replicas"},
         "cpu_baseline": {"value": value, "unit": "tokens/s/layer", "cores": oracle.default_threads(),
-                         "kind": "oracle", "sample": "16 of 96 heads x 2048 tokens per step"},
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -338,7 +389,7 @@ def reference_main(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--algo", default="auto", choices=["auto", "scan", "chunked"])
@@ -368,26 +419,34 @@ def main():
     r = prefill_arm(args, dev, world, rank)
     w = r["w"]
     H, T = w.H, w.total_tokens
-    value = T * world / (r["ms_max"] / 1e3)
+    value = whole_job_value(T, r["ms_max"], world)
 
     # roofline of the dominant kernel (largest share of the step)
     chunked = r["algo_resolved"] == "chunked"
-    names = ["prestage_kernel", "chunked_kernel" if chunked else "scan_kernel", "epilogue_kernel", "ring_update_kernel"]
-    srcs = ["kda_prestage.cu", "kda_chunk.cu" if chunked else "kda_scan.cu", "kda_epilogue.cu", "kda_prestage.cu"]
-    per_th = [prestage_bytes_per_token_head(2, 2 if chunked else 4),
-              recurrence_bytes_per_token_head(2 if chunked else 4),
-              epilogue_bytes_per_token_head(2), 0]
+    stage_names = ["prestage", "chunk_prep", "recurrence", "epilogue", "ring"]
+    kernels = ["prestage_kernel", "chunk_prep_kernel", "chunk_recurrence_kernel" if chunked else "scan_kernel",
+               "epilogue_kernel", "ring_update_kernel"]
+    srcs = ["kda_prestage.cu", "kda_chunk_prep.cu", "kda_chunk.cu" if chunked else "kda_scan.cu",
+            "kda_epilogue.cu", "kda_prestage.cu"]
+    state_bytes = 2 * D * D * 4 * w.n_seqs * H  # S read + written once per (sequence, head)
+    per_launch = [prestage_bytes_per_token_head(2, 2 if chunked else 4) * T * H,
+                  prep_bytes_per_token_head() * T * H if chunked else 0,
+                  (chunk_recurrence_bytes_per_token_head(2) if chunked else scan_bytes_per_token_head()) * T * H
+                  + state_bytes,
+                  0 if chunked else epilogue_bytes_per_token_head(2) * T * H, 0]
     stage_ms = r["stage_ms"]
-    dom = max(range(3), key=lambda i: stage_ms[i])
-    alg_bytes = per_th[dom] * T * H
+    dom = max(range(4), key=lambda i: stage_ms[i])
+    alg_bytes = per_launch[dom]
     achieved = alg_bytes / (stage_ms[dom] / 1e3) / 1e9
     src_path = os.path.join(ROOT, "gated_delta_rule_04_gb300", "csrc", srcs[dom])
-    roofline = {"bound": "hbm", "kernel": names[dom], "achieved": achieved, "peak": hbm, "unit": "GB/s",
+    roofline = {"bound": "hbm", "kernel": kernels[dom], "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm, "peak_kind": f"{peak_kind} copy bandwidth",
-                "traffic": ncu_traffic(names[dom], src_path),
+                "traffic": ncu_traffic(kernels[dom], src_path),
                 "algorithmic_bytes_per_launch": alg_bytes,
-                "bytes_per_token_head": per_th[dom], "ms_per_launch": stage_ms[dom],
-                "stage_ms": dict(zip(["prestage", "recurrence", "epilogue", "ring"], stage_ms))}
+                "bytes_per_token_head": alg_bytes / (T * H), "ms_per_launch": stage_ms[dom],
+                "stage_ms": dict(zip(stage_names, stage_ms)),
+                "stage_frac_of_hbm": {n: (b / (ms / 1e3) / 1e9 / hbm if ms > 0 and b else None)
+                                      for n, b, ms in zip(stage_names, per_launch, stage_ms)}}
 
     line = {
         "metric": "KDA tokens/s/layer (chunked prefill)", "value": value, "unit": "tokens/s/layer",
@@ -408,7 +467,7 @@ def main():
         gbs = dr["bytes"] / (dr["ms"] / 1e3) / 1e9
         line["decode"] = {
             "workload": "batched decode: 256 sessions x H=32, d=128, one token each, bf16 I/O, fp32 state from 512 warm-up tokens",
-            "value": dr["sessions"] * world / (dr["ms"] / 1e3), "unit": "session*tokens/s",
+            "value": whole_job_value(dr["sessions"], allreduce_max(dr["ms"], world), world), "unit": "session*tokens/s",
             "ms_per_step": dr["ms"], "steps": dr["steps"],
             "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                          "frac": gbs / hbm, "peak_kind": f"{peak_kind} copy bandwidth",
@@ -418,7 +477,7 @@ def main():
     if not args.no_e2e:
         ms, h2d, d2h = e2e_arm(args, dev, w, r["kp"])
         ms = allreduce_max(ms, world)
-        line["e2e"] = {"value": T * world / (ms / 1e3), "unit": "tokens/s/layer", "ms_per_step": ms,
+        line["e2e"] = {"value": whole_job_value(T, ms, world), "unit": "tokens/s/layer", "ms_per_step": ms,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args)

@@ -152,7 +152,7 @@ def _cu_array(cu_seqlens: Sequence[int]):
     return (ctypes.c_int64 * len(vals))(*vals), len(vals) - 1, vals[-1]
 
 
-KDA_PREFILL_EVENTS = 5
+KDA_PREFILL_EVENTS = 6
 
 
 def kda_prefill(params: Params, q, k, v, z, b, gout, cu_seqlens, S_in=None, S_out=None,

@@ -231,37 +231,37 @@ kda_status prefill_impl(const kda_params* p, const void* q, const void* k, const
                     ws + L.qh, ws + L.kh, ws + L.vh, gbuf, beta};
     if (algo == Algo::Scan) {
         e = launch_prestage(pa, io_bf16, /*out_fp16=*/0, /*cumsum=*/0, s);
-        if (e != cudaSuccess || mark(ev, 1, s) != cudaSuccess) return KDA_ERR_CUDA;
+        if (e != cudaSuccess || mark(ev, 1, s) != cudaSuccess || mark(ev, 2, s) != cudaSuccess) return KDA_ERR_CUDA;
         ScanArgs sa{reinterpret_cast<const float*>(ws + L.qh), reinterpret_cast<const float*>(ws + L.kh),
                     reinterpret_cast<const float*>(ws + L.vh), gbuf, beta, S_in, S_out, ocore, d_cu,
                     n_seqs, H};
         e = launch_scan(sa, s);
-        if (e != cudaSuccess || mark(ev, 2, s) != cudaSuccess) return KDA_ERR_CUDA;
+        if (e != cudaSuccess || mark(ev, 3, s) != cudaSuccess) return KDA_ERR_CUDA;
     } else {
         e = launch_prestage(pa, io_bf16, /*out_fp16=*/1, /*cumsum=*/1, s);
         if (e != cudaSuccess || mark(ev, 1, s) != cudaSuccess) return KDA_ERR_CUDA;
         PrepArgs pr{ws + L.qh, ws + L.kh, ws + L.vh, gbuf, beta, d_chunks, (int32_t)n_chunks, H, ws + L.rec,
                     reinterpret_cast<int32_t*>(ws + L.status)};
         e = launch_chunk_prep(pr, s);
-        if (e != cudaSuccess) return KDA_ERR_CUDA;
+        if (e != cudaSuccess || mark(ev, 2, s) != cudaSuccess) return KDA_ERR_CUDA;
         // the recurrence kernel applies the output norm itself
         ChunkRecArgs ca{ws + L.rec, S_in, S_out, gout, p->norm_w, o, p->norm_eps, d_cu, d_coff, d_order,
                         reinterpret_cast<int32_t*>(ws + L.status), n_seqs, H};
         e = launch_chunk_recurrence(ca, s);
-        if (e != cudaSuccess || mark(ev, 2, s) != cudaSuccess) return KDA_ERR_CUDA;
+        if (e != cudaSuccess || mark(ev, 3, s) != cudaSuccess) return KDA_ERR_CUDA;
     }
     if (algo == Algo::Scan) {
         EpilogueArgs ea{ocore, gout, p->norm_w, o, total_tokens, H, p->norm_eps};
         e = launch_epilogue(ea, io_bf16, s);
         if (e != cudaSuccess) return KDA_ERR_CUDA;
     }
-    if (mark(ev, 3, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (mark(ev, 4, s) != cudaSuccess) return KDA_ERR_CUDA;
     if (ring_out) {
         RingArgs ra{q, k, v, ring_in, ring_out, d_cu, n_seqs, W};
         e = launch_ring_update(ra, io_bf16, s);
         if (e != cudaSuccess) return KDA_ERR_CUDA;
     }
-    if (mark(ev, 4, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (mark(ev, 5, s) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }
 

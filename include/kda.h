@@ -120,11 +120,14 @@ kda_status kda_prefill(const kda_params* p,
 
 /* Same as kda_prefill, and records caller-created CUDA events on `stream` at
  * the stage boundaries, for profiling: stage_events[0] before the pre-stage,
- * [1] after the pre-stage (conv, norms, gate, beta), [2] after the
- * recurrence (chunked or scan), [3] after the RMSNormGated epilogue, [4]
- * after the conv-ring update.  stage_events holds KDA_PREFILL_EVENTS
- * cudaEvent_t handles (any may be NULL to skip it) or is NULL. */
-#define KDA_PREFILL_EVENTS 5
+ * [1] after the pre-stage (conv, norms, gate, beta), [2] after the chunk
+ * preparation (chunked path; right after [1] on the scan path), [3] after
+ * the recurrence (on the chunked path it includes the RMSNormGated output),
+ * [4] after the separate RMSNormGated epilogue (scan path; right after [3]
+ * on the chunked path), [5] after the conv-ring update.  stage_events holds
+ * KDA_PREFILL_EVENTS cudaEvent_t handles (any may be NULL to skip it) or is
+ * NULL. */
+#define KDA_PREFILL_EVENTS 6
 kda_status kda_prefill_with_events(const kda_params* p,
                                    const void* q, const void* k, const void* v, const void* z,
                                    const void* b, const void* gout,
