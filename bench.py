@@ -197,9 +197,9 @@ def scan_bytes_per_token_head():
 REC_BYTES = 74240  # one chunk-head record of operand tiles (kda_chunk_layout.cuh)
 
 
-def prep_bytes_per_token_head():
-    # reads q^,k^,v^ (fp16) + cumulative gate (fp32) + beta; writes the record
-    return 3 * D * 2 + 4 * D + 4 + REC_BYTES / 64
+def prep_bytes_per_token_head(io_bytes):
+    # reads raw q,k,v (+ the three rows before each 64-token chunk), z and b; writes the record
+    return 3 * D * io_bytes * (64 + 3) / 64 + D * io_bytes + io_bytes + REC_BYTES / 64
 
 
 def chunk_recurrence_bytes_per_token_head(io_bytes):
@@ -269,8 +269,10 @@ def prefill_arm(args, dev, world, rank):
                 for i in range(kda.KDA_PREFILL_EVENTS - 1)]
     ms_max = allreduce_max(ms, world)
     ws_status = kda.kda_workspace_status(ws, stream)
+    algo = kda.kda_prefill_algo(kp)
+    per_step = 3 if algo == "chunked" else 4  # chunked: prep, recurrence, ring; scan: + pre-stage, epilogue
     return dict(w=w, ms=ms, ms_max=ms_max, stage_ms=stage_ms, clocks=clk.summary(), kp=kp,
-                launches=4 * args.steps, ws_status=ws_status, algo_resolved=kda.kda_prefill_algo(kp))
+                launches=per_step * args.steps, ws_status=ws_status, algo_resolved=algo)
 
 
 def e2e_arm(args, dev, w, kp):
@@ -429,8 +431,8 @@ def main():
     srcs = ["kda_prestage.cu", "kda_chunk_prep.cu", "kda_chunk.cu" if chunked else "kda_scan.cu",
             "kda_epilogue.cu", "kda_prestage.cu"]
     state_bytes = 2 * D * D * 4 * w.n_seqs * H  # S read + written once per (sequence, head)
-    per_launch = [prestage_bytes_per_token_head(2, 2 if chunked else 4) * T * H,
-                  prep_bytes_per_token_head() * T * H if chunked else 0,
+    per_launch = [0 if chunked else prestage_bytes_per_token_head(2, 4) * T * H,
+                  prep_bytes_per_token_head(2) * T * H if chunked else 0,
                   (chunk_recurrence_bytes_per_token_head(2) if chunked else scan_bytes_per_token_head()) * T * H
                   + state_bytes,
                   0 if chunked else epilogue_bytes_per_token_head(2) * T * H, 0]

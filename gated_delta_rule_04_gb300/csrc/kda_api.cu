@@ -76,7 +76,7 @@ struct WsLayout {
 WsLayout layout(const kda_params* p, Algo algo, int32_t n_seqs, int64_t T, int64_t n_chunks) {
     WsLayout L;
     const size_t W = (size_t)p->num_heads * D;
-    const size_t op = (algo == Algo::Chunked) ? 2 : 4;  // q^/k^/v^: fp16 (chunked) or fp32 (scan)
+    const size_t op = 4;  // q^/k^/v^ of the scan path: fp32
     size_t off = 0;
     L.status = off; off += WS_ALIGN;
     L.meta = off;
@@ -85,13 +85,17 @@ WsLayout layout(const kda_params* p, Algo algo, int32_t n_seqs, int64_t T, int64
     L.off_chunks = align_up(L.off_order + sizeof(int32_t) * (size_t)n_seqs, 16);
     L.meta_bytes = L.off_chunks + sizeof(ChunkDesc) * (size_t)n_chunks;
     off = align_up(off + L.meta_bytes, WS_ALIGN);
-    L.qh = off; off = align_up(off + op * (size_t)T * W, WS_ALIGN);
-    L.kh = off; off = align_up(off + op * (size_t)T * W, WS_ALIGN);
-    L.vh = off; off = align_up(off + op * (size_t)T * W, WS_ALIGN);
-    L.g = off; off = align_up(off + 4 * (size_t)T * W, WS_ALIGN);
-    L.beta = off; off = align_up(off + 4 * (size_t)T * p->num_heads, WS_ALIGN);
-    L.ocore = off;  // o_core: only the scan path has a separate output stage
-    if (algo == Algo::Scan) off = align_up(off + 4 * (size_t)T * W, WS_ALIGN);
+    // q^, k^, v^ (fp32), gate, beta and o_core: only the scan path has a
+    // separate pre-stage and output stage; the chunked path keeps them on chip
+    const bool scan = algo == Algo::Scan;
+    const size_t tw = scan ? (size_t)T * W : 0;
+    L.qh = off; off = align_up(off + op * tw, WS_ALIGN);
+    L.kh = off; off = align_up(off + op * tw, WS_ALIGN);
+    L.vh = off; off = align_up(off + op * tw, WS_ALIGN);
+    L.g = off; off = align_up(off + 4 * tw, WS_ALIGN);
+    L.beta = off; off = align_up(off + 4 * (scan ? (size_t)T * p->num_heads : 0), WS_ALIGN);
+    L.ocore = off;
+    off = align_up(off + 4 * tw, WS_ALIGN);
     L.rec = off;
     if (algo == Algo::Chunked) off = align_up(off + (size_t)REC_BYTES * (size_t)n_chunks * p->num_heads, WS_ALIGN);
     L.total = off;
@@ -238,10 +242,10 @@ kda_status prefill_impl(const kda_params* p, const void* q, const void* k, const
         e = launch_scan(sa, s);
         if (e != cudaSuccess || mark(ev, 3, s) != cudaSuccess) return KDA_ERR_CUDA;
     } else {
-        e = launch_prestage(pa, io_bf16, /*out_fp16=*/1, /*cumsum=*/1, s);
-        if (e != cudaSuccess || mark(ev, 1, s) != cudaSuccess) return KDA_ERR_CUDA;
-        PrepArgs pr{ws + L.qh, ws + L.kh, ws + L.vh, gbuf, beta, d_chunks, (int32_t)n_chunks, H, ws + L.rec,
-                    reinterpret_cast<int32_t*>(ws + L.status)};
+        // the chunk preparation runs the pre-stage itself
+        if (mark(ev, 1, s) != cudaSuccess) return KDA_ERR_CUDA;
+        PrepArgs pr{q, k, v, z, b, ring_in, p->conv_w, p->A_log, p->dt_bias, p->gate_lower_bound, p->l2_eps, qs,
+                    d_chunks, (int32_t)n_chunks, H, ws + L.rec, reinterpret_cast<int32_t*>(ws + L.status)};
         e = launch_chunk_prep(pr, s);
         if (e != cudaSuccess || mark(ev, 2, s) != cudaSuccess) return KDA_ERR_CUDA;
         // the recurrence kernel applies the output norm itself

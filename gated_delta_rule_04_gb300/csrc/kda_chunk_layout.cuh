@@ -32,14 +32,17 @@ __host__ __device__ __forceinline__ uint32_t sw128_off(int row, int k, int rows)
     return (uint32_t)(panel * rows * 128 + row * 128 + (((chunk ^ (row & 7)) & 7) << 4) + within * 2);
 }
 
+// Inputs of the chunk preparation (pre-stage fused in): the raw bf16
+// projections and the layer parameters.
 struct PrepArgs {
-    const void *qh, *kh, *vh;  // fp16 [T][H*128]
-    const float* gcum;         // [T][H*128] chunk-local inclusive cumulative gate
-    const float* beta;         // [T][H]
+    const void *q, *k, *v, *z, *b;  // bf16 [T][H*128]; b [T][H]
+    const void* ring_in;            // bf16 [n][3][3][H*128] or NULL (zero)
+    const float *conv_w, *A_log, *dt_bias;
+    float lb, l2_eps, q_scale;
     const ChunkDesc* chunks;
     int32_t n_chunks, H;
-    void* records;             // [n_chunks][H][REC_BYTES]
-    int32_t* status;           // workspace error word
+    void* records;                  // [n_chunks][H][REC_BYTES]
+    int32_t* status;                // workspace error word
 };
 cudaError_t launch_chunk_prep(const PrepArgs& a, cudaStream_t s);
 size_t chunk_prep_smem_bytes();

@@ -1,82 +1,104 @@
-// Chunk preparation for the chunked prefill: everything inside a 64-token
-// chunk that does not depend on the recurrent state, for all chunks and heads
-// in parallel.  The chunked form follows the "chunked UT transform" with a
-// per-channel cumulative log gate described on "memra-engine 0.124.0, module
-// kda" (PREFILL DISPATCH) and the 16-token tile bound of "Kimi K3 - Retention
-// gate - OpenModelAtlas" (section "Why": with g >= -5 every rescaling over a
-// 16-token tile stays below e^80, inside bf16's range).
+// Chunk preparation of the chunked prefill, with the pre-stage fused in:
+// from the raw projections of a 64-token chunk of one head to the record of
+// operand tiles the tcgen05 recurrence consumes.  Everything here is
+// independent of the recurrent state, so all (chunk, head) items run in
+// parallel.
 //
-// With G_r the inclusive cumulative gate inside the chunk (per key channel):
-//   A[r][s] = beta_r sum_i k_ri k_si e^{G_ri - G_si}   (s < r)
-//   P[r][s] =        sum_i q_ri k_si e^{G_ri - G_si}   (s <= r)
-//   T  = (I + A)^{-1} Diag(beta)
-//   W  = T (k * e^{G}),  U0 = T v,  Q+ = q * e^{G},  Kt = k * e^{G_last - G},
-//   decay = e^{G_last}
-// The sequential kernel then needs only U = U0 - W S, O = Q+ S + P U and
-// S' = Diag(decay) S + Kt^T U per chunk.
+// Per item (sources: "Kimi Delta Attention (KDA) -- analysis & C kernel
+// plan", sections "The KDA layer, precisely" and "Recurrence"; "ferrox-models
+// 0.8.0, module kda", module overview; "Kimi K3 - Retention gate -
+// OpenModelAtlas", gate formula):
+//   1. short causal conv (kernel 4) + SiLU of q, k, v; q^ = q / |q| * q_scale,
+//      k^ = k / |k| (eps inside the root); g = lb * sigmoid(e^A (z + dt_bias));
+//      beta = sigmoid(b); G = chunk-local inclusive cumulative sum of g.
+//   2. the chunked form ("chunked UT transform" with a per-channel cumulative
+//      log gate, "memra-engine 0.124.0, module kda", PREFILL DISPATCH; 16-token
+//      tiles kept in range by the lower bound, "Kimi K3 - Retention gate",
+//      section "Why"):
+//        A[r][s] = beta_r sum_i k_ri k_si e^{G_ri - G_si}   (s < r)
+//        P[r][s] =        sum_i q_ri k_si e^{G_ri - G_si}   (s <= r)
+//        T = (I + A)^{-1} Diag(beta),  W = T (k e^G),  U0 = T v,
+//        Q+ = q e^G,  Kt = k e^{G_last - G},  decay = e^{G_last}
+//      The recurrence then needs only U = U0 - W S, O = Q+ S + P U and
+//      S' = Diag(decay) S + Kt^T U per chunk.
 //
 // Range.  For s in 16-token sub-tile b the reference point is the last token
-// of that sub-tile, en(b):  e^{G_r - G_s} = e^{G_r - G_en(b)} * Y_s with
-// Y_s = e^{G_en(b) - G_s} <= 1.  The left factor is <= 1 when r lies in a
-// later sub-tile and at most e^{75} inside the diagonal sub-tile, which bf16
-// holds.  All of A and the off-diagonal blocks of P therefore run on the
-// tensor cores as two bf16 MMAs (M = 128, N = 64 = every s, K = 128 keys):
-// 256 left rows = (A rows grouped by column sub-tile b: 64+48+32+16) +
-// (off-diagonal P rows: 48+32+16).  The diagonal blocks of P stay in fp32 on
-// the CUDA cores: P reaches the output directly, and bf16 there would triple
-// the end-to-end error, while bf16 in A changes it by under 5%.
-// Left factors for a later sub-tile a > b are formed as a product of two
-// factors <= 1, e^{G_r - G_st(a)} e^{G_st(a) - G_en(b)}, so nothing
-// overflows or loses precision to fp32 subnormals.
+// of b, en(b): e^{G_r - G_s} = e^{G_r - G_en(b)} Y_s with Y_s = e^{G_en(b) - G_s}
+// <= 1.  For r in sub-tile a the left factor is iY_r C_ab with
+// iY_r = e^{G_r - G_en(a)} in [1, e^{75}] and C_ab = e^{G_en(a) - G_en(b)} <= 1,
+// which bf16 holds; a factor that underflows stands for a product far below
+// every other term.
 //
-// The unit lower-triangular solve is blockwise: the four 16 x 16 diagonal
-// inverses by forward substitution, then the off-diagonal blocks of the
-// inverse by 16 x 16 products, diagonal by diagonal.  W^T = (k e^G)^T T^T and
-// U0^T = v^T T^T run as two fp16 M=128 MMAs.
+// Tensor cores.  A and the off-diagonal blocks of P are two bf16 M = 128 MMAs
+// against the right operand R = k Y (N = 64, K = 128 keys).  The 256 left
+// rows are the A rows grouped by column sub-tile b (64 + 48 + 32 + 16) and the
+// off-diagonal P rows (48 + 32 + 16).  The diagonal blocks of P reach the
+// output directly and need more than bf16: their operands are split into
+// bf16 high and low parts and one accumulator takes hi*hi + lo*hi + hi*lo
+// (24 K-steps), good to about 16 bits.  W = T (k e^G) and U0^T = v^T T^T are
+// fp16 MMAs; the unit lower-triangular solve is fp32 on the CUDA cores
+// (16 x 16 diagonal inverses, then the off-diagonal blocks diagonal by
+// diagonal).
 //
-// Output: one record per (chunk, head) holding the operand tiles in the exact
-// shared-memory image the tcgen05 recurrence kernel consumes (fp16, K-major,
-// 128-byte swizzle: 16-byte chunk j of row r stored at chunk position j ^ (r & 7)).
+// Thread mapping of the element-wise part: warp w, lane l -> token octet
+// o = w / 2 (tokens 8o .. 8o+7, inside sub-tile o / 2) and channel pair
+// p = 32 (w % 2) + l (channels 2p, 2p+1).  Each thread keeps its 16 elements
+// in registers from the conv to the operand tiles; token sums (L2 norms) are
+// warp reduce-scatters plus one shared-memory exchange, and the cumulative
+// gate is a per-thread running sum plus a prefix over octets.
+//
+// Schedule.  The grid is persistent (one CTA per SM); the raw rows of a CTA's
+// next item are bulk-copied into shared memory as soon as the current item
+// has read its own, so the load overlaps the rest of the item.
+//
+// Output: one record per (chunk, head) in the exact shared-memory image the
+// recurrence kernel consumes (fp16, K-major, 128-byte swizzle), written
+// straight from registers.
 #include "kda_chunk_layout.cuh"
 #include "tc_ptx.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int PT = 512;        // threads (16 warps: four per scheduler to hide latency)
-constexpr int C = CHUNK_T;     // 64 tokens
-constexpr int LDS = 65;        // padded fp32 row stride of the 64 x 64 matrices
-constexpr int LDY = 132;       // padded fp32 row stride of Y
-constexpr uint32_t TMEM_COLS = 256;  // [0,64) left tile 0, [64,128) left tile 1, [128,192) W^T, [192,256) U0^T
+constexpr int PT = 512;
+constexpr int C = CHUNK_T;                 // 64 tokens
+constexpr int RAW_ROWS = C + RING;         // raw q/k/v rows incl. the three before the chunk
+constexpr uint32_t ROW_B = D * 2;          // one bf16 row of a head
+constexpr int LDS = 65;                    // padded fp32 row stride of the 64 x 64 matrices
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_D0 = 0, TM_D1 = 64, TM_D2 = 128, TM_W = 192, TM_U = 320;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr float LOG2E = 1.4426950408889634f;
 
-// shared-memory map (bytes, from a 1 KiB aligned base)
-constexpr uint32_t S_G = 0;                      // fp32 [64][128] G (rows past the chunk repeat the last)
-constexpr uint32_t S_Y = S_G + 32768;            // fp32 [64][132] Y; later X = (I+A)^{-1} fp32 [64][65]
-constexpr uint32_t S_KH = S_Y + 33792;           // fp16 [64][128] k^ (plain row-major)
-constexpr uint32_t S_QH = S_KH + 16384;          // fp16 [64][128] q^
-constexpr uint32_t S_VH = S_QH + 16384;          // fp16 [64][128] v^
-constexpr uint32_t S_LAP = S_VH + 16384;         // bf16 2 tiles x [128 rows][128 keys] (swizzled); later KPT/VT/TT
-constexpr uint32_t S_KPT = S_LAP;                //   fp16 [128 key][64 tok]  (k e^G)^T
-constexpr uint32_t S_VT = S_LAP + 16384;         //   fp16 [128 val][64 tok]  v^T
-constexpr uint32_t S_TT = S_LAP + 32768;         //   fp16 [64 r][64 s]       T
-constexpr uint32_t S_RT = S_LAP + 65536;         // bf16 [64 s][128 keys] k Y (swizzled); later the W tile
-constexpr uint32_t S_AM = S_RT + 16384;          // fp32 [64][65] A (with beta)
-constexpr uint32_t S_PT = S_AM + 64 * LDS * 4;   // fp16 [64 r][64 s] P, in the record's swizzled layout
-constexpr uint32_t S_MT = S_PT + 8192;           // fp32 [6][128] e^{G_st(a) - G_en(b)} per pair a > b; [4][128] e^{G_en(a) - G_st(a)}
-constexpr uint32_t S_BT = S_MT + 10 * 128 * 4;   // fp32 [64] beta
-constexpr uint32_t S_BAR = S_BT + 256;           // mbarrier, TMEM slot, flag
+// shared-memory map (bytes from a 1 KiB aligned base)
+constexpr uint32_t S_RQ = 0;                               // bf16 [67][128] raw q (row 0 = token t0 - 3)
+constexpr uint32_t S_RK = S_RQ + RAW_ROWS * ROW_B;
+constexpr uint32_t S_RV = S_RK + RAW_ROWS * ROW_B;
+constexpr uint32_t S_RZ = S_RV + RAW_ROWS * ROW_B;         // bf16 [64][128] raw z
+constexpr uint32_t S_OPS = 68608;                          // operand region (1 KiB aligned)
+constexpr uint32_t S_LAP = S_OPS;                          //   bf16 2 x [128 rows][128 keys]
+constexpr uint32_t S_QD = S_OPS + 65536;                   //   bf16 [128][128]: rows 0-63 hi, 64-127 lo
+constexpr uint32_t S_RH = S_OPS + 98304;                   //   bf16 [64 s][128 keys] R, high part
+constexpr uint32_t S_RL = S_OPS + 114688;                  //   low part
+constexpr uint32_t S_AM = S_OPS;                           // after the first MMAs: fp32 [64][65] A
+constexpr uint32_t S_XM = S_OPS + 16640;                   //   fp32 [64][65] X = (I + A)^{-1}
+constexpr uint32_t S_TT = S_OPS + 33792;                   //   fp16 [128 r][64 s] T (rows 64-127 zero)
+constexpr uint32_t S_KPT = S_OPS + 50176;                  //   fp16 [128 key][64 s] (k e^G)^T
+constexpr uint32_t S_VT = S_OPS + 66560;                   //   fp16 [128 val][64 s] v^T
+constexpr uint32_t S_NRM = S_OPS + 131072;                 // fp32 [16 warps][16] partial sums of squares
+constexpr uint32_t S_TOT = S_NRM + 1024;                   // fp32 [8 octets][128] gate sums
+constexpr uint32_t S_BT = S_TOT + 4096;                    // fp32 [64] beta
+constexpr uint32_t S_BAR = S_BT + 256;                     // 3 mbarriers, TMEM slot, abort flag
 constexpr uint32_t SMEM_BYTES = S_BAR + 64 + 1024;
-
-// sub-tile pairs a > b in the order of the factor table
-__constant__ int8_t kPairA[6] = {1, 2, 3, 2, 3, 3};
-__constant__ int8_t kPairB[6] = {0, 0, 0, 1, 1, 2};
-__device__ __forceinline__ int pair_of(int a, int b) { return b == 0 ? a - 1 : (b == 1 ? a + 1 : 5); }
+static_assert(S_RZ + C * ROW_B <= S_OPS, "raw rows overlap the operand region");
+static_assert(S_VT + 16384 <= S_OPS + 131072, "late tiles overflow the operand region");
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 // Row groups of the 256 left rows: (is_P, column sub-tile b, first r, first row)
 __constant__ int16_t kGroup[7][4] = {
     {0, 0, 0, 0}, {0, 1, 16, 64}, {0, 2, 32, 112}, {0, 3, 48, 144},
     {1, 0, 16, 160}, {1, 1, 32, 208}, {1, 2, 48, 240}};
+
 __device__ __forceinline__ int group_of(int row) {
     int g = 0;
 #pragma unroll
@@ -85,58 +107,31 @@ __device__ __forceinline__ int group_of(int row) {
     return g;
 }
 
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcpf(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float2 bf2f(uint32_t u) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_f16(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
 __device__ __forceinline__ uint4 pack8_f16(const float* v) {
-    uint4 u;
-    __half2* p = reinterpret_cast<__half2*>(&u);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) p[e] = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
-    return u;
+    return make_uint4(pack_f16(v[0], v[1]), pack_f16(v[2], v[3]), pack_f16(v[4], v[5]), pack_f16(v[6], v[7]));
 }
-__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
-    uint4 u;
-    __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) p[e] = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
-    return u;
-}
-
-// eight fp16 / fp32 values from shared memory (16-byte aligned) as fp32
-__device__ __forceinline__ void lds_h8(const __half* p, float (&x)[8]) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
-    const __half2* h = reinterpret_cast<const __half2*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = __half22float2(h[i]);
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
-    }
-}
-__device__ __forceinline__ void lds_f8(const float* p, float (&x)[8]) {
-    const float4 a = reinterpret_cast<const float4*>(p)[0];
-    const float4 b = reinterpret_cast<const float4*>(p)[1];
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-__device__ __forceinline__ void sts_f8(float* p, const float (&x)[8]) {
-    reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
-    reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
-}
-
-// One-instruction reciprocal (max error 1 ulp); every argument here is a
-// normal number in [e^-75, 1].
-__device__ __forceinline__ float rcp_approx(float y) {
-    float r;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
-    return r;
-}
-
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void sts32(unsigned char* p, uint32_t v) { *reinterpret_cast<uint32_t*>(p) = v; }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
@@ -151,8 +146,8 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// One diagonal of the blockwise inverse (block pairs (b + d, b)), with the
-// inner products unrolled so every load is issued ahead of its FMA.
+// One diagonal of the blockwise inverse (block pairs (b + Dg, b)):
+//   M_ab = sum_{k=b}^{a-1} A_ak X_kb  (kept in A's unused upper block (b, a)),  X_ab = -X_aa M_ab
 template <int Dg>
 __device__ __forceinline__ void solve_level(float* Am, float* Xm, int tid) {
     constexpr int nblk = 4 - Dg;
@@ -180,374 +175,475 @@ __device__ __forceinline__ void solve_level(float* Am, float* Xm, int tid) {
     __syncthreads();
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+// Asynchronous 16-byte copies of one item's raw rows into shared memory, by
+// all threads.  q/k/v rows 0-2 are the three tokens before the chunk: earlier
+// rows of the same sequence, or the conv ring at a sequence start (left
+// unloaded, and read as zero, when there is no ring).
+__device__ __forceinline__ void issue_raw(const PrepArgs& a, int item, uint32_t base, int tid) {
+    const int H = a.H, W = H * D;
+    const ChunkDesc cd = a.chunks[item / H];
+    const int h = item % H, len = cd.len;
+    const int halo = (cd.pos > 0 || a.ring_in != nullptr) ? RING : 0;
+    const int r0 = RING - halo;                 // first loaded raw row of a q/k/v plane
+    const int n16 = (halo + len) * 16;          // 16-byte pieces per q/k/v plane
+    const size_t hoff = (size_t)h * D;
+#pragma unroll
+    for (int pl = 0; pl < 3; ++pl) {
+        const __nv_bfloat16* plane = static_cast<const __nv_bfloat16*>(pl == 0 ? a.q : (pl == 1 ? a.k : a.v));
+        for (int i = tid; i < n16; i += PT) {
+            const int r = r0 + (i >> 4), piece = i & 15;
+            const __nv_bfloat16* src;
+            if (cd.pos + r - RING >= 0)
+                src = plane + (size_t)(cd.t0 + r - RING) * W + hoff;
+            else  // sequence start: ring slot r (slot 0 oldest)
+                src = static_cast<const __nv_bfloat16*>(a.ring_in) + (((size_t)cd.seq * 3 + pl) * RING + r) * W + hoff;
+            cp_async16(base + S_RQ + (uint32_t)pl * RAW_ROWS * ROW_B + (uint32_t)r * ROW_B + 16 * piece, src + 8 * piece);
+        }
+    }
+    const __nv_bfloat16* zp = static_cast<const __nv_bfloat16*>(a.z) + (size_t)cd.t0 * W + hoff;
+    for (int i = tid; i < len * 16; i += PT) {
+        const int r = i >> 4, piece = i & 15;
+        cp_async16(base + S_RZ + (uint32_t)r * ROW_B + 16 * piece, zp + (size_t)r * W + 8 * piece);
+    }
+    cp_async_commit();
+}
+
+__device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
+__device__ __forceinline__ float2 h2f(uint32_t u) { return __half22float2(*reinterpret_cast<const __half2*>(&u)); }
+
 __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char* sb = smem_raw + (base - raw);
-    float* G = reinterpret_cast<float*>(sb + S_G);
-    float* Y = reinterpret_cast<float*>(sb + S_Y);
-    float* Xm = reinterpret_cast<float*>(sb + S_Y);
-    const __half* KH = reinterpret_cast<const __half*>(sb + S_KH);
-    const __half* QH = reinterpret_cast<const __half*>(sb + S_QH);
-    const __half* VH = reinterpret_cast<const __half*>(sb + S_VH);
     float* Am = reinterpret_cast<float*>(sb + S_AM);
-    unsigned char* ptile = sb + S_PT;
-    float* Mt = reinterpret_cast<float*>(sb + S_MT);
+    float* Xm = reinterpret_cast<float*>(sb + S_XM);
+    float* nrm = reinterpret_cast<float*>(sb + S_NRM);
+    float* tot = reinterpret_cast<float*>(sb + S_TOT);
     float* bt = reinterpret_cast<float*>(sb + S_BT);
-    const uint32_t bar = base + S_BAR;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sb + S_BAR + 16);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sb + S_BAR + 20);
+    const uint32_t bar_mma1 = base + S_BAR + 8, bar_mma2 = base + S_BAR + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sb + S_BAR + 24);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sb + S_BAR + 28);
 
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, W = H * D;
-    const int chunk = blockIdx.x / H, h = blockIdx.x % H;
-    const ChunkDesc cd = a.chunks[chunk];
-    const int L = cd.len, t0 = cd.t0;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const __half* qh = static_cast<const __half*>(a.qh);
-    const __half* kh = static_cast<const __half*>(a.kh);
-    const __half* vh = static_cast<const __half*>(a.vh);
-    const size_t hb = (size_t)h * D;
-    auto gidx = [&](int r, int i) { return (size_t)(t0 + r) * W + hb + i; };
+    const int n_items = a.n_chunks * H;
+    const int o = warp >> 1;                       // token octet
+    const int a_sub = o >> 1;                      // 16-token sub-tile of the octet
+    const int c0 = 2 * (32 * (warp & 1) + lane);   // first of this thread's two channels
+    const int tok0 = 8 * o;
 
     if (warp == 0) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
         ptx::tmem_relinquish();
     }
     if (tid == 0) {
-        ptx::mbar_init(bar, 1);
+        ptx::mbar_init(bar_mma1, 1);
+        ptx::mbar_init(bar_mma2, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
-
-    // ---- 1. G, k^, q^, v^ into shared memory: three cp.async groups, all in
-    // flight at once, each awaited where it is first needed
-    for (int idx = tid; idx < C * 32; idx += PT) {
-        const int r = idx >> 5, v4 = idx & 31;
-        const int rr = r < L ? r : L - 1;
-        cp_async16(sb + S_G + 16 * idx, a.gcum + gidx(rr, 4 * v4));
-    }
-    cp_async_commit();
-    for (int idx = tid; idx < C * 16; idx += PT) {
-        const int r = idx >> 4, v8 = idx & 15;
-        if (r < L) {
-            cp_async16(sb + S_KH + 16 * idx, kh + gidx(r, 8 * v8));
-            cp_async16(sb + S_QH + 16 * idx, qh + gidx(r, 8 * v8));
-        } else {
-            reinterpret_cast<uint4*>(sb + S_KH)[idx] = make_uint4(0, 0, 0, 0);
-            reinterpret_cast<uint4*>(sb + S_QH)[idx] = make_uint4(0, 0, 0, 0);
-        }
-    }
-    cp_async_commit();
-    for (int idx = tid; idx < C * 16; idx += PT) {
-        const int r = idx >> 4, v8 = idx & 15;
-        if (r < L) cp_async16(sb + S_VH + 16 * idx, vh + gidx(r, 8 * v8));
-        else reinterpret_cast<uint4*>(sb + S_VH)[idx] = make_uint4(0, 0, 0, 0);
-    }
-    cp_async_commit();
-    if (tid < C) bt[tid] = tid < L ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
-    for (int idx = tid; idx < 512; idx += PT) reinterpret_cast<uint4*>(ptile)[idx] = make_uint4(0, 0, 0, 0);
-    cp_async_wait_group<2>();  // G
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if ((int)blockIdx.x < n_items) issue_raw(a, blockIdx.x, base, tid);
+    int mma_pending = 0;                            // thread 0: 1 = bar_mma1, 2 = bar_mma2 in flight
+    uint32_t k_iter = 0;
 
-    // ---- 2. Y_s = e^{G_en(b) - G_s} and the per-sub-tile factors (8 channels per step)
-    for (int idx = tid; idx < C * 16; idx += PT) {
-        const int r = idx >> 4, ch = idx & 15;
-        const int en = min((r & ~15) + 15, L - 1);
-        float g[8], ge[8], y[8];
-        lds_f8(G + r * D + 8 * ch, g);
-        lds_f8(G + en * D + 8 * ch, ge);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = __expf(ge[e] - g[e]);
-        sts_f8(Y + r * LDY + 8 * ch, y);
-    }
-    for (int idx = tid; idx < 10 * D; idx += PT) {
-        const int m = idx >> 7, i = idx & 127;
-        int st, en;
-        if (m < 6) { st = min(16 * kPairA[m], L - 1); en = min(16 * kPairB[m] + 15, L - 1); }
-        else { st = min(16 * (m - 6) + 15, L - 1); en = min(16 * (m - 6), L - 1); }  // e^{G_en(a) - G_st(a)}
-        Mt[idx] = __expf(G[st * D + i] - G[en * D + i]);
-    }
-    __syncthreads();
-
-    // ---- 3. right operand R_s = k_s Y_s and the 256 left rows (bf16, swizzled).
-    // One item = (token r, 8 channels): the reciprocal 1/Y_r is formed once and
-    // every left row that token appears in (A rows for b <= a, P rows for
-    // b < a) is written from it.
-    cp_async_wait_group<1>();  // k^, q^
-    __syncthreads();
-    for (int idx = tid; idx < C * 16; idx += PT) {
-        const int r = idx >> 4, ch = idx & 15;
-        const int ta = r >> 4;
-        float k8[8], q8[8], y8[8], iy[8], v[8];
-        lds_h8(KH + r * D + 8 * ch, k8);
-        lds_h8(QH + r * D + 8 * ch, q8);
-        lds_f8(Y + r * LDY + 8 * ch, y8);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) { v[e] = k8[e] * y8[e]; iy[e] = rcp_approx(y8[e]); }
-        *reinterpret_cast<uint4*>(sb + S_RT + sw128_off(r, 8 * ch, C)) = pack8_bf16(v);
-        float va[8];
-        lds_f8(Mt + (6 + ta) * D + 8 * ch, va);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) va[e] *= iy[e];  // e^{G_r - G_st(a)} = e^{G_en(a) - G_st(a)} / Y_r
-        for (int b = 0; b <= ta; ++b) {
-            // A row of (column sub-tile b, r)
-            const int arow = kGroup[b][3] + (r - kGroup[b][2]);
-            float f[8];
-            if (b == ta) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = iy[e];
-            } else {
-                float cab[8];
-                lds_f8(Mt + pair_of(ta, b) * D + 8 * ch, cab);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = va[e] * cab[e];
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = k8[e] * f[e];
-            *reinterpret_cast<uint4*>(sb + S_LAP + (arow >> 7) * 32768 + sw128_off(arow & 127, 8 * ch, 128)) =
-                pack8_bf16(v);
-            if (b < ta) {  // off-diagonal P row of (b, r)
-                const int prow = kGroup[4 + b][3] + (r - kGroup[4 + b][2]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = q8[e] * f[e];
-                *reinterpret_cast<uint4*>(sb + S_LAP + (prow >> 7) * 32768 + sw128_off(prow & 127, 8 * ch, 128)) =
-                    pack8_bf16(v);
-            }
-        }
-    }
-    ptx::fence_async_smem();
-    ptx::tc_fence_before();
-    __syncthreads();
-
-    // ---- 4. A and the off-diagonal P blocks on the tensor cores
-    constexpr uint32_t IDESC_BF16_N64 = ptx::idesc_bf16_f32(128, 64);
-    constexpr uint32_t IDESC_F16_N64 = ptx::idesc_f16_f32(128, 64);
-    if (tid == 0) {
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t koff = (kk & 3) * 32;
-            const uint64_t bR = ptx::sdesc_sw128(base + S_RT + (kk >> 2) * 8192 + koff);
-            const uint64_t a0 = ptx::sdesc_sw128(base + S_LAP + (kk >> 2) * 16384 + koff);
-            const uint64_t a1 = ptx::sdesc_sw128(base + S_LAP + 32768 + (kk >> 2) * 16384 + koff);
-            ptx::mma_f16(tmem, a0, bR, IDESC_BF16_N64, kk > 0);
-            ptx::mma_f16(tmem + 64, a1, bR, IDESC_BF16_N64, kk > 0);
-        }
-        ptx::mma_commit(bar);
-    }
-
-    // ---- 5. diagonal blocks of P in fp32 while the MMAs run: e^{G_r - G_s} = Y_s / Y_r.
-    // Thread = (sub-tile, 4x4 block, K quarter); the quarters interleave 8-channel
-    // chunks so that neighbouring lanes read different banks.
-    for (int idx = tid; idx < C * LDS; idx += PT) Am[idx] = 0.f;
-    __syncthreads();
-    {
-        const int ta = tid >> 7, rem = tid & 127;
-        const int blk = rem >> 3, kq = rem & 7;   // 16 blocks of 4x4 x 8 interleaved K slices
-        const int br = blk >> 2, bc = blk & 3;
-        float acc[4][4];
-#pragma unroll
-        for (int x = 0; x < 4; ++x)
-#pragma unroll
-            for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
-        const int r0 = 16 * ta + 4 * br, s0 = 16 * ta + 4 * bc;
-        if (bc <= br) {
 #pragma unroll 1
-            for (int c8 = kq; c8 < 16; c8 += 8) {
-                float lq[4][8], rr[4][8];
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++k_iter) {
+        const uint32_t par = k_iter & 1u;
+        const ChunkDesc cd = a.chunks[item / H];
+        const int h = item % H, len = cd.len;
+        unsigned char* rec = static_cast<unsigned char*>(a.records) + (size_t)item * REC_BYTES;
+
+        // ---- per-item constants (issued before the wait)
+        float2 wt[3][4];   // conv taps of the two channels
 #pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    float q8[8], yr[8], k8[8], ys[8];
-                    lds_h8(QH + (r0 + x) * D + 8 * c8, q8);
-                    lds_f8(Y + (r0 + x) * LDY + 8 * c8, yr);
-                    lds_h8(KH + (s0 + x) * D + 8 * c8, k8);
-                    lds_f8(Y + (s0 + x) * LDY + 8 * c8, ys);
+        for (int pl = 0; pl < 3; ++pl) {
+            const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.conv_w + ((size_t)pl * W + h * D + c0) * CONV_K));
+            const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.conv_w + ((size_t)pl * W + h * D + c0 + 1) * CONV_K));
+            wt[pl][0] = make_float2(w0.x, w1.x); wt[pl][1] = make_float2(w0.y, w1.y);
+            wt[pl][2] = make_float2(w0.z, w1.z); wt[pl][3] = make_float2(w0.w, w1.w);
+        }
+        const float2 dtb = __ldg(reinterpret_cast<const float2*>(a.dt_bias + h * D + c0));
+        const float eA = __expf(__ldg(a.A_log + h));
+        float b_raw = 0.f;
+        if (tid < len) b_raw = __bfloat162float(static_cast<const __nv_bfloat16*>(a.b)[(size_t)(cd.t0 + tid) * H + h]);
+        const bool zero_halo = cd.pos == 0 && a.ring_in == nullptr;
+
+        cp_async_wait_all();
+        __syncthreads();
+
+        // ---- 1. conv + SiLU of q, k, v (kept as fp16 pairs); gate; sums of squares
+        uint32_t aq[8], ak[8], av[8];
+        float sq[16];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        lq[x][e] = q8[e] * rcp_approx(yr[e]);
-                        rr[x][e] = k8[e] * ys[e];
+        for (int pl = 0; pl < 3; ++pl) {
+            float2 xr[11];
+#pragma unroll
+            for (int j = 0; j < 11; ++j) {
+                const int row = tok0 + j;
+                const uint32_t u = *reinterpret_cast<const uint32_t*>(sb + S_RQ + pl * RAW_ROWS * ROW_B + row * ROW_B + 2 * c0);
+                xr[j] = (zero_halo && row < RING) ? make_float2(0.f, 0.f) : bf2f(u);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float2 acc = __fmul2_rn(wt[pl][0], xr[j]);
+                acc = __ffma2_rn(wt[pl][1], xr[j + 1], acc);
+                acc = __ffma2_rn(wt[pl][2], xr[j + 2], acc);
+                acc = __ffma2_rn(wt[pl][3], xr[j + 3], acc);
+                // x sigmoid(x) with sigmoid(x) = (1 + tanh(x / 2)) / 2 in half precision: the
+                // result is rounded to fp16 next, and the error (about 2^-11 of x) is at that level
+                const float2 hx = __fmul2_rn(acc, f2(0.5f));
+                const __half2 hin = __float22half2_rn(hx);
+                uint32_t t;
+                asm("tanh.approx.f16x2 %0, %1;" : "=r"(t) : "r"(*reinterpret_cast<const uint32_t*>(&hin)));
+                const float2 y = __fmul2_rn(acc, __ffma2_rn(h2f(t), f2(0.5f), f2(0.5f)));
+                const bool valid = tok0 + j < len;
+                const uint32_t hv = valid ? pack_f16(y.x, y.y) : 0u;
+                if (pl == 0) { aq[j] = hv; sq[j] = valid ? fmaf(y.x, y.x, y.y * y.y) : 0.f; }
+                if (pl == 1) { ak[j] = hv; sq[8 + j] = valid ? fmaf(y.x, y.x, y.y * y.y) : 0.f; }
+                if (pl == 2) av[j] = hv;
+            }
+        }
+        float2 gc[8];
+        float2 run = make_float2(0.f, 0.f);
+        {
+            const float2 eA2 = f2(eA), nl2 = f2(-LOG2E), lb2 = f2(a.lb);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t u = *reinterpret_cast<const uint32_t*>(sb + S_RZ + (tok0 + j) * ROW_B + 2 * c0);
+                const float2 sarg = __fmul2_rn(__fmul2_rn(__fadd2_rn(bf2f(u), dtb), eA2), nl2);
+                const float2 g = __fmul2_rn(lb2, make_float2(rcpf(1.f + ex2f(sarg.x)), rcpf(1.f + ex2f(sarg.y))));
+                if (tok0 + j < len) run = __fadd2_rn(run, g);
+                gc[j] = run;
+            }
+        }
+        // sums of squares of q (values 0-7) and k (8-15) per token, reduce-scattered
+        // over the warp: afterwards lanes 2v and 2v+1 hold value v's sum over 64 channels
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const bool up = lane & 16;
+            const float send = up ? sq[i] : sq[i + 8], keep = up ? sq[i + 8] : sq[i];
+            sq[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const bool up = lane & 8;
+            const float send = up ? sq[i] : sq[i + 4], keep = up ? sq[i + 4] : sq[i];
+            sq[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const bool up = lane & 4;
+            const float send = up ? sq[i] : sq[i + 2], keep = up ? sq[i + 2] : sq[i];
+            sq[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+        {
+            const bool up = lane & 2;
+            const float send = up ? sq[0] : sq[1], keep = up ? sq[1] : sq[0];
+            sq[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        }
+        sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], 1);
+        if ((lane & 1) == 0) nrm[warp * 16 + (lane >> 1)] = sq[0];
+        *reinterpret_cast<float2*>(tot + o * D + c0) = run;
+        if (tid < C) bt[tid] = tid < len ? rcpf(1.f + ex2f(-b_raw * LOG2E)) : 0.f;
+        __syncthreads();
+
+        // ---- norms (lane 2v, 2v+1 computes value v; then broadcast)
+        float nv;
+        {
+            const int v = lane >> 1;
+            const float ss = nrm[(2 * o) * 16 + v] + nrm[(2 * o + 1) * 16 + v];
+            nv = rsqrtf(ss + a.l2_eps) * (v < 8 ? a.q_scale : 1.f);
+        }
+        // ---- cumulative gate: prefix over octets, sub-tile ends, last token
+        float2 pre = make_float2(0.f, 0.f), gen[4];
+        {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int oo = 0; oo < 8; ++oo) {
+                const float2 t2 = *reinterpret_cast<const float2*>(tot + oo * D + c0);
+                if (oo == o) pre = acc;
+                acc = __fadd2_rn(acc, t2);
+                if (oo & 1) gen[oo >> 1] = acc;
+            }
+        }
+        const float2 ge = a_sub == 0 ? gen[0] : a_sub == 1 ? gen[1] : a_sub == 2 ? gen[2] : gen[3];
+        const float2 L2 = f2(LOG2E);
+        // per-channel factors: E = e^{G_en(a)}, F = e^{G_last - G_en(a)}, Cb = e^{G_en(a) - G_en(b)}
+        const float2 E = make_float2(ex2f(ge.x * LOG2E), ex2f(ge.y * LOG2E));
+        const float2 F = make_float2(ex2f((gen[3].x - ge.x) * LOG2E), ex2f((gen[3].y - ge.y) * LOG2E));
+        float2 Cb[3];
+#pragma unroll
+        for (int b = 0; b < 3; ++b) Cb[b] = make_float2(ex2f((ge.x - gen[b].x) * LOG2E), ex2f((ge.y - gen[b].y) * LOG2E));
+        if (o == 0)
+            *reinterpret_cast<float2*>(rec + REC_DECAY + 4 * c0) =
+                make_float2(ex2f(gen[3].x * LOG2E), ex2f(gen[3].y * LOG2E));
+        const float2 dofs = __fmul2_rn(__fadd2_rn(pre, make_float2(-ge.x, -ge.y)), L2);  // (G_oct_start - G_en(a)) log2 e
+
+        // ---- 2. operand tiles.  Per token: R (hi, lo), the A / P left rows, the
+        // diagonal P rows (hi, lo), Q+ and Kt to the record; (k e^G) and v stay
+        // packed for the later fp16 MMAs.
+        uint32_t kt[2][4], kp[2][4], vp[2][4];
+        uint32_t kt_prev = 0, kp_prev = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int r = tok0 + j;
+            const float nq = __shfl_sync(0xffffffffu, nv, 2 * j);
+            const float nk = __shfl_sync(0xffffffffu, nv, 16 + 2 * j);
+            const float2 q = __fmul2_rn(h2f(aq[j]), f2(nq));
+            const float2 k = __fmul2_rn(h2f(ak[j]), f2(nk));
+            const float2 d = __ffma2_rn(gc[j], L2, dofs);                  // (G_r - G_en(a)) log2 e >= 0
+            const float2 y = make_float2(ex2f(-d.x), ex2f(-d.y));          // Y  = e^{G_en(a) - G_r} <= 1
+            const float2 iy = make_float2(ex2f(d.x), ex2f(d.y));           // iY = e^{G_r - G_en(a)} >= 1
+            const float2 ky = __fmul2_rn(k, y);
+            const uint32_t rh = pack_bf16(ky.x, ky.y);
+            const float2 rlo = __fadd2_rn(ky, make_float2(-bf2f(rh).x, -bf2f(rh).y));
+            sts32(sb + S_RH + sw128_off(r, c0, C), rh);
+            sts32(sb + S_RL + sw128_off(r, c0, C), pack_bf16(rlo.x, rlo.y));
+            const float2 ki = __fmul2_rn(k, iy), qi = __fmul2_rn(q, iy);
+            {   // A row of the diagonal sub-tile
+                const int R = kGroup[a_sub][3] + (r - kGroup[a_sub][2]);
+                sts32(sb + S_LAP + (R >> 7) * 32768 + sw128_off(R & 127, c0, 128), pack_bf16(ki.x, ki.y));
+            }
+#pragma unroll
+            for (int b = 0; b < 3; ++b) {
+                if (b < a_sub) {
+                    const int RA = kGroup[b][3] + (r - kGroup[b][2]);
+                    const int RP = kGroup[4 + b][3] + (r - kGroup[4 + b][2]);
+                    const float2 kf = __fmul2_rn(ki, Cb[b]), qf = __fmul2_rn(qi, Cb[b]);
+                    sts32(sb + S_LAP + (RA >> 7) * 32768 + sw128_off(RA & 127, c0, 128), pack_bf16(kf.x, kf.y));
+                    sts32(sb + S_LAP + (RP >> 7) * 32768 + sw128_off(RP & 127, c0, 128), pack_bf16(qf.x, qf.y));
+                }
+            }
+            const uint32_t qh = pack_bf16(qi.x, qi.y);
+            const float2 qlo = __fadd2_rn(qi, make_float2(-bf2f(qh).x, -bf2f(qh).y));
+            sts32(sb + S_QD + sw128_off(r, c0, 128), qh);
+            sts32(sb + S_QD + sw128_off(64 + r, c0, 128), pack_bf16(qlo.x, qlo.y));
+            // record: Q+ = q e^{G} = q iY E
+            const float2 qp = __fmul2_rn(qi, E);
+            *reinterpret_cast<uint32_t*>(rec + REC_Q + sw128_off(r, c0, C)) = pack_f16(qp.x, qp.y);
+            // Kt = k e^{G_last - G} = k Y F;  (k e^G) = k iY E;  v.  Pairs of tokens are
+            // transposed into per-channel rows: word w of channel e holds tokens 2w, 2w+1.
+            const float2 ktf = __fmul2_rn(ky, F), kpf = __fmul2_rn(ki, E);
+            const uint32_t t_kt = pack_f16(ktf.x, ktf.y), t_kp = pack_f16(kpf.x, kpf.y);
+            if (j & 1) {
+                const int w = j >> 1;
+                kt[0][w] = __byte_perm(kt_prev, t_kt, 0x5410);
+                kt[1][w] = __byte_perm(kt_prev, t_kt, 0x7632);
+                kp[0][w] = __byte_perm(kp_prev, t_kp, 0x5410);
+                kp[1][w] = __byte_perm(kp_prev, t_kp, 0x7632);
+                vp[0][w] = __byte_perm(av[j - 1], av[j], 0x5410);
+                vp[1][w] = __byte_perm(av[j - 1], av[j], 0x7632);
+            } else {
+                kt_prev = t_kt;
+                kp_prev = t_kp;
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+            *reinterpret_cast<uint4*>(rec + REC_KT + sw128_off(c0 + e, tok0, 128)) =
+                make_uint4(kt[e][0], kt[e][1], kt[e][2], kt[e][3]);
+        ptx::fence_async_smem();
+        ptx::tc_fence_before();
+        __syncthreads();
+
+        // ---- 3. A, off-diagonal P, diagonal P on the tensor cores
+        constexpr uint32_t IDESC_BF16_N64 = ptx::idesc_bf16_f32(128, 64);
+        if (tid == 0) {
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t koff = (kk & 3) * 32, pn = kk >> 2;
+                const uint64_t bR = ptx::sdesc_sw128(base + S_RH + pn * 8192 + koff);
+                ptx::mma_f16(tmem + TM_D0, ptx::sdesc_sw128(base + S_LAP + pn * 16384 + koff), bR, IDESC_BF16_N64, kk > 0);
+                ptx::mma_f16(tmem + TM_D1, ptx::sdesc_sw128(base + S_LAP + 32768 + pn * 16384 + koff), bR, IDESC_BF16_N64,
+                             kk > 0);
+            }
+            // diagonal P: hi*hi, then lo*hi (rows 64-127 of the QD tile as the A rows), then hi*lo
+#pragma unroll
+            for (int part = 0; part < 3; ++part) {
+                const uint32_t abase = base + S_QD + (part == 1 ? 8192u : 0u);
+                const uint32_t bbase = base + (part == 2 ? S_RL : S_RH);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = (kk & 3) * 32, pn = kk >> 2;
+                    ptx::mma_f16(tmem + TM_D2, ptx::sdesc_sw128(abase + pn * 16384 + koff),
+                                 ptx::sdesc_sw128(bbase + pn * 8192 + koff), IDESC_BF16_N64, (part > 0 || kk > 0));
+                }
+            }
+            ptx::mma_commit(bar_mma1);
+            mma_pending = 1;
+        }
+        // the raw rows are consumed: fetch the next item's while this one finishes
+        if (item + (int)gridDim.x < n_items) issue_raw(a, item + gridDim.x, base, tid);
+        if (!ptx::mbar_wait(bar_mma1, par, WAIT_LIMIT_NS)) *abort_flag = 1;
+        ptx::tc_fence_after();
+        if (tid == 0 && !*abort_flag) mma_pending = 0;
+
+        // ---- 4. read out A (to fp32 Am, times beta_r) and P (to the record); (k e^G)^T, v^T tiles
+        if (!*abort_flag) {
+            if (warp < 8) {
+                const int row = 128 * (warp >> 2) + 32 * (warp & 3) + lane;
+                const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (warp < 4 ? TM_D0 : TM_D1);
+                const int g = group_of(row);
+                const int isP = kGroup[g][0], b = kGroup[g][1];
+                const int r = kGroup[g][2] + (row - kGroup[g][3]);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    float v[16];
+                    tmem_ld16(taddr + 16 * q4, v);
+                    if (q4 == b) {
+                        if (isP) {
+                            *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * b, C)) = pack8_f16(v);
+                            *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * b + 8, C)) = pack8_f16(v + 8);
+                        } else {
+                            const float be = bt[r];
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj)
+                                if (16 * b + jj < r) Am[r * LDS + 16 * b + jj] = be * v[jj];
+                        }
                     }
                 }
+            } else if (warp < 10) {
+                const int r = 32 * (warp & 3) + lane;                 // 0..63
+                const int ta = r >> 4;
+                const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + TM_D2;
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    const int blk = 2 * (warp & 1) + q2;              // sub-tiles of this warp's rows
+                    float v[16];
+                    tmem_ld16(taddr + 16 * blk, v);
+                    if (blk == ta) {
 #pragma unroll
-                    for (int x = 0; x < 4; ++x)
+                        for (int jj = 0; jj < 16; ++jj)
+                            if (16 * ta + jj > r) v[jj] = 0.f;
+                        *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * ta, C)) = pack8_f16(v);
+                        *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * ta + 8, C)) = pack8_f16(v + 8);
+                    }
+                }
+                for (int tb = ta + 1; tb < 4; ++tb) {
+                    *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * tb, C)) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * tb + 8, C)) = make_uint4(0, 0, 0, 0);
+                }
+            }
 #pragma unroll
-                        for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(lq[x][e], rr[y][e], acc[x][y]);
+            for (int e = 0; e < 2; ++e) {
+                *reinterpret_cast<uint4*>(sb + S_KPT + sw128_off(c0 + e, tok0, 128)) =
+                    make_uint4(kp[e][0], kp[e][1], kp[e][2], kp[e][3]);
+                *reinterpret_cast<uint4*>(sb + S_VT + sw128_off(c0 + e, tok0, 128)) =
+                    make_uint4(vp[e][0], vp[e][1], vp[e][2], vp[e][3]);
             }
         }
-#pragma unroll
-        for (int x = 0; x < 4; ++x)
-#pragma unroll
-            for (int y = 0; y < 4; ++y) {
-                float v = acc[x][y];
-                v += __shfl_xor_sync(0xffffffffu, v, 1);
-                v += __shfl_xor_sync(0xffffffffu, v, 2);
-                v += __shfl_xor_sync(0xffffffffu, v, 4);
-                acc[x][y] = v;
-            }
-        if (kq == 0 && bc <= br) {
-#pragma unroll
-            for (int x = 0; x < 4; ++x)
-#pragma unroll
-                for (int y = 0; y < 4; ++y)
-                    if (s0 + y <= r0 + x)
-                        *reinterpret_cast<__half*>(ptile + sw128_off(r0 + x, s0 + y, C)) = __float2half_rn(acc[x][y]);
-        }
-    }
+        ptx::tc_fence_before();
+        __syncthreads();
+        if (*abort_flag) break;
 
-    // ---- 6. A and off-diagonal P out of TMEM (warps 0-3: left tile 0, 4-7: tile 1)
-    if (!ptx::mbar_wait(bar, 0, WAIT_LIMIT_NS)) *abort_flag = 1;
-    ptx::tc_fence_after();
-    if (warp < 8) {
-        const int lane_row = 32 * (warp & 3) + (tid & 31);
-        const int row = (warp < 4 ? 0 : 128) + lane_row;
-        const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (warp < 4 ? 0 : 64);
-        const int g = group_of(row);
-        const int isP = kGroup[g][0], b = kGroup[g][1];
-        const int r = kGroup[g][2] + (row - kGroup[g][3]);
+        // ---- 5. X = (I + A)^{-1}: diagonal 16 x 16 inverses by forward substitution
+        if (tid < 64) {
+            const int ta = tid >> 4, j = tid & 15;
+            const int ob = 16 * ta;
+            float x[16];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            float v[16];
-            tmem_ld16(taddr + 16 * q4, v);  // columns s = 16 q4 .. 16 q4 + 15
-            if (q4 == b && !*abort_flag) {
-                if (isP) {
-                    *reinterpret_cast<uint4*>(ptile + sw128_off(r, 16 * b, C)) = pack8_f16(v);
-                    *reinterpret_cast<uint4*>(ptile + sw128_off(r, 16 * b + 8, C)) = pack8_f16(v + 8);
-                } else {
-                    const float be = bt[r];
+            for (int r = 0; r < 16; ++r) {
+                float t = (r == j) ? 1.f : 0.f;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (16 * b + j < r) Am[r * LDS + 16 * b + j] = be * v[j];
+                for (int s = 0; s < r; ++s) t = fmaf(-Am[(ob + r) * LDS + ob + s], x[s], t);
+                x[r] = (r < j) ? 0.f : t;
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) Xm[(ob + r) * LDS + ob + j] = x[r];
+        }
+        __syncthreads();
+        solve_level<1>(Am, Xm, tid);
+        solve_level<2>(Am, Xm, tid);
+        solve_level<3>(Am, Xm, tid);
+
+        // ---- 6. T = X Diag(beta) (fp16, blocks above the diagonal zero; rows 64-127 zero)
+        {
+            const int r = tid >> 3, ch = tid & 7;   // 512 threads = 64 rows x 8 column groups
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int s = 8 * ch + e;
+                v[e] = ((s >> 4) <= (r >> 4)) ? Xm[r * LDS + s] * bt[s] : 0.f;
+            }
+            *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 8 * ch, 128)) = pack8_f16(v);
+            *reinterpret_cast<uint4*>(sb + S_TT + 64 * 128 + 16 * tid) = make_uint4(0, 0, 0, 0);
+        }
+        ptx::fence_async_smem();
+        ptx::tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            ptx::tc_fence_after();
+            constexpr uint32_t IDESC_W = ptx::idesc_f16_f32(128, 128);
+            constexpr uint32_t IDESC_U = ptx::idesc_f16_f32(128, 64);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t dT = ptx::sdesc_sw128(base + S_TT + kk * 32);
+                ptx::mma_f16(tmem + TM_W, dT, ptx::sdesc_sw128(base + S_KPT + kk * 32), IDESC_W, kk > 0);
+                ptx::mma_f16(tmem + TM_U, ptx::sdesc_sw128(base + S_VT + kk * 32), dT, IDESC_U, kk > 0);
+            }
+            ptx::mma_commit(bar_mma2);
+            mma_pending = 2;
+        }
+        if (!ptx::mbar_wait(bar_mma2, par, WAIT_LIMIT_NS)) *abort_flag = 1;
+        ptx::tc_fence_after();
+        if (tid == 0 && !*abort_flag) mma_pending = 0;
+
+        // ---- 7. W (lanes = tokens 0-63) and U0^T (lanes = values) to the record
+        if (!*abort_flag) {
+            if (warp < 8 && (warp & 3) < 2) {       // warps 0,1: keys 0-63; warps 4,5: keys 64-127
+                const int r = 32 * (warp & 3) + lane;
+                const int kb = 64 * (warp >> 2);
+                const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + TM_W + kb;
+#pragma unroll
+                for (int h32 = 0; h32 < 2; ++h32) {
+                    float v[32];
+                    ptx::tmem_ld32(taddr + 32 * h32, v);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4*>(rec + REC_W + sw128_off(r, kb + 32 * h32 + 8 * q, C)) =
+                            pack8_f16(v + 8 * q);
+                }
+            } else if (warp >= 8 && warp < 12) {
+                const int vrow = 32 * (warp & 3) + lane;
+                const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + TM_U;
+#pragma unroll
+                for (int h32 = 0; h32 < 2; ++h32) {
+                    float v[32];
+                    ptx::tmem_ld32(taddr + 32 * h32, v);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4*>(rec + REC_UT + sw128_off(vrow, 32 * h32 + 8 * q, 128)) =
+                            pack8_f16(v + 8 * q);
                 }
             }
         }
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-
-    // ---- 7. X = (I + A)^{-1}: diagonal 16 x 16 inverses by forward substitution
-    for (int idx = tid; idx < C * LDS; idx += PT) Xm[idx] = 0.f;
-    __syncthreads();
-    if (tid < 64) {
-        const int ta = tid >> 4, j = tid & 15;
-        const int o = 16 * ta;
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float t = (r == j) ? 1.f : 0.f;
-#pragma unroll
-            for (int s = 0; s < r; ++s) t = fmaf(-Am[(o + r) * LDS + o + s], x[s], t);
-            x[r] = (r < j) ? 0.f : t;
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Xm[(o + r) * LDS + o + j] = x[r];
-    }
-    __syncthreads();
-    // off-diagonal blocks, one diagonal at a time: X_ab = -X_aa sum_{k=b}^{a-1} A_ak X_kb.
-    // The temporaries M_ab live in A's unused upper-right block (b, a).
-    solve_level<1>(Am, Xm, tid);
-    solve_level<2>(Am, Xm, tid);
-    solve_level<3>(Am, Xm, tid);
-    cp_async_wait_group<0>();  // v^
-    __syncthreads();
-
-    // ---- 8. operands of W^T and U0^T (fp16; the left tiles are dead, reuse their space)
-    //   TT[r][s] = X[r][s] beta_s ; KPT[key][s] = k_s e^{G_s} ; VT[val][s] = v_s
-    for (int idx = tid; idx < C * 8; idx += PT) {
-        const int r = idx >> 3, ch = idx & 7;
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = Xm[r * LDS + 8 * ch + e] * bt[8 * ch + e];
-        *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 8 * ch, C)) = pack8_f16(v);
-    }
-    for (int idx = tid; idx < D * 8; idx += PT) {
-        const int row = idx & 127, ch = idx >> 7;
-        float vk[8], vv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int s = 8 * ch + e;
-            vk[e] = __half2float(KH[s * D + row]) * __expf(G[s * D + row]);
-            vv[e] = __half2float(VH[s * D + row]);
-        }
-        *reinterpret_cast<uint4*>(sb + S_KPT + sw128_off(row, 8 * ch, 128)) = pack8_f16(vk);
-        *reinterpret_cast<uint4*>(sb + S_VT + sw128_off(row, 8 * ch, 128)) = pack8_f16(vv);
-    }
-    ptx::fence_async_smem();
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (tid == 0 && !*abort_flag) {
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bT = ptx::sdesc_sw128(base + S_TT + kk * 32);
-            const uint64_t aK = ptx::sdesc_sw128(base + S_KPT + kk * 32);
-            const uint64_t aV = ptx::sdesc_sw128(base + S_VT + kk * 32);
-            ptx::mma_f16(tmem + 128, aK, bT, IDESC_F16_N64, kk > 0);
-            ptx::mma_f16(tmem + 192, aV, bT, IDESC_F16_N64, kk > 0);
-        }
-        ptx::mma_commit(bar);
+        ptx::tc_fence_before();
+        __syncthreads();
+        if (*abort_flag) break;
     }
 
-    unsigned char* rec = static_cast<unsigned char*>(a.records) + ((size_t)chunk * H + h) * REC_BYTES;
-
-    // ---- 9. tiles that need no MMA, straight to the record: Q+ [tok][key], Kt^T [key][tok], P, decay
-    for (int idx = tid; idx < C * 16; idx += PT) {
-        const int r = idx >> 4, ch = idx & 15;
-        float q8[8], g8[8], v[8];
-        lds_h8(QH + r * D + 8 * ch, q8);
-        lds_f8(G + r * D + 8 * ch, g8);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = q8[e] * __expf(g8[e]);
-        *reinterpret_cast<uint4*>(rec + REC_Q + sw128_off(r, 8 * ch, C)) = pack8_f16(v);
-    }
-    for (int idx = tid; idx < D * 8; idx += PT) {
-        const int key = idx & 127, ch = idx >> 7;
-        const float glast = G[(C - 1) * D + key];
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int s = 8 * ch + e;
-            v[e] = __half2float(KH[s * D + key]) * __expf(glast - G[s * D + key]);
-        }
-        *reinterpret_cast<uint4*>(rec + REC_KT + sw128_off(key, 8 * ch, 128)) = pack8_f16(v);
-    }
-    for (int idx = tid; idx < 512; idx += PT)  // the 8 KiB P image
-        reinterpret_cast<uint4*>(rec + REC_P)[idx] = reinterpret_cast<const uint4*>(ptile)[idx];
-    if (tid < D) reinterpret_cast<float*>(rec + REC_DECAY)[tid] = expf(G[(C - 1) * D + tid]);
-
-    // ---- 10. W^T (warps 0-3, lane = key) through a shared-memory W tile; U0^T (warps 4-7, lane = value) direct
-    if (!ptx::mbar_wait(bar, 1, WAIT_LIMIT_NS)) *abort_flag = 1;
-    ptx::tc_fence_after();
-    if (warp < 8) {
-        const int row = 32 * (warp & 3) + (tid & 31);
-        const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (warp < 4 ? 128 : 192);
-#pragma unroll 1
-        for (int q4 = 0; q4 < 4; ++q4) {
-            float v[16];
-            tmem_ld16(taddr + 16 * q4, v);
-            if (warp < 4) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    *reinterpret_cast<__half*>(sb + S_RT + sw128_off(16 * q4 + j, row, C)) = __float2half_rn(v[j]);
-            } else if (!*abort_flag) {
-                *reinterpret_cast<uint4*>(rec + REC_UT + sw128_off(row, 16 * q4, 128)) = pack8_f16(v);
-                *reinterpret_cast<uint4*>(rec + REC_UT + sw128_off(row, 16 * q4 + 8, 128)) = pack8_f16(v + 8);
-            }
-        }
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (!*abort_flag) {
-        for (int idx = tid; idx < 1024; idx += PT)  // the 16 KiB W image, 16 bytes per thread step
-            reinterpret_cast<uint4*>(rec + REC_W)[idx] = reinterpret_cast<const uint4*>(sb + S_RT)[idx];
-    } else if (tid == 0) {
+    cp_async_wait_all();  // this thread's copies of a prefetch that was not consumed
+    if (*abort_flag && tid == 0) {
+        // record the timeout, then let this CTA's own MMAs land
         atomicExch(a.status, ERR_TIMEOUT);
+        const uint32_t par = k_iter & 1u;
+        if (mma_pending == 1) ptx::mbar_wait(bar_mma1, par, WAIT_LIMIT_NS);
+        if (mma_pending == 2) ptx::mbar_wait(bar_mma2, par, WAIT_LIMIT_NS);
     }
+    ptx::tc_fence_before();
+    __syncthreads();
     if (warp == 0) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
@@ -559,12 +655,19 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
 size_t chunk_prep_smem_bytes() { return SMEM_BYTES; }
 
 cudaError_t launch_chunk_prep(const PrepArgs& a, cudaStream_t s) {
+    const int64_t items = (int64_t)a.n_chunks * a.H;
+    if (items == 0) return cudaSuccess;
+    if (items > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int64_t blocks = (int64_t)a.n_chunks * a.H;
-    if (blocks == 0) return cudaSuccess;
-    chunk_prep_kernel<<<(unsigned)blocks, PT, SMEM_BYTES, s>>>(a);
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = items < sms ? items : sms;
+    chunk_prep_kernel<<<(unsigned)grid, PT, SMEM_BYTES, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -50,7 +50,8 @@ struct NaLayout {
 // Same region order as the caller-provided workspace of kda_prefill.
 NaLayout na_layout(int H, bool chunked, int32_t n, int64_t T, int64_t nc) {
     NaLayout L{};
-    const size_t W = (size_t)H * D, op = chunked ? 2 : 4;
+    const size_t W = (size_t)H * D, op = 4;
+    const size_t tw = chunked ? 0 : (size_t)T * W;  // pre-stage outputs: scan path only
     size_t off = 0;
     L.status = off; off += NA_ALIGN;
     L.meta = off;
@@ -59,13 +60,13 @@ NaLayout na_layout(int H, bool chunked, int32_t n, int64_t T, int64_t nc) {
     L.off_chunks = up(L.off_order + sizeof(int32_t) * (size_t)n, 16);
     L.meta_bytes = L.off_chunks + sizeof(ChunkDesc) * (size_t)nc;
     off = up(off + L.meta_bytes, NA_ALIGN);
-    L.qh = off; off = up(off + op * (size_t)T * W, NA_ALIGN);
-    L.kh = off; off = up(off + op * (size_t)T * W, NA_ALIGN);
-    L.vh = off; off = up(off + op * (size_t)T * W, NA_ALIGN);
-    L.g = off; off = up(off + 4 * (size_t)T * W, NA_ALIGN);
-    L.beta = off; off = up(off + 4 * (size_t)T * H, NA_ALIGN);
+    L.qh = off; off = up(off + op * tw, NA_ALIGN);
+    L.kh = off; off = up(off + op * tw, NA_ALIGN);
+    L.vh = off; off = up(off + op * tw, NA_ALIGN);
+    L.g = off; off = up(off + 4 * tw, NA_ALIGN);
+    L.beta = off; off = up(off + 4 * (chunked ? 0 : (size_t)T * H), NA_ALIGN);
     L.ocore = off;
-    if (!chunked) off = up(off + 4 * (size_t)T * W, NA_ALIGN);
+    off = up(off + 4 * tw, NA_ALIGN);
     L.rec = off;
     if (chunked) off = up(off + (size_t)REC_BYTES * (size_t)nc * H, NA_ALIGN);
     L.total = off;
@@ -182,8 +183,8 @@ extern "C" kda_status kda_prefill_noalloc(const kda_params* p, const void* q, co
                     n_seqs, H};
         if (launch_scan(sa, s) != cudaSuccess) return KDA_ERR_CUDA;
     } else {
-        if (launch_prestage(pa, io_bf16, 1, 1, s) != cudaSuccess) return KDA_ERR_CUDA;
-        PrepArgs pr{ws + L.qh, ws + L.kh, ws + L.vh, gbuf, beta, d_chunks, (int32_t)nc, H, ws + L.rec, status};
+        PrepArgs pr{q, k, v, z, b, ring_in, p->conv_w, p->A_log, p->dt_bias, p->gate_lower_bound, p->l2_eps, qs,
+                    d_chunks, (int32_t)nc, H, ws + L.rec, status};
         if (launch_chunk_prep(pr, s) != cudaSuccess) return KDA_ERR_CUDA;
         ChunkRecArgs ca{ws + L.rec, S_in, S_out, gout, p->norm_w, o, p->norm_eps, d_cu, d_coff, d_order, status,
                         n_seqs, H};
