@@ -64,6 +64,12 @@ __device__ __forceinline__ uint4 pack8_f16(const float* v) {
     return u;
 }
 
+__device__ __forceinline__ float tanh_fast(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // named barrier over `count` threads (ids 1 and 2; id 0 is __syncthreads)
 __device__ __forceinline__ void bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -90,11 +96,12 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
     // completing between their waits
     const uint32_t bar_mma23_0 = base + OFF_BAR + 24;    // + 8 * buffer (3)
     const uint32_t bar_ofree0 = base + OFF_BAR + 48;     // + 8 * buffer (3): D[b] read by the output warps
+    const uint32_t bar_drain = base + OFF_BAR + 104;     // completion of in-flight MMAs after a timeout
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sb + OFF_BAR + 72);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sb + OFF_BAR + 76);
-    // in-flight bookkeeping for the drain after a timeout (thread 0 only):
-    // [0],[1] load pending per stage and [2],[3] its parity; [4] MMA commit pending
-    // (barrier address), [5] its parity
+    // in-flight bookkeeping for the drain after a timeout (written by the issuing
+    // thread, read by thread 0): [0],[1] load pending per stage and [2],[3] its
+    // parity; [4] MMAs in flight
     int* pend = reinterpret_cast<int*>(sb + OFF_BAR + 80);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -117,6 +124,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
             ptx::mbar_init(bar_mma23_0 + 8 * b, 1);
             ptx::mbar_init(bar_ofree0 + 8 * b, 1);
         }
+        ptx::mbar_init(bar_drain, 1);
         *abort_flag = 0;
         for (int i = 0; i < 6; ++i) pend[i] = 0;
         ptx::fence_mbar_init();
@@ -133,10 +141,16 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
     auto issue_load = [&](int64_t c) {
         const int s = (int)(c & 1);
         ptx::mbar_expect_tx(bar_load0 + 8 * s, REC_BYTES);
-        ptx::bulk_g2s(base + s * STAGE_STRIDE, recs + ((size_t)(c0 + c) * H + h) * REC_BYTES, REC_BYTES,
-                      bar_load0 + 8 * s);
+        // four copies in flight at once rather than one long one
+        const unsigned char* src = recs + ((size_t)(c0 + c) * H + h) * REC_BYTES;
+#pragma unroll
+        for (int part = 0; part < 4; ++part)
+            ptx::bulk_g2s(base + s * STAGE_STRIDE + part * (REC_BYTES / 4), src + part * (REC_BYTES / 4),
+                          REC_BYTES / 4, bar_load0 + 8 * s);
         pend[s] = 1;
         pend[2 + s] = (int)((c >> 1) & 1);
+        if (c + 2 < nc)  // the record after next goes to L2 already
+            ptx::bulk_prefetch_l2(recs + ((size_t)(c0 + c + 2) * H + h) * REC_BYTES, REC_BYTES);
     };
     const size_t soff = ((size_t)n * H + h) * D * D;
 
@@ -169,49 +183,71 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
             if (*abort_flag) break;
             if (tid == 0) pend[s] = 0;
 
-            // ---- state transition: fp16 copy of S^T for MMA1, then S^T *= decay (per key column)
-            const float* decay = reinterpret_cast<const float*>(sp + REC_DECAY);
-#pragma unroll 1
-            for (int j = 2 * half; j < 2 * half + 2; ++j) {
-                float v[32];
-                ptx::tmem_ld32(tlane + 32 * j, v);
+            // ---- state transition: fp16 copy of S^T, the A operand of MMA1
+            float sv[2][32];
+#pragma unroll
+            for (int j2 = 0; j2 < 2; ++j2) {
+                const int j = 2 * half + j2;
+                ptx::tmem_ld32(tlane + 32 * j, sv[j2]);
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4*>(sb + OFF_ST + sw128_off(vrow, 32 * j + 8 * q, 128)) = pack8_f16(v + 8 * q);
-#pragma unroll
-                for (int x = 0; x < 32; ++x) v[x] *= decay[32 * j + x];
-                ptx::tmem_st32(tlane + 32 * j, v);
+                    *reinterpret_cast<uint4*>(sb + OFF_ST + sw128_off(vrow, 32 * j + 8 * q, 128)) =
+                        pack8_f16(sv[j2] + 8 * q);
             }
             ptx::fence_async_smem();
             ptx::tc_fence_before();
             bar_sync(1, NSTATE);
+            // MMA1a (the chain's critical path): D[buf][:, 0:64] = S^T W^T
             if (tid == 0) {
-                // D[buf] must have been read out by the output warps (chunk c - NBUF)
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = (kk & 3) * 32;  // 16 fp16 of K inside the 128-byte row
+                    const uint64_t ad = ptx::sdesc_sw128(base + OFF_ST + (kk >> 2) * 16384 + koff);
+                    const uint64_t bw = ptx::sdesc_sw128(stg + REC_W + (kk >> 2) * 8192 + koff);
+                    ptx::mma_f16(tmem + dcol, ad, bw, IDESC_N64, kk > 0);
+                }
+                ptx::mma_commit(bar_mma1);
+                pend[4] = 1;
+            }
+            // while it runs: S^T *= decay (per key column), back into TMEM before MMA2
+            {
+                const float* decay = reinterpret_cast<const float*>(sp + REC_DECAY);
+#pragma unroll
+                for (int j2 = 0; j2 < 2; ++j2) {
+                    const int j = 2 * half + j2;
+#pragma unroll
+                    for (int x = 0; x < 32; x += 4) {
+                        const float4 d4 = *reinterpret_cast<const float4*>(decay + 32 * j + x);
+                        const float2 lo = __fmul2_rn(make_float2(sv[j2][x], sv[j2][x + 1]), make_float2(d4.x, d4.y));
+                        const float2 hi = __fmul2_rn(make_float2(sv[j2][x + 2], sv[j2][x + 3]), make_float2(d4.z, d4.w));
+                        sv[j2][x] = lo.x; sv[j2][x + 1] = lo.y; sv[j2][x + 2] = hi.x; sv[j2][x + 3] = hi.y;
+                    }
+                    ptx::tmem_st32(tlane + 32 * j, sv[j2]);
+                }
+            }
+            // MMA1b (off the critical path): D[buf][:, 64:128] = S^T Q+^T, once the output
+            // warps have read D[buf] of chunk c - NBUF
+            if (tid == 0) {
                 bool ok = true;
                 if (c >= NBUF) ok = ptx::mbar_wait(bar_ofree0 + 8 * buf, use ^ 1u, WAIT_LIMIT_NS);
                 if (!ok) {
                     *abort_flag = 1;
                 } else {
-                    ptx::tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t koff = (kk & 3) * 32;  // 16 fp16 of K inside the 128-byte row
+                        const uint32_t koff = (kk & 3) * 32;
                         const uint64_t ad = ptx::sdesc_sw128(base + OFF_ST + (kk >> 2) * 16384 + koff);
-                        const uint64_t bw = ptx::sdesc_sw128(stg + REC_W + (kk >> 2) * 8192 + koff);
                         const uint64_t bq = ptx::sdesc_sw128(stg + REC_Q + (kk >> 2) * 8192 + koff);
-                        ptx::mma_f16(tmem + dcol, ad, bw, IDESC_N64, kk > 0);
                         ptx::mma_f16(tmem + dcol + 64, ad, bq, IDESC_N64, kk > 0);
                     }
-                    ptx::mma_commit(bar_mma1);
-                    pend[4] = (int)bar_mma1;
-                    pend[5] = (int)(c & 1);
                 }
             }
             // the abort flag (set by thread 0 above) is checked after this wait and barrier
             if (!*abort_flag && !ptx::mbar_wait(bar_mma1, (uint32_t)(c & 1), WAIT_LIMIT_NS)) *abort_flag = 1;
+            ptx::tc_fence_before();
             bar_sync(1, NSTATE);
             if (*abort_flag) break;
-            if (tid == 0) pend[4] = 0;
             ptx::tc_fence_after();
 
             // ---- U^T = U0^T - (W S)^T as the fp16 A operand of MMA2 / MMA3 (this warp: 32 tokens)
@@ -243,24 +279,16 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
                     const uint64_t au = ptx::sdesc_sw128(base + OFF_UT + kk * 32);
                     const uint64_t bk = ptx::sdesc_sw128(stg + REC_KT + kk * 32);
                     const uint64_t bp = ptx::sdesc_sw128(stg + REC_P + kk * 32);
-                    ptx::mma_f16(tmem, au, bk, IDESC_N128, 1);
-                    ptx::mma_f16(tmem + dcol + 64, au, bp, IDESC_N64, 1);
+                    ptx::mma_f16(tmem, au, bk, IDESC_N128, 1);             // S^T += U^T Kt
+                    ptx::mma_f16(tmem + dcol + 64, au, bp, IDESC_N64, 1);  // O^T += U^T P^T
                 }
                 ptx::mma_commit(bar_mma23_0 + 8 * buf);
-                pend[4] = (int)(bar_mma23_0 + 8 * buf);
-                pend[5] = (int)use;
             }
             if (!ptx::mbar_wait(bar_mma23_0 + 8 * buf, use, WAIT_LIMIT_NS)) *abort_flag = 1;
             bar_sync(1, NSTATE);
             if (*abort_flag) break;
             ptx::tc_fence_after();
-            if (tid == 0) {
-                pend[4] = 0;
-                if (c + 2 < nc) {
-                    ptx::fence_async_smem();
-                    issue_load(c + 2);
-                }
-            }
+            if (tid == 0) pend[4] = 0;  // every MMA issued so far has completed
         }
         if (!*abort_flag) {
             // final state: S_out[key][value] = S^T[value][key]
@@ -287,6 +315,25 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
         float wv[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) wv[e] = a.norm_w[16 * rseg + e];
+        // gate logits of this thread's two token rows, one chunk ahead of use
+        auto load_gout = [&](int64_t c, uint4 (&g)[2][2]) {
+            const int64_t rem = L - (int64_t)CHUNK_T * c;
+            const int Lc = rem < CHUNK_T ? (int)rem : CHUNK_T;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int t = 32 * hf + rt;
+                if (c < nc && t < Lc) {
+                    const uint4* src = reinterpret_cast<const uint4*>(
+                        gout + (size_t)(bos + (int64_t)CHUNK_T * c + t) * W + (size_t)h * D + 16 * rseg);
+                    g[hf][0] = __ldg(src);
+                    g[hf][1] = __ldg(src + 1);
+                } else {
+                    g[hf][0] = g[hf][1] = make_uint4(0, 0, 0, 0);
+                }
+            }
+        };
+        uint4 gcur[2][2], gnext[2][2];
+        load_gout(0, gcur);
 #pragma unroll 1
         for (int64_t c = 0; c < nc; ++c) {
             const int buf = (int)(c % NBUF);
@@ -294,7 +341,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
             const int64_t rem = L - (int64_t)CHUNK_T * c;
             const int Lc = rem < CHUNK_T ? (int)rem : CHUNK_T;
             const size_t row0 = (size_t)(bos + (int64_t)CHUNK_T * c);
+            load_gout(c + 1, gnext);
             if (!ptx::mbar_wait(bar_mma23_0 + 8 * buf, use, WAIT_LIMIT_NS)) *abort_flag = 1;
+            // the chain is done with stage c & 1: fetch chunk c + 2 into it (issuing bulk
+            // copies takes time, so it is kept off the chain's critical path)
+            if (otid == 0 && c + 2 < nc && !*abort_flag) {
+                ptx::fence_async_smem();
+                issue_load(c + 2);
+            }
             bar_sync(2, 256);
             if (*abort_flag) break;
             ptx::tc_fence_after();
@@ -304,15 +358,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
             ptx::tc_fence_before();
             bar_sync(2, 256);
             if (otid == 0) mbar_arrive(bar_ofree0 + 8 * buf);
-#pragma unroll 1
+#pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int t = 32 * half + rt;          // token of this thread's row pass
-                uint4 g2[2];
-                const size_t roff = (row0 + t) * W + (size_t)h * D + 16 * rseg;
-                if (t < Lc) {
-                    g2[0] = __ldg(reinterpret_cast<const uint4*>(gout + roff));
-                    g2[1] = __ldg(reinterpret_cast<const uint4*>(gout + roff) + 1);
-                }
                 if (th == half) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) ys[j * LDYS + vrow] = o[j];
@@ -329,29 +377,45 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
                 ss += __shfl_xor_sync(0xffffffffu, ss, 4);
                 const float rs = rsqrtf(ss * (1.0f / D) + a.eps);
                 if (t < Lc) {
-                    float g16[16], r[16];
-                    const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(g2);
+                    // o * rs * w * sigmoid(g), sigmoid(g) = (1 + tanh(g / 2)) / 2; the result
+                    // is rounded to bf16, far coarser than the tanh's 2^-11
+                    float r[16];
+                    const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(gcur[half]);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const float2 gf = __bfloat1622float2(gh[e]);
-                        g16[2 * e] = gf.x; g16[2 * e + 1] = gf.y;
+                        const float2 yw = __fmul2_rn(make_float2(y[2 * e], y[2 * e + 1]),
+                                                     __fmul2_rn(make_float2(wv[2 * e], wv[2 * e + 1]), make_float2(rs, rs)));
+                        const float2 th2 = make_float2(tanh_fast(0.5f * gf.x), tanh_fast(0.5f * gf.y));
+                        const float2 sg = __ffma2_rn(th2, make_float2(0.5f, 0.5f), make_float2(0.5f, 0.5f));
+                        const float2 rr = __fmul2_rn(yw, sg);
+                        r[2 * e] = rr.x;
+                        r[2 * e + 1] = rr.y;
                     }
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) r[e] = y[e] * rs * wv[e] * sigmoid_fast(g16[e]);
+                    const size_t roff = (row0 + t) * W + (size_t)h * D + 16 * rseg;
                     Vec8<TO>::store(out + roff, *reinterpret_cast<float(*)[8]>(r));
                     Vec8<TO>::store(out + roff + 8, *reinterpret_cast<float(*)[8]>(r + 8));
                 }
                 bar_sync(2, 256);  // the tile is read before the next half overwrites it
             }
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                gcur[hf][0] = gnext[hf][0];
+                gcur[hf][1] = gnext[hf][1];
+            }
         }
     }
 
+    __syncthreads();
     if (*abort_flag && tid == 0) {
         // record the timeout, then let this CTA's own copies and MMAs land
         atomicExch(a.status, ERR_TIMEOUT);
         for (int s = 0; s < 2; ++s)
             if (pend[s]) ptx::mbar_wait(bar_load0 + 8 * s, (uint32_t)pend[2 + s], WAIT_LIMIT_NS);
-        if (pend[4]) ptx::mbar_wait((uint32_t)pend[4], (uint32_t)pend[5], WAIT_LIMIT_NS);
+        if (pend[4]) {  // MMAs in flight: one more commit tracks all of them
+            ptx::mma_commit(bar_drain);
+            ptx::mbar_wait(bar_drain, 0, WAIT_LIMIT_NS);
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();

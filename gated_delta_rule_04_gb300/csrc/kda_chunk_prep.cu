@@ -64,7 +64,7 @@ constexpr int PT = 512;
 constexpr int C = CHUNK_T;                 // 64 tokens
 constexpr int RAW_ROWS = C + RING;         // raw q/k/v rows incl. the three before the chunk
 constexpr uint32_t ROW_B = D * 2;          // one bf16 row of a head
-constexpr int LDS = 65;                    // padded fp32 row stride of the 64 x 64 matrices
+constexpr int LDS = 68;                    // fp32 row stride of the 64 x 64 matrices (16-byte rows)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_D0 = 0, TM_D1 = 64, TM_D2 = 128, TM_W = 192, TM_U = 320;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
@@ -74,24 +74,23 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr uint32_t S_RQ = 0;                               // bf16 [67][128] raw q (row 0 = token t0 - 3)
 constexpr uint32_t S_RK = S_RQ + RAW_ROWS * ROW_B;
 constexpr uint32_t S_RV = S_RK + RAW_ROWS * ROW_B;
-constexpr uint32_t S_RZ = S_RV + RAW_ROWS * ROW_B;         // bf16 [64][128] raw z
-constexpr uint32_t S_OPS = 68608;                          // operand region (1 KiB aligned)
+constexpr uint32_t S_OPS = 52224;                          // operand region (1 KiB aligned)
 constexpr uint32_t S_LAP = S_OPS;                          //   bf16 2 x [128 rows][128 keys]
 constexpr uint32_t S_QD = S_OPS + 65536;                   //   bf16 [128][128]: rows 0-63 hi, 64-127 lo
 constexpr uint32_t S_RH = S_OPS + 98304;                   //   bf16 [64 s][128 keys] R, high part
 constexpr uint32_t S_RL = S_OPS + 114688;                  //   low part
-constexpr uint32_t S_AM = S_OPS;                           // after the first MMAs: fp32 [64][65] A
-constexpr uint32_t S_XM = S_OPS + 16640;                   //   fp32 [64][65] X = (I + A)^{-1}
-constexpr uint32_t S_TT = S_OPS + 33792;                   //   fp16 [128 r][64 s] T (rows 64-127 zero)
-constexpr uint32_t S_KPT = S_OPS + 50176;                  //   fp16 [128 key][64 s] (k e^G)^T
-constexpr uint32_t S_VT = S_OPS + 66560;                   //   fp16 [128 val][64 s] v^T
-constexpr uint32_t S_NRM = S_OPS + 131072;                 // fp32 [16 warps][16] partial sums of squares
+constexpr uint32_t S_AM = S_OPS;                           // after the first MMAs: fp32 [64][68] A
+constexpr uint32_t S_XM = S_OPS + 17408;                   //   fp32 [64][68] X = (I + A)^{-1}
+constexpr uint32_t S_TT = S_OPS + 34816;                   //   fp16 [128 r][64 s] T (rows 64-127 zero)
+constexpr uint32_t S_KPT = S_OPS + 131072;                 // fp16 [128 key][64 s] (k e^G)^T
+constexpr uint32_t S_VT = S_KPT + 16384;                   // fp16 [128 val][64 s] v^T
+constexpr uint32_t S_NRM = S_VT + 16384;                   // fp32 [16 warps][16] partial sums of squares
 constexpr uint32_t S_TOT = S_NRM + 1024;                   // fp32 [8 octets][128] gate sums
 constexpr uint32_t S_BT = S_TOT + 4096;                    // fp32 [64] beta
-constexpr uint32_t S_BAR = S_BT + 256;                     // 3 mbarriers, TMEM slot, abort flag
+constexpr uint32_t S_BAR = S_BT + 256;                     // 2 mbarriers, TMEM slot, abort flag
 constexpr uint32_t SMEM_BYTES = S_BAR + 64 + 1024;
-static_assert(S_RZ + C * ROW_B <= S_OPS, "raw rows overlap the operand region");
-static_assert(S_VT + 16384 <= S_OPS + 131072, "late tiles overflow the operand region");
+static_assert(S_RV + RAW_ROWS * ROW_B <= S_OPS, "raw rows overlap the operand region");
+static_assert(S_TT + 16384 <= S_OPS + 131072, "late tiles overflow the operand region");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 // Row groups of the 256 left rows: (is_P, column sub-tile b, first r, first row)
@@ -148,29 +147,36 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 
 // One diagonal of the blockwise inverse (block pairs (b + Dg, b)):
 //   M_ab = sum_{k=b}^{a-1} A_ak X_kb  (kept in A's unused upper block (b, a)),  X_ab = -X_aa M_ab
+// Thread = (block pair, row, 4 consecutive columns): one broadcast load of the
+// left factor and one 16-byte load of the right row per 4 FMAs.
 template <int Dg>
 __device__ __forceinline__ void solve_level(float* Am, float* Xm, int tid) {
-    constexpr int nblk = 4 - Dg;
-    for (int idx = tid; idx < nblk * 256; idx += PT) {
-        const int b = idx >> 8, e = idx & 255, ab = b + Dg;
-        const int r = e >> 4, cc = e & 15;
-        float acc = 0.f;
+    constexpr int nthr = (4 - Dg) * 64;
+    const int b = tid >> 6, r = (tid >> 2) & 15, c = 4 * (tid & 3), ab = b + Dg;
+    if (tid < nthr) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int kk = 0; kk < Dg; ++kk)
 #pragma unroll
-            for (int s = 0; s < 16; ++s)
-                acc = fmaf(Am[(16 * ab + r) * LDS + 16 * (b + kk) + s], Xm[(16 * (b + kk) + s) * LDS + 16 * b + cc], acc);
-        Am[(16 * b + r) * LDS + 16 * ab + cc] = acc;
+            for (int s = 0; s < 16; ++s) {
+                const float l = Am[(16 * ab + r) * LDS + 16 * (b + kk) + s];
+                const float4 x = *reinterpret_cast<const float4*>(Xm + (16 * (b + kk) + s) * LDS + 16 * b + c);
+                acc.x = fmaf(l, x.x, acc.x); acc.y = fmaf(l, x.y, acc.y);
+                acc.z = fmaf(l, x.z, acc.z); acc.w = fmaf(l, x.w, acc.w);
+            }
+        *reinterpret_cast<float4*>(Am + (16 * b + r) * LDS + 16 * ab + c) = acc;
     }
     __syncthreads();
-    for (int idx = tid; idx < nblk * 256; idx += PT) {
-        const int b = idx >> 8, e = idx & 255, ab = b + Dg;
-        const int r = e >> 4, cc = e & 15;
-        float acc = 0.f;
+    if (tid < nthr) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int s = 0; s < 16; ++s)
-            acc = fmaf(Xm[(16 * ab + r) * LDS + 16 * ab + s], Am[(16 * b + s) * LDS + 16 * ab + cc], acc);
-        Xm[(16 * ab + r) * LDS + 16 * b + cc] = -acc;
+        for (int s = 0; s < 16; ++s) {
+            const float l = Xm[(16 * ab + r) * LDS + 16 * ab + s];
+            const float4 m = *reinterpret_cast<const float4*>(Am + (16 * b + s) * LDS + 16 * ab + c);
+            acc.x = fmaf(l, m.x, acc.x); acc.y = fmaf(l, m.y, acc.y);
+            acc.z = fmaf(l, m.z, acc.z); acc.w = fmaf(l, m.w, acc.w);
+        }
+        *reinterpret_cast<float4*>(Xm + (16 * ab + r) * LDS + 16 * b + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     __syncthreads();
 }
@@ -181,8 +187,8 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
-// Asynchronous 16-byte copies of one item's raw rows into shared memory, by
-// all threads.  q/k/v rows 0-2 are the three tokens before the chunk: earlier
+// Asynchronous 16-byte copies of one item's raw q/k/v rows into shared
+// memory, by all threads.  Rows 0-2 are the three tokens before the chunk: earlier
 // rows of the same sequence, or the conv ring at a sequence start (left
 // unloaded, and read as zero, when there is no ring).
 __device__ __forceinline__ void issue_raw(const PrepArgs& a, int item, uint32_t base, int tid) {
@@ -205,11 +211,6 @@ __device__ __forceinline__ void issue_raw(const PrepArgs& a, int item, uint32_t 
                 src = static_cast<const __nv_bfloat16*>(a.ring_in) + (((size_t)cd.seq * 3 + pl) * RING + r) * W + hoff;
             cp_async16(base + S_RQ + (uint32_t)pl * RAW_ROWS * ROW_B + (uint32_t)r * ROW_B + 16 * piece, src + 8 * piece);
         }
-    }
-    const __nv_bfloat16* zp = static_cast<const __nv_bfloat16*>(a.z) + (size_t)cd.t0 * W + hoff;
-    for (int i = tid; i < len * 16; i += PT) {
-        const int r = i >> 4, piece = i & 15;
-        cp_async16(base + S_RZ + (uint32_t)r * ROW_B + 16 * piece, zp + (size_t)r * W + 8 * piece);
     }
     cp_async_commit();
 }
@@ -253,7 +254,24 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    if ((int)blockIdx.x < n_items) issue_raw(a, blockIdx.x, base, tid);
+    // gate inputs (this thread's tokens and channels) and the beta logit of an
+    // item, loaded into registers one item ahead of use
+    uint32_t zr[8];
+    float b_raw = 0.f;
+    auto load_zb = [&](int it) {
+        const ChunkDesc cn = a.chunks[it / H];
+        const int hn = it % H;
+        const uint32_t* zp = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.z) +
+                                                               (size_t)(cn.t0 + tok0) * W + hn * D + c0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) zr[j] = tok0 + j < cn.len ? __ldg(zp + (size_t)j * (W / 2)) : 0u;
+        b_raw = tid < cn.len ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.b)[(size_t)(cn.t0 + tid) * H + hn])
+                             : 0.f;
+    };
+    if ((int)blockIdx.x < n_items) {
+        issue_raw(a, blockIdx.x, base, tid);
+        load_zb(blockIdx.x);
+    }
     int mma_pending = 0;                            // thread 0: 1 = bar_mma1, 2 = bar_mma2 in flight
     uint32_t k_iter = 0;
 
@@ -275,8 +293,6 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
         }
         const float2 dtb = __ldg(reinterpret_cast<const float2*>(a.dt_bias + h * D + c0));
         const float eA = __expf(__ldg(a.A_log + h));
-        float b_raw = 0.f;
-        if (tid < len) b_raw = __bfloat162float(static_cast<const __nv_bfloat16*>(a.b)[(size_t)(cd.t0 + tid) * H + h]);
         const bool zero_halo = cd.pos == 0 && a.ring_in == nullptr;
 
         cp_async_wait_all();
@@ -320,8 +336,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
             const float2 eA2 = f2(eA), nl2 = f2(-LOG2E), lb2 = f2(a.lb);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const uint32_t u = *reinterpret_cast<const uint32_t*>(sb + S_RZ + (tok0 + j) * ROW_B + 2 * c0);
-                const float2 sarg = __fmul2_rn(__fmul2_rn(__fadd2_rn(bf2f(u), dtb), eA2), nl2);
+                const float2 sarg = __fmul2_rn(__fmul2_rn(__fadd2_rn(bf2f(zr[j]), dtb), eA2), nl2);
                 const float2 g = __fmul2_rn(lb2, make_float2(rcpf(1.f + ex2f(sarg.x)), rcpf(1.f + ex2f(sarg.y))));
                 if (tok0 + j < len) run = __fadd2_rn(run, g);
                 gc[j] = run;
@@ -450,9 +465,14 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
             }
         }
 #pragma unroll
-        for (int e = 0; e < 2; ++e)
+        for (int e = 0; e < 2; ++e) {
             *reinterpret_cast<uint4*>(rec + REC_KT + sw128_off(c0 + e, tok0, 128)) =
                 make_uint4(kt[e][0], kt[e][1], kt[e][2], kt[e][3]);
+            *reinterpret_cast<uint4*>(sb + S_KPT + sw128_off(c0 + e, tok0, 128)) =
+                make_uint4(kp[e][0], kp[e][1], kp[e][2], kp[e][3]);
+            *reinterpret_cast<uint4*>(sb + S_VT + sw128_off(c0 + e, tok0, 128)) =
+                make_uint4(vp[e][0], vp[e][1], vp[e][2], vp[e][3]);
+        }
         ptx::fence_async_smem();
         ptx::tc_fence_before();
         __syncthreads();
@@ -485,12 +505,15 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
             mma_pending = 1;
         }
         // the raw rows are consumed: fetch the next item's while this one finishes
-        if (item + (int)gridDim.x < n_items) issue_raw(a, item + gridDim.x, base, tid);
+        if (item + (int)gridDim.x < n_items) {
+            issue_raw(a, item + gridDim.x, base, tid);
+            load_zb(item + gridDim.x);
+        }
         if (!ptx::mbar_wait(bar_mma1, par, WAIT_LIMIT_NS)) *abort_flag = 1;
         ptx::tc_fence_after();
         if (tid == 0 && !*abort_flag) mma_pending = 0;
 
-        // ---- 4. read out A (to fp32 Am, times beta_r) and P (to the record); (k e^G)^T, v^T tiles
+        // ---- 4. read out A (to fp32 Am, times beta_r) and P (to the record)
         if (!*abort_flag) {
             if (warp < 8) {
                 const int row = 128 * (warp >> 2) + 32 * (warp & 3) + lane;
@@ -506,11 +529,17 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
                         if (isP) {
                             *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * b, C)) = pack8_f16(v);
                             *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * b + 8, C)) = pack8_f16(v + 8);
-                        } else {
+                        } else {  // beta_r A, strictly lower part (zeros above in the diagonal block)
                             const float be = bt[r];
 #pragma unroll
-                            for (int jj = 0; jj < 16; ++jj)
-                                if (16 * b + jj < r) Am[r * LDS + 16 * b + jj] = be * v[jj];
+                            for (int q = 0; q < 4; ++q) {
+                                float4 w4;
+                                w4.x = 16 * b + 4 * q + 0 < r ? be * v[4 * q + 0] : 0.f;
+                                w4.y = 16 * b + 4 * q + 1 < r ? be * v[4 * q + 1] : 0.f;
+                                w4.z = 16 * b + 4 * q + 2 < r ? be * v[4 * q + 2] : 0.f;
+                                w4.w = 16 * b + 4 * q + 3 < r ? be * v[4 * q + 3] : 0.f;
+                                *reinterpret_cast<float4*>(Am + r * LDS + 16 * b + 4 * q) = w4;
+                            }
                         }
                     }
                 }
@@ -535,13 +564,6 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
                     *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * tb, C)) = make_uint4(0, 0, 0, 0);
                     *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * tb + 8, C)) = make_uint4(0, 0, 0, 0);
                 }
-            }
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                *reinterpret_cast<uint4*>(sb + S_KPT + sw128_off(c0 + e, tok0, 128)) =
-                    make_uint4(kp[e][0], kp[e][1], kp[e][2], kp[e][3]);
-                *reinterpret_cast<uint4*>(sb + S_VT + sw128_off(c0 + e, tok0, 128)) =
-                    make_uint4(vp[e][0], vp[e][1], vp[e][2], vp[e][3]);
             }
         }
         ptx::tc_fence_before();
@@ -571,12 +593,12 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
         // ---- 6. T = X Diag(beta) (fp16, blocks above the diagonal zero; rows 64-127 zero)
         {
             const int r = tid >> 3, ch = tid & 7;   // 512 threads = 64 rows x 8 column groups
-            float v[8];
+            float v[8], xr[8], b8[8];
+            lds8(Xm + r * LDS + 8 * ch, xr);
+            lds8(bt + 8 * ch, b8);
+            const bool keep = (ch >> 1) <= (r >> 4);   // blocks above the diagonal are zero
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int s = 8 * ch + e;
-                v[e] = ((s >> 4) <= (r >> 4)) ? Xm[r * LDS + s] * bt[s] : 0.f;
-            }
+            for (int e = 0; e < 8; ++e) v[e] = keep ? xr[e] * b8[e] : 0.f;
             *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 8 * ch, 128)) = pack8_f16(v);
             *reinterpret_cast<uint4*>(sb + S_TT + 64 * 128 + 16 * tid) = make_uint4(0, 0, 0, 0);
         }
