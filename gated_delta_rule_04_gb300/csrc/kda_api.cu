@@ -245,7 +245,7 @@ kda_status prefill_impl(const kda_params* p, const void* q, const void* k, const
         // the chunk preparation runs the pre-stage itself
         if (mark(ev, 1, s) != cudaSuccess) return KDA_ERR_CUDA;
         PrepArgs pr{q, k, v, z, b, ring_in, p->conv_w, p->A_log, p->dt_bias, p->gate_lower_bound, p->l2_eps, qs,
-                    d_chunks, (int32_t)n_chunks, H, ws + L.rec, reinterpret_cast<int32_t*>(ws + L.status)};
+                    d_chunks, (int32_t)n_chunks, H, total_tokens, ws + L.rec, reinterpret_cast<int32_t*>(ws + L.status), {}, {}};
         e = launch_chunk_prep(pr, s);
         if (e != cudaSuccess || mark(ev, 2, s) != cudaSuccess) return KDA_ERR_CUDA;
         // the recurrence kernel applies the output norm itself

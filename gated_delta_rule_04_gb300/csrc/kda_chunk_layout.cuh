@@ -4,6 +4,8 @@
 // memory, so one bulk copy moves a whole record.
 #pragma once
 
+#include <cuda.h>
+
 #include "kda_common.cuh"
 
 namespace kda {
@@ -41,8 +43,12 @@ struct PrepArgs {
     float lb, l2_eps, q_scale;
     const ChunkDesc* chunks;
     int32_t n_chunks, H;
+    int64_t T;                      // total tokens
     void* records;                  // [n_chunks][H][REC_BYTES]
     int32_t* status;                // workspace error word
+    // set by launch_chunk_prep: TMA descriptors of q, k, v as [T][H*128] bf16
+    // with a 67-row box (a chunk and the three rows before it) and a 64-row box
+    CUtensorMap map67[3], map64[3];
 };
 cudaError_t launch_chunk_prep(const PrepArgs& a, cudaStream_t s);
 size_t chunk_prep_smem_bytes();

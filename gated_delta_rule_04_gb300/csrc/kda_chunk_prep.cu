@@ -34,8 +34,8 @@
 // rows are the A rows grouped by column sub-tile b (64 + 48 + 32 + 16) and the
 // off-diagonal P rows (48 + 32 + 16).  The diagonal blocks of P reach the
 // output directly and need more than bf16: their operands are split into
-// bf16 high and low parts and one accumulator takes hi*hi + lo*hi + hi*lo
-// (24 K-steps), good to about 16 bits.  W = T (k e^G) and U0^T = v^T T^T are
+// bf16 high and low parts: one N = 128 MMA multiplies [q hi; q lo] by
+// [R hi | R lo] and the readout adds hi*hi + hi*lo + lo*hi, good to about 16 bits.  W = T (k e^G) and U0^T = v^T T^T are
 // fp16 MMAs; the unit lower-triangular solve is fp32 on the CUDA cores
 // (16 x 16 diagonal inverses, then the off-diagonal blocks diagonal by
 // diagonal).
@@ -66,7 +66,7 @@ constexpr int RAW_ROWS = C + RING;         // raw q/k/v rows incl. the three bef
 constexpr uint32_t ROW_B = D * 2;          // one bf16 row of a head
 constexpr int LDS = 68;                    // fp32 row stride of the 64 x 64 matrices (16-byte rows)
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_D0 = 0, TM_D1 = 64, TM_D2 = 128, TM_W = 192, TM_U = 320;
+constexpr uint32_t TM_D0 = 0, TM_D1 = 64, TM_D2 = 128, TM_W = 256, TM_U = 384;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -77,8 +77,7 @@ constexpr uint32_t S_RV = S_RK + RAW_ROWS * ROW_B;
 constexpr uint32_t S_OPS = 52224;                          // operand region (1 KiB aligned)
 constexpr uint32_t S_LAP = S_OPS;                          //   bf16 2 x [128 rows][128 keys]
 constexpr uint32_t S_QD = S_OPS + 65536;                   //   bf16 [128][128]: rows 0-63 hi, 64-127 lo
-constexpr uint32_t S_RH = S_OPS + 98304;                   //   bf16 [64 s][128 keys] R, high part
-constexpr uint32_t S_RL = S_OPS + 114688;                  //   low part
+constexpr uint32_t S_RHL = S_OPS + 98304;                  //   bf16 [128][128 keys] R: rows 0-63 hi, 64-127 lo
 constexpr uint32_t S_AM = S_OPS;                           // after the first MMAs: fp32 [64][68] A
 constexpr uint32_t S_XM = S_OPS + 17408;                   //   fp32 [64][68] X = (I + A)^{-1}
 constexpr uint32_t S_TT = S_OPS + 34816;                   //   fp16 [128 r][64 s] T (rows 64-127 zero)
@@ -87,7 +86,7 @@ constexpr uint32_t S_VT = S_KPT + 16384;                   // fp16 [128 val][64 
 constexpr uint32_t S_NRM = S_VT + 16384;                   // fp32 [16 warps][16] partial sums of squares
 constexpr uint32_t S_TOT = S_NRM + 1024;                   // fp32 [8 octets][128] gate sums
 constexpr uint32_t S_BT = S_TOT + 4096;                    // fp32 [64] beta
-constexpr uint32_t S_BAR = S_BT + 256;                     // 2 mbarriers, TMEM slot, abort flag
+constexpr uint32_t S_BAR = S_BT + 256;                     // 3 mbarriers, TMEM slot, abort flag
 constexpr uint32_t SMEM_BYTES = S_BAR + 64 + 1024;
 static_assert(S_RV + RAW_ROWS * ROW_B <= S_OPS, "raw rows overlap the operand region");
 static_assert(S_TT + 16384 <= S_OPS + 131072, "late tiles overflow the operand region");
@@ -129,6 +128,10 @@ __device__ __forceinline__ uint32_t pack_f16(float a, float b) {
 }
 __device__ __forceinline__ uint4 pack8_f16(const float* v) {
     return make_uint4(pack_f16(v[0], v[1]), pack_f16(v[2], v[3]), pack_f16(v[4], v[5]), pack_f16(v[6], v[7]));
+}
+// named barrier over `count` threads (id 0 is __syncthreads)
+__device__ __forceinline__ void bar_sync_n(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 __device__ __forceinline__ void sts32(unsigned char* p, uint32_t v) { *reinterpret_cast<uint32_t*>(p) = v; }
 
@@ -187,38 +190,46 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
-// Asynchronous 16-byte copies of one item's raw q/k/v rows into shared
-// memory, by all threads.  Rows 0-2 are the three tokens before the chunk: earlier
-// rows of the same sequence, or the conv ring at a sequence start (left
-// unloaded, and read as zero, when there is no ring).
-__device__ __forceinline__ void issue_raw(const PrepArgs& a, int item, uint32_t base, int tid) {
+// Raw q/k/v rows of one item into shared memory, issued by one warp: one TMA
+// box per plane (the chunk and the three rows before it).  At a sequence
+// start the three rows before the chunk belong to the conv ring (16-byte
+// copies by the warp, awaited with cp.async.wait) or are zero (left unloaded
+// and read as zero).  Rows past the end of the tensor read as zero;
+// rows past the chunk are never used.
+__device__ __forceinline__ void issue_raw(const PrepArgs& a, int item, uint32_t base, uint32_t bar, int lane) {
     const int H = a.H, W = H * D;
     const ChunkDesc cd = a.chunks[item / H];
-    const int h = item % H, len = cd.len;
-    const int halo = (cd.pos > 0 || a.ring_in != nullptr) ? RING : 0;
-    const int r0 = RING - halo;                 // first loaded raw row of a q/k/v plane
-    const int n16 = (halo + len) * 16;          // 16-byte pieces per q/k/v plane
-    const size_t hoff = (size_t)h * D;
+    const int h = item % H;
+    if (lane == 0) {
+        if (cd.pos > 0) {
+            ptx::mbar_expect_tx(bar, 3u * RAW_ROWS * ROW_B);
 #pragma unroll
-    for (int pl = 0; pl < 3; ++pl) {
-        const __nv_bfloat16* plane = static_cast<const __nv_bfloat16*>(pl == 0 ? a.q : (pl == 1 ? a.k : a.v));
-        for (int i = tid; i < n16; i += PT) {
-            const int r = r0 + (i >> 4), piece = i & 15;
-            const __nv_bfloat16* src;
-            if (cd.pos + r - RING >= 0)
-                src = plane + (size_t)(cd.t0 + r - RING) * W + hoff;
-            else  // sequence start: ring slot r (slot 0 oldest)
-                src = static_cast<const __nv_bfloat16*>(a.ring_in) + (((size_t)cd.seq * 3 + pl) * RING + r) * W + hoff;
-            cp_async16(base + S_RQ + (uint32_t)pl * RAW_ROWS * ROW_B + (uint32_t)r * ROW_B + 16 * piece, src + 8 * piece);
+            for (int pl = 0; pl < 3; ++pl)
+                ptx::tma_load_2d(base + S_RQ + (uint32_t)pl * RAW_ROWS * ROW_B, &a.map67[pl], h * D, cd.t0 - RING, bar);
+        } else {
+            ptx::mbar_expect_tx(bar, 3u * C * ROW_B);
+#pragma unroll
+            for (int pl = 0; pl < 3; ++pl)
+                ptx::tma_load_2d(base + S_RQ + (uint32_t)pl * RAW_ROWS * ROW_B + RING * ROW_B, &a.map64[pl], h * D,
+                                 cd.t0, bar);
         }
     }
-    cp_async_commit();
+    if (cd.pos == 0 && a.ring_in != nullptr) {
+        for (int i = lane; i < 3 * RING * 16; i += 32) {
+            const int pl = i / (RING * 16), r = (i / 16) % RING, piece = i & 15;  // ring slot r = raw row r
+            const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.ring_in) +
+                                       (((size_t)cd.seq * 3 + pl) * RING + r) * W + (size_t)h * D;
+            cp_async16(base + S_RQ + (uint32_t)pl * RAW_ROWS * ROW_B + (uint32_t)r * ROW_B + 16 * piece,
+                       src + 8 * piece);
+        }
+        cp_async_commit();
+    }
 }
 
 __device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
 __device__ __forceinline__ float2 h2f(uint32_t u) { return __half22float2(*reinterpret_cast<const __half2*>(&u)); }
 
-__global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
+__global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant__ PrepArgs a) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -228,7 +239,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
     float* nrm = reinterpret_cast<float*>(sb + S_NRM);
     float* tot = reinterpret_cast<float*>(sb + S_TOT);
     float* bt = reinterpret_cast<float*>(sb + S_BT);
-    const uint32_t bar_mma1 = base + S_BAR + 8, bar_mma2 = base + S_BAR + 16;
+    const uint32_t bar_raw = base + S_BAR, bar_mma1 = base + S_BAR + 8, bar_mma2 = base + S_BAR + 16;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sb + S_BAR + 24);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sb + S_BAR + 28);
 
@@ -245,6 +256,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
         ptx::tmem_relinquish();
     }
     if (tid == 0) {
+        ptx::mbar_init(bar_raw, 1);
         ptx::mbar_init(bar_mma1, 1);
         ptx::mbar_init(bar_mma2, 1);
         *abort_flag = 0;
@@ -269,10 +281,15 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
                              : 0.f;
     };
     if ((int)blockIdx.x < n_items) {
-        issue_raw(a, blockIdx.x, base, tid);
+        if (warp == PT / 32 - 1) issue_raw(a, blockIdx.x, base, bar_raw, lane);
         load_zb(blockIdx.x);
     }
-    int mma_pending = 0;                            // thread 0: 1 = bar_mma1, 2 = bar_mma2 in flight
+    // in-flight bookkeeping for the drain after a timeout: a raw load issued by
+    // the last warp and not yet consumed (flag in that warp's lane 0), and the
+    // MMAs of thread 0 (1 = bar_mma1, 2 = bar_mma2 in flight)
+    int pend_raw = (int)blockIdx.x < n_items && tid == PT - 32;
+    uint32_t raw_par = 0;                           // phase parity of that load
+    int mma_pending = 0;
     uint32_t k_iter = 0;
 
 #pragma unroll 1
@@ -295,8 +312,11 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
         const float eA = __expf(__ldg(a.A_log + h));
         const bool zero_halo = cd.pos == 0 && a.ring_in == nullptr;
 
-        cp_async_wait_all();
+        if (!ptx::mbar_wait(bar_raw, par, WAIT_LIMIT_NS)) *abort_flag = 1;
+        else pend_raw = 0;
+        cp_async_wait_all();   // ring rows at a sequence start
         __syncthreads();
+        if (*abort_flag) break;
 
         // ---- 1. conv + SiLU of q, k, v (kept as fp16 pairs); gate; sums of squares
         uint32_t aq[8], ak[8], av[8];
@@ -423,8 +443,8 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
             const float2 ky = __fmul2_rn(k, y);
             const uint32_t rh = pack_bf16(ky.x, ky.y);
             const float2 rlo = __fadd2_rn(ky, make_float2(-bf2f(rh).x, -bf2f(rh).y));
-            sts32(sb + S_RH + sw128_off(r, c0, C), rh);
-            sts32(sb + S_RL + sw128_off(r, c0, C), pack_bf16(rlo.x, rlo.y));
+            sts32(sb + S_RHL + sw128_off(r, c0, 128), rh);
+            sts32(sb + S_RHL + sw128_off(64 + r, c0, 128), pack_bf16(rlo.x, rlo.y));
             const float2 ki = __fmul2_rn(k, iy), qi = __fmul2_rn(q, iy);
             {   // A row of the diagonal sub-tile
                 const int R = kGroup[a_sub][3] + (r - kGroup[a_sub][2]);
@@ -479,36 +499,29 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
 
         // ---- 3. A, off-diagonal P, diagonal P on the tensor cores
         constexpr uint32_t IDESC_BF16_N64 = ptx::idesc_bf16_f32(128, 64);
+        constexpr uint32_t IDESC_BF16_N128 = ptx::idesc_bf16_f32(128, 128);
         if (tid == 0) {
             ptx::tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t koff = (kk & 3) * 32, pn = kk >> 2;
-                const uint64_t bR = ptx::sdesc_sw128(base + S_RH + pn * 8192 + koff);
+                const uint64_t bR = ptx::sdesc_sw128(base + S_RHL + pn * 16384 + koff);   // R hi rows
                 ptx::mma_f16(tmem + TM_D0, ptx::sdesc_sw128(base + S_LAP + pn * 16384 + koff), bR, IDESC_BF16_N64, kk > 0);
                 ptx::mma_f16(tmem + TM_D1, ptx::sdesc_sw128(base + S_LAP + 32768 + pn * 16384 + koff), bR, IDESC_BF16_N64,
                              kk > 0);
             }
-            // diagonal P: hi*hi, then lo*hi (rows 64-127 of the QD tile as the A rows), then hi*lo
+            // diagonal P: [q hi; q lo] x [R hi; R lo] (N = 128); the readout adds hi*hi + hi*lo + lo*hi
 #pragma unroll
-            for (int part = 0; part < 3; ++part) {
-                const uint32_t abase = base + S_QD + (part == 1 ? 8192u : 0u);
-                const uint32_t bbase = base + (part == 2 ? S_RL : S_RH);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t koff = (kk & 3) * 32, pn = kk >> 2;
-                    ptx::mma_f16(tmem + TM_D2, ptx::sdesc_sw128(abase + pn * 16384 + koff),
-                                 ptx::sdesc_sw128(bbase + pn * 8192 + koff), IDESC_BF16_N64, (part > 0 || kk > 0));
-                }
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t koff = (kk & 3) * 32, pn = kk >> 2;
+                ptx::mma_f16(tmem + TM_D2, ptx::sdesc_sw128(base + S_QD + pn * 16384 + koff),
+                             ptx::sdesc_sw128(base + S_RHL + pn * 16384 + koff), IDESC_BF16_N128, kk > 0);
             }
             ptx::mma_commit(bar_mma1);
             mma_pending = 1;
         }
-        // the raw rows are consumed: fetch the next item's while this one finishes
-        if (item + (int)gridDim.x < n_items) {
-            issue_raw(a, item + gridDim.x, base, tid);
-            load_zb(item + gridDim.x);
-        }
+        // the next item's gate inputs; its raw rows follow after the readout
+        if (item + (int)gridDim.x < n_items) load_zb(item + gridDim.x);
         if (!ptx::mbar_wait(bar_mma1, par, WAIT_LIMIT_NS)) *abort_flag = 1;
         ptx::tc_fence_after();
         if (tid == 0 && !*abort_flag) mma_pending = 0;
@@ -543,32 +556,68 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
                         }
                     }
                 }
-            } else if (warp < 10) {
-                const int r = 32 * (warp & 3) + lane;                 // 0..63
+            } else if (warp < 12) {
+                // diagonal P blocks: D2 rows are [q hi; q lo], columns [R hi | R lo].
+                // Warps 10-11 hand the lo*hi terms (lanes 64-127) to warps 8-9 through
+                // shared memory; warps 8-9 add hi*hi + hi*lo + lo*hi.
+                float* pdl = tot;   // fp32 [64 r][16]; the gate totals are no longer needed
+                const int qd = warp & 3;
+                const int r = 32 * (qd & 1) + lane;                    // 0..63
                 const int ta = r >> 4;
-                const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + TM_D2;
+                const uint32_t taddr = tmem + ((uint32_t)(32 * qd) << 16) + TM_D2;
+                if (qd >= 2) {
 #pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) {
-                    const int blk = 2 * (warp & 1) + q2;              // sub-tiles of this warp's rows
-                    float v[16];
-                    tmem_ld16(taddr + 16 * blk, v);
-                    if (blk == ta) {
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        const int blk = 2 * (qd & 1) + q2;             // sub-tiles of this warp's rows
+                        float v[16];
+                        tmem_ld16(taddr + 16 * blk, v);                // q lo x R hi
+                        if (blk == ta) {
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj)
-                            if (16 * ta + jj > r) v[jj] = 0.f;
-                        *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * ta, C)) = pack8_f16(v);
-                        *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * ta + 8, C)) = pack8_f16(v + 8);
+                            for (int q = 0; q < 4; ++q)
+                                *reinterpret_cast<float4*>(pdl + r * 16 + 4 * q) =
+                                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                        }
                     }
                 }
-                for (int tb = ta + 1; tb < 4; ++tb) {
-                    *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * tb, C)) = make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * tb + 8, C)) = make_uint4(0, 0, 0, 0);
+                bar_sync_n(1, 128);
+                if (qd < 2) {
+#pragma unroll
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        const int blk = 2 * qd + q2;
+                        float v[16], w[16];
+                        tmem_ld16(taddr + 16 * blk, v);                // q hi x R hi
+                        tmem_ld16(taddr + 64 + 16 * blk, w);           // q hi x R lo
+                        if (blk == ta) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const float4 l4 = *reinterpret_cast<const float4*>(pdl + r * 16 + 4 * q);
+                                v[4 * q] += w[4 * q] + l4.x;
+                                v[4 * q + 1] += w[4 * q + 1] + l4.y;
+                                v[4 * q + 2] += w[4 * q + 2] + l4.z;
+                                v[4 * q + 3] += w[4 * q + 3] + l4.w;
+                            }
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj)
+                                if (16 * ta + jj > r) v[jj] = 0.f;
+                            *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * ta, C)) = pack8_f16(v);
+                            *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * ta + 8, C)) = pack8_f16(v + 8);
+                        }
+                    }
+                    for (int tb = ta + 1; tb < 4; ++tb) {
+                        *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * tb, C)) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * tb + 8, C)) = make_uint4(0, 0, 0, 0);
+                    }
                 }
             }
         }
         ptx::tc_fence_before();
         __syncthreads();
         if (*abort_flag) break;
+        // the raw rows are consumed: the last warp (idle in the solve) fetches the next item's
+        if (warp == PT / 32 - 1 && item + (int)gridDim.x < n_items) {
+            issue_raw(a, item + gridDim.x, base, bar_raw, lane);
+            if (lane == 0) { pend_raw = 1; raw_par = (k_iter + 1) & 1u; }
+        }
 
         // ---- 5. X = (I + A)^{-1}: diagonal 16 x 16 inverses by forward substitution
         if (tid < 64) {
@@ -657,6 +706,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
     }
 
     cp_async_wait_all();  // this thread's copies of a prefetch that was not consumed
+    if (*abort_flag && pend_raw) ptx::mbar_wait(bar_raw, raw_par, WAIT_LIMIT_NS);
     if (*abort_flag && tid == 0) {
         // record the timeout, then let this CTA's own MMAs land
         atomicExch(a.status, ERR_TIMEOUT);
@@ -676,10 +726,50 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(PrepArgs a) {
 
 size_t chunk_prep_smem_bytes() { return SMEM_BYTES; }
 
-cudaError_t launch_chunk_prep(const PrepArgs& a, cudaStream_t s) {
-    const int64_t items = (int64_t)a.n_chunks * a.H;
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// [T][W] bf16 tensor, boxes of `rows` rows x 128 channels, zero fill out of bounds
+bool encode_rows(CUtensorMap* m, const void* base, int64_t T, int64_t W, uint32_t rows) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)W, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)W * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)D, rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_prep(const PrepArgs& args, cudaStream_t s) {
+    const int64_t items = (int64_t)args.n_chunks * args.H;
     if (items == 0) return cudaSuccess;
     if (items > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
+    PrepArgs a = args;
+    const void* planes[3] = {a.q, a.k, a.v};
+    for (int pl = 0; pl < 3; ++pl)
+        if (!encode_rows(&a.map67[pl], planes[pl], a.T, (int64_t)a.H * D, RAW_ROWS) ||
+            !encode_rows(&a.map64[pl], planes[pl], a.T, (int64_t)a.H * D, C))
+            return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
