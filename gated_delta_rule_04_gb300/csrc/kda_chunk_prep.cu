@@ -54,6 +54,8 @@
 // Output: one record per (chunk, head) in the exact shared-memory image the
 // recurrence kernel consumes (fp16, K-major, 128-byte swizzle), written
 // straight from registers.
+#include <type_traits>
+
 #include "kda_chunk_layout.cuh"
 #include "tc_ptx.cuh"
 
@@ -80,8 +82,10 @@ constexpr uint32_t S_QD = S_OPS + 65536;                   //   bf16 [128][128]:
 constexpr uint32_t S_RHL = S_OPS + 98304;                  //   bf16 [128][128 keys] R: rows 0-63 hi, 64-127 lo
 constexpr uint32_t S_AM = S_OPS;                           // after the first MMAs: fp32 [64][68] A
 constexpr uint32_t S_XM = S_OPS + 17408;                   //   fp32 [64][68] X = (I + A)^{-1}
-constexpr uint32_t S_TT = S_OPS + 34816;                   //   fp16 [128 r][64 s] T (rows 64-127 zero)
-constexpr uint32_t S_KPT = S_OPS + 131072;                 // fp16 [128 key][64 s] (k e^G)^T
+constexpr uint32_t S_TT = S_OPS + 131072;                  // fp16 [64 r][64 s] T; the W product reads it as
+                                                           //   128 A rows, rows 64-127 being the first 8 KiB of
+                                                           //   the next tile (their output lanes are unused)
+constexpr uint32_t S_KPT = S_TT + 8192;                    // fp16 [128 key][64 s] (k e^G)^T
 constexpr uint32_t S_VT = S_KPT + 16384;                   // fp16 [128 val][64 s] v^T
 constexpr uint32_t S_NRM = S_VT + 16384;                   // fp32 [16 warps][16] partial sums of squares
 constexpr uint32_t S_TOT = S_NRM + 1024;                   // fp32 [8 octets][128] gate sums
@@ -89,8 +93,9 @@ constexpr uint32_t S_BT = S_TOT + 4096;                    // fp32 [64] beta
 constexpr uint32_t S_BAR = S_BT + 256;                     // 3 mbarriers, TMEM slot, abort flag
 constexpr uint32_t SMEM_BYTES = S_BAR + 64 + 1024;
 static_assert(S_RV + RAW_ROWS * ROW_B <= S_OPS, "raw rows overlap the operand region");
-static_assert(S_TT + 16384 <= S_OPS + 131072, "late tiles overflow the operand region");
+static_assert(S_XM + 64 * LDS * 4 <= S_OPS + 131072, "solve tiles overflow the operand region");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
+static_assert(S_TT + 16384 <= S_VT, "the W product's A rows stay inside the T and (k e^G)^T tiles");
 
 // Row groups of the 256 left rows: (is_P, column sub-tile b, first r, first row)
 __constant__ int16_t kGroup[7][4] = {
@@ -148,38 +153,46 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// One diagonal of the blockwise inverse (block pairs (b + Dg, b)):
-//   M_ab = sum_{k=b}^{a-1} A_ak X_kb  (kept in A's unused upper block (b, a)),  X_ab = -X_aa M_ab
+// Blockwise inverse X = (I + A)^{-1} over 16 x 16 blocks, once the diagonal
+// blocks X_aa are known:  X_ab = -X_aa sum_{k=b}^{a-1} A_ak X_kb.  First
+// At_ak = X_aa A_ak for every a > k (one pass, kept in A's unused upper block
+// (k, a)); then one pass per block diagonal, X_ab = -sum_k At_ak X_kb.
 // Thread = (block pair, row, 4 consecutive columns): one broadcast load of the
 // left factor and one 16-byte load of the right row per 4 FMAs.
+__device__ __forceinline__ void solve_premultiply(float* Am, const float* Xm, int tid) {
+    if (tid < 6 * 64) {
+        const int p = tid >> 6, r = (tid >> 2) & 15, c = 4 * (tid & 3);
+        const int a = p < 3 ? p + 1 : (p < 5 ? p - 1 : 3);   // (a, k): (1,0) (2,0) (3,0) (2,1) (3,1) (3,2)
+        const int k = p < 3 ? 0 : (p < 5 ? 1 : 2);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+            const float l = Xm[(16 * a + r) * LDS + 16 * a + s];
+            const float4 m = *reinterpret_cast<const float4*>(Am + (16 * a + s) * LDS + 16 * k + c);
+            acc.x = fmaf(l, m.x, acc.x); acc.y = fmaf(l, m.y, acc.y);
+            acc.z = fmaf(l, m.z, acc.z); acc.w = fmaf(l, m.w, acc.w);
+        }
+        *reinterpret_cast<float4*>(Am + (16 * k + r) * LDS + 16 * a + c) = acc;
+    }
+    __syncthreads();
+}
+
 template <int Dg>
-__device__ __forceinline__ void solve_level(float* Am, float* Xm, int tid) {
+__device__ __forceinline__ void solve_level(const float* Am, float* Xm, int tid) {
     constexpr int nthr = (4 - Dg) * 64;
-    const int b = tid >> 6, r = (tid >> 2) & 15, c = 4 * (tid & 3), ab = b + Dg;
+    const int b = tid >> 6, r = (tid >> 2) & 15, c = 4 * (tid & 3), a = b + Dg;
     if (tid < nthr) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int kk = 0; kk < Dg; ++kk)
 #pragma unroll
             for (int s = 0; s < 16; ++s) {
-                const float l = Am[(16 * ab + r) * LDS + 16 * (b + kk) + s];
+                const float l = Am[(16 * (b + kk) + r) * LDS + 16 * a + s];   // At_{a, b+kk}[r][s]
                 const float4 x = *reinterpret_cast<const float4*>(Xm + (16 * (b + kk) + s) * LDS + 16 * b + c);
                 acc.x = fmaf(l, x.x, acc.x); acc.y = fmaf(l, x.y, acc.y);
                 acc.z = fmaf(l, x.z, acc.z); acc.w = fmaf(l, x.w, acc.w);
             }
-        *reinterpret_cast<float4*>(Am + (16 * b + r) * LDS + 16 * ab + c) = acc;
-    }
-    __syncthreads();
-    if (tid < nthr) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-            const float l = Xm[(16 * ab + r) * LDS + 16 * ab + s];
-            const float4 m = *reinterpret_cast<const float4*>(Am + (16 * b + s) * LDS + 16 * ab + c);
-            acc.x = fmaf(l, m.x, acc.x); acc.y = fmaf(l, m.y, acc.y);
-            acc.z = fmaf(l, m.z, acc.z); acc.w = fmaf(l, m.w, acc.w);
-        }
-        *reinterpret_cast<float4*>(Xm + (16 * ab + r) * LDS + 16 * b + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        *reinterpret_cast<float4*>(Xm + (16 * a + r) * LDS + 16 * b + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     __syncthreads();
 }
@@ -290,7 +303,32 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
     int pend_raw = (int)blockIdx.x < n_items && tid == PT - 32;
     uint32_t raw_par = 0;                           // phase parity of that load
     int mma_pending = 0;
+    uint32_t mma_par = 0;                           // phase parity of those MMAs
     uint32_t k_iter = 0;
+
+    // W (lanes = tokens 0-63) and U0^T (lanes = values) of an item, from TMEM to its
+    // record, spread over all 16 warps: warp w reads TMEM lane quarter w % 4 and
+    // column group g = w / 4 (W: 32 keys 32g.., quarters 0-1 only; U0^T: 16 tokens 16g..)
+    unsigned char* rec_prev = nullptr;
+    auto wu_out = [&](unsigned char* rp) {
+        const int qd = warp & 3, g = warp >> 2;
+        const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
+        if (qd < 2) {
+            const int r = 32 * qd + lane;
+            float v[32];
+            ptx::tmem_ld32(tl + TM_W + 32 * g, v);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(rp + REC_W + sw128_off(r, 32 * g + 8 * q, C)) = pack8_f16(v + 8 * q);
+        }
+        {
+            const int vrow = 32 * qd + lane;
+            float v[16];
+            tmem_ld16(tl + TM_U + 16 * g, v);
+            *reinterpret_cast<uint4*>(rp + REC_UT + sw128_off(vrow, 16 * g, 128)) = pack8_f16(v);
+            *reinterpret_cast<uint4*>(rp + REC_UT + sw128_off(vrow, 16 * g + 8, 128)) = pack8_f16(v + 8);
+        }
+    };
 
 #pragma unroll 1
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++k_iter) {
@@ -305,8 +343,9 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         for (int pl = 0; pl < 3; ++pl) {
             const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.conv_w + ((size_t)pl * W + h * D + c0) * CONV_K));
             const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.conv_w + ((size_t)pl * W + h * D + c0 + 1) * CONV_K));
-            wt[pl][0] = make_float2(w0.x, w1.x); wt[pl][1] = make_float2(w0.y, w1.y);
-            wt[pl][2] = make_float2(w0.z, w1.z); wt[pl][3] = make_float2(w0.w, w1.w);
+            // taps times 1/2: the conv yields x/2, the argument of tanh in the SiLU
+            wt[pl][0] = make_float2(0.5f * w0.x, 0.5f * w1.x); wt[pl][1] = make_float2(0.5f * w0.y, 0.5f * w1.y);
+            wt[pl][2] = make_float2(0.5f * w0.z, 0.5f * w1.z); wt[pl][3] = make_float2(0.5f * w0.w, 0.5f * w1.w);
         }
         const float2 dtb = __ldg(reinterpret_cast<const float2*>(a.dt_bias + h * D + c0));
         const float eA = __expf(__ldg(a.A_log + h));
@@ -318,50 +357,58 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         __syncthreads();
         if (*abort_flag) break;
 
-        // ---- 1. conv + SiLU of q, k, v (kept as fp16 pairs); gate; sums of squares
+        // ---- 1. conv + SiLU of q, k, v (kept as fp16 pairs); gate; sums of squares.
+        // Octets inside the chunk (all but a ragged tail) skip the token masks.
         uint32_t aq[8], ak[8], av[8];
         float sq[16];
-#pragma unroll
-        for (int pl = 0; pl < 3; ++pl) {
-            float2 xr[11];
-#pragma unroll
-            for (int j = 0; j < 11; ++j) {
-                const int row = tok0 + j;
-                const uint32_t u = *reinterpret_cast<const uint32_t*>(sb + S_RQ + pl * RAW_ROWS * ROW_B + row * ROW_B + 2 * c0);
-                xr[j] = (zero_halo && row < RING) ? make_float2(0.f, 0.f) : bf2f(u);
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float2 acc = __fmul2_rn(wt[pl][0], xr[j]);
-                acc = __ffma2_rn(wt[pl][1], xr[j + 1], acc);
-                acc = __ffma2_rn(wt[pl][2], xr[j + 2], acc);
-                acc = __ffma2_rn(wt[pl][3], xr[j + 3], acc);
-                // x sigmoid(x) with sigmoid(x) = (1 + tanh(x / 2)) / 2 in half precision: the
-                // result is rounded to fp16 next, and the error (about 2^-11 of x) is at that level
-                const float2 hx = __fmul2_rn(acc, f2(0.5f));
-                const __half2 hin = __float22half2_rn(hx);
-                uint32_t t;
-                asm("tanh.approx.f16x2 %0, %1;" : "=r"(t) : "r"(*reinterpret_cast<const uint32_t*>(&hin)));
-                const float2 y = __fmul2_rn(acc, __ffma2_rn(h2f(t), f2(0.5f), f2(0.5f)));
-                const bool valid = tok0 + j < len;
-                const uint32_t hv = valid ? pack_f16(y.x, y.y) : 0u;
-                if (pl == 0) { aq[j] = hv; sq[j] = valid ? fmaf(y.x, y.x, y.y * y.y) : 0.f; }
-                if (pl == 1) { ak[j] = hv; sq[8 + j] = valid ? fmaf(y.x, y.x, y.y * y.y) : 0.f; }
-                if (pl == 2) av[j] = hv;
-            }
-        }
         float2 gc[8];
         float2 run = make_float2(0.f, 0.f);
-        {
-            const float2 eA2 = f2(eA), nl2 = f2(-LOG2E), lb2 = f2(a.lb);
+        const bool halo0 = zero_halo && tok0 == 0;        // rows 0-2 read as zero
+        const float2 gsc = f2(-eA * LOG2E);                 // gate argument: (z + dt_bias) e^A, as -log2 e units
+        const float2 gof = __fmul2_rn(dtb, gsc);
+        const float2 lb2 = f2(a.lb);
+        auto stage = [&](auto full_c) {
+            constexpr bool FULL = decltype(full_c)::value;
+#pragma unroll
+            for (int pl = 0; pl < 3; ++pl) {
+                float2 xr[11];
+#pragma unroll
+                for (int j = 0; j < 11; ++j) {
+                    const uint32_t u =
+                        *reinterpret_cast<const uint32_t*>(sb + S_RQ + pl * RAW_ROWS * ROW_B + (tok0 + j) * ROW_B + 2 * c0);
+                    xr[j] = bf2f(u);
+                    if (j < RING && halo0) xr[j] = make_float2(0.f, 0.f);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    // h = x / 2;  x sigmoid(x) = h + h tanh(h), tanh in half precision: the
+                    // result is rounded to fp16 next, and the error (about 2^-11 of x) is at that level
+                    float2 hx = __fmul2_rn(wt[pl][0], xr[j]);
+                    hx = __ffma2_rn(wt[pl][1], xr[j + 1], hx);
+                    hx = __ffma2_rn(wt[pl][2], xr[j + 2], hx);
+                    hx = __ffma2_rn(wt[pl][3], xr[j + 3], hx);
+                    const __half2 hin = __float22half2_rn(hx);
+                    uint32_t t;
+                    asm("tanh.approx.f16x2 %0, %1;" : "=r"(t) : "r"(*reinterpret_cast<const uint32_t*>(&hin)));
+                    const float2 y = __ffma2_rn(hx, h2f(t), hx);
+                    const bool valid = FULL || tok0 + j < len;
+                    const uint32_t hv = valid ? pack_f16(y.x, y.y) : 0u;
+                    const float yy = valid ? fmaf(y.x, y.x, y.y * y.y) : 0.f;
+                    if (pl == 0) { aq[j] = hv; sq[j] = yy; }
+                    if (pl == 1) { ak[j] = hv; sq[8 + j] = yy; }
+                    if (pl == 2) av[j] = hv;
+                }
+            }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const float2 sarg = __fmul2_rn(__fmul2_rn(__fadd2_rn(bf2f(zr[j]), dtb), eA2), nl2);
+                const float2 sarg = __ffma2_rn(bf2f(zr[j]), gsc, gof);
                 const float2 g = __fmul2_rn(lb2, make_float2(rcpf(1.f + ex2f(sarg.x)), rcpf(1.f + ex2f(sarg.y))));
-                if (tok0 + j < len) run = __fadd2_rn(run, g);
+                if (FULL || tok0 + j < len) run = __fadd2_rn(run, g);
                 gc[j] = run;
             }
-        }
+        };
+        if (tok0 + 8 <= len) stage(std::true_type{});
+        else stage(std::false_type{});
         // sums of squares of q (values 0-7) and k (8-15) per token, reduce-scattered
         // over the warp: afterwards lanes 2v and 2v+1 hold value v's sum over 64 channels
 #pragma unroll
@@ -430,9 +477,26 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         // packed for the later fp16 MMAs.
         uint32_t kt[2][4], kp[2][4], vp[2][4];
         uint32_t kt_prev = 0, kp_prev = 0;
+        // Store addresses.  Every row-major tile here is K-major with the 128-byte
+        // swizzle and every row index is (multiple of 8) + j, so element (row0 + j,
+        // c0) sits at  tile + row-block offset + colpart + 128 j + ((lane/4 ^ j) << 4).
+        const uint32_t colpart = (uint32_t)(warp & 1) * 16384u + 4u * (lane & 3);   // 128-row tiles
+        const uint32_t colrec = (uint32_t)(warp & 1) * 8192u + 4u * (lane & 3);     // 64-row record tiles
+        const uint32_t chunk = (uint32_t)lane >> 2;
+        auto lap_off = [&](int row0) {   // row0: LAP row of token tok0 (a multiple of 8)
+            return (uint32_t)(row0 >> 7) * 32768u + (uint32_t)(row0 & 127) * 128u + colpart;
+        };
+        constexpr int kRowA[4] = {0, 48, 80, 96};     // LAP row - r of the A rows of column sub-tile b
+        constexpr int kRowP[3] = {144, 176, 192};     // LAP row - r of the off-diagonal P rows of b
+        const int rowA_diag = (a_sub == 0 ? 0 : a_sub == 1 ? 48 : a_sub == 2 ? 80 : 96) + tok0;
+        const uint32_t offA_diag = lap_off(rowA_diag);
+        unsigned char* const sRHL = sb + S_RHL + (uint32_t)tok0 * 128u + colpart;
+        unsigned char* const sQD = sb + S_QD + (uint32_t)tok0 * 128u + colpart;
+        unsigned char* const sLAP = sb + S_LAP;
+        unsigned char* const gQ = rec + REC_Q + (uint32_t)tok0 * 128u + colrec;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const int r = tok0 + j;
+            const uint32_t jo = 128u * j + ((chunk ^ j) << 4);   // row j of the 8-row block, swizzled
             const float nq = __shfl_sync(0xffffffffu, nv, 2 * j);
             const float nk = __shfl_sync(0xffffffffu, nv, 16 + 2 * j);
             const float2 q = __fmul2_rn(h2f(aq[j]), f2(nq));
@@ -442,31 +506,28 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
             const float2 iy = make_float2(ex2f(d.x), ex2f(d.y));           // iY = e^{G_r - G_en(a)} >= 1
             const float2 ky = __fmul2_rn(k, y);
             const uint32_t rh = pack_bf16(ky.x, ky.y);
-            const float2 rlo = __fadd2_rn(ky, make_float2(-bf2f(rh).x, -bf2f(rh).y));
-            sts32(sb + S_RHL + sw128_off(r, c0, 128), rh);
-            sts32(sb + S_RHL + sw128_off(64 + r, c0, 128), pack_bf16(rlo.x, rlo.y));
+            const float2 rhf = bf2f(rh);
+            const float2 rlo = __fadd2_rn(ky, make_float2(-rhf.x, -rhf.y));
+            sts32(sRHL + jo, rh);
+            sts32(sRHL + 64 * 128 + jo, pack_bf16(rlo.x, rlo.y));
             const float2 ki = __fmul2_rn(k, iy), qi = __fmul2_rn(q, iy);
-            {   // A row of the diagonal sub-tile
-                const int R = kGroup[a_sub][3] + (r - kGroup[a_sub][2]);
-                sts32(sb + S_LAP + (R >> 7) * 32768 + sw128_off(R & 127, c0, 128), pack_bf16(ki.x, ki.y));
-            }
+            sts32(sLAP + offA_diag + jo, pack_bf16(ki.x, ki.y));      // A row of the diagonal sub-tile
 #pragma unroll
             for (int b = 0; b < 3; ++b) {
                 if (b < a_sub) {
-                    const int RA = kGroup[b][3] + (r - kGroup[b][2]);
-                    const int RP = kGroup[4 + b][3] + (r - kGroup[4 + b][2]);
                     const float2 kf = __fmul2_rn(ki, Cb[b]), qf = __fmul2_rn(qi, Cb[b]);
-                    sts32(sb + S_LAP + (RA >> 7) * 32768 + sw128_off(RA & 127, c0, 128), pack_bf16(kf.x, kf.y));
-                    sts32(sb + S_LAP + (RP >> 7) * 32768 + sw128_off(RP & 127, c0, 128), pack_bf16(qf.x, qf.y));
+                    sts32(sLAP + lap_off(kRowA[b] + tok0) + jo, pack_bf16(kf.x, kf.y));
+                    sts32(sLAP + lap_off(kRowP[b] + tok0) + jo, pack_bf16(qf.x, qf.y));
                 }
             }
             const uint32_t qh = pack_bf16(qi.x, qi.y);
-            const float2 qlo = __fadd2_rn(qi, make_float2(-bf2f(qh).x, -bf2f(qh).y));
-            sts32(sb + S_QD + sw128_off(r, c0, 128), qh);
-            sts32(sb + S_QD + sw128_off(64 + r, c0, 128), pack_bf16(qlo.x, qlo.y));
+            const float2 qhf = bf2f(qh);
+            const float2 qlo = __fadd2_rn(qi, make_float2(-qhf.x, -qhf.y));
+            sts32(sQD + jo, qh);
+            sts32(sQD + 64 * 128 + jo, pack_bf16(qlo.x, qlo.y));
             // record: Q+ = q e^{G} = q iY E
             const float2 qp = __fmul2_rn(qi, E);
-            *reinterpret_cast<uint32_t*>(rec + REC_Q + sw128_off(r, c0, C)) = pack_f16(qp.x, qp.y);
+            *reinterpret_cast<uint32_t*>(gQ + jo) = pack_f16(qp.x, qp.y);
             // Kt = k e^{G_last - G} = k Y F;  (k e^G) = k iY E;  v.  Pairs of tokens are
             // transposed into per-channel rows: word w of channel e holds tokens 2w, 2w+1.
             const float2 ktf = __fmul2_rn(ky, F), kpf = __fmul2_rn(ki, E);
@@ -484,6 +545,8 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                 kp_prev = t_kp;
             }
         }
+        // the previous item's W / U0 MMAs read (k e^G)^T, v^T and T: they have long finished
+        if (k_iter > 0 && !ptx::mbar_wait(bar_mma2, par ^ 1u, WAIT_LIMIT_NS)) *abort_flag = 1;
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             *reinterpret_cast<uint4*>(rec + REC_KT + sw128_off(c0 + e, tok0, 128)) =
@@ -519,9 +582,14 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
             }
             ptx::mma_commit(bar_mma1);
             mma_pending = 1;
+            mma_par = par;
         }
         // the next item's gate inputs; its raw rows follow after the readout
         if (item + (int)gridDim.x < n_items) load_zb(item + gridDim.x);
+        if (k_iter > 0 && !*abort_flag) {
+            ptx::tc_fence_after();
+            wu_out(rec_prev);       // the previous item's W / U0 (its MMAs completed, see above)
+        }
         if (!ptx::mbar_wait(bar_mma1, par, WAIT_LIMIT_NS)) *abort_flag = 1;
         ptx::tc_fence_after();
         if (tid == 0 && !*abort_flag) mma_pending = 0;
@@ -635,11 +703,12 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
             for (int r = 0; r < 16; ++r) Xm[(ob + r) * LDS + ob + j] = x[r];
         }
         __syncthreads();
+        solve_premultiply(Am, Xm, tid);
         solve_level<1>(Am, Xm, tid);
         solve_level<2>(Am, Xm, tid);
         solve_level<3>(Am, Xm, tid);
 
-        // ---- 6. T = X Diag(beta) (fp16, blocks above the diagonal zero; rows 64-127 zero)
+        // ---- 6. T = X Diag(beta) (fp16, blocks above the diagonal zero)
         {
             const int r = tid >> 3, ch = tid & 7;   // 512 threads = 64 rows x 8 column groups
             float v[8], xr[8], b8[8];
@@ -649,7 +718,6 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
 #pragma unroll
             for (int e = 0; e < 8; ++e) v[e] = keep ? xr[e] * b8[e] : 0.f;
             *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 8 * ch, 128)) = pack8_f16(v);
-            *reinterpret_cast<uint4*>(sb + S_TT + 64 * 128 + 16 * tid) = make_uint4(0, 0, 0, 0);
         }
         ptx::fence_async_smem();
         ptx::tc_fence_before();
@@ -666,53 +734,28 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
             }
             ptx::mma_commit(bar_mma2);
             mma_pending = 2;
+            mma_par = par;
         }
-        if (!ptx::mbar_wait(bar_mma2, par, WAIT_LIMIT_NS)) *abort_flag = 1;
-        ptx::tc_fence_after();
-        if (tid == 0 && !*abort_flag) mma_pending = 0;
-
-        // ---- 7. W (lanes = tokens 0-63) and U0^T (lanes = values) to the record
-        if (!*abort_flag) {
-            if (warp < 8 && (warp & 3) < 2) {       // warps 0,1: keys 0-63; warps 4,5: keys 64-127
-                const int r = 32 * (warp & 3) + lane;
-                const int kb = 64 * (warp >> 2);
-                const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + TM_W + kb;
-#pragma unroll
-                for (int h32 = 0; h32 < 2; ++h32) {
-                    float v[32];
-                    ptx::tmem_ld32(taddr + 32 * h32, v);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<uint4*>(rec + REC_W + sw128_off(r, kb + 32 * h32 + 8 * q, C)) =
-                            pack8_f16(v + 8 * q);
-                }
-            } else if (warp >= 8 && warp < 12) {
-                const int vrow = 32 * (warp & 3) + lane;
-                const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + TM_U;
-#pragma unroll
-                for (int h32 = 0; h32 < 2; ++h32) {
-                    float v[32];
-                    ptx::tmem_ld32(taddr + 32 * h32, v);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<uint4*>(rec + REC_UT + sw128_off(vrow, 32 * h32 + 8 * q, 128)) =
-                            pack8_f16(v + 8 * q);
-                }
-            }
-        }
+        // W and U0^T of this item are read out while the next item's first MMAs run
+        rec_prev = rec;
         ptx::tc_fence_before();
         __syncthreads();
         if (*abort_flag) break;
     }
 
+    if (!*abort_flag && rec_prev != nullptr) {
+        if (!ptx::mbar_wait(bar_mma2, (k_iter - 1) & 1u, WAIT_LIMIT_NS)) *abort_flag = 1;
+        ptx::tc_fence_after();
+        if (!*abort_flag) wu_out(rec_prev);
+        if (tid == 0 && !*abort_flag) mma_pending = 0;
+    }
     cp_async_wait_all();  // this thread's copies of a prefetch that was not consumed
     if (*abort_flag && pend_raw) ptx::mbar_wait(bar_raw, raw_par, WAIT_LIMIT_NS);
     if (*abort_flag && tid == 0) {
         // record the timeout, then let this CTA's own MMAs land
         atomicExch(a.status, ERR_TIMEOUT);
-        const uint32_t par = k_iter & 1u;
-        if (mma_pending == 1) ptx::mbar_wait(bar_mma1, par, WAIT_LIMIT_NS);
-        if (mma_pending == 2) ptx::mbar_wait(bar_mma2, par, WAIT_LIMIT_NS);
+        if (mma_pending == 1) ptx::mbar_wait(bar_mma1, mma_par, WAIT_LIMIT_NS);
+        if (mma_pending == 2) ptx::mbar_wait(bar_mma2, mma_par, WAIT_LIMIT_NS);
     }
     ptx::tc_fence_before();
     __syncthreads();
