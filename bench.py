@@ -63,15 +63,16 @@ def source_sha(path):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, src: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
+def ncu_traffic(kernel: str, src: str, units: float):
+    """DRAM bytes of one launch processing `units` (token-heads or session-heads),
+    from the committed ncu summary scaled by the units it was captured on, or
+    None when the kernel source changed since the counters were taken."""
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)[kernel]
         if d.get("source_sha") != source_sha(src):
             return None
-        return float(d["dram_bytes_per_launch"]) * d.get("scale", 1.0)
+        return float(d["dram_bytes_per_launch"]) * units / float(d["units"])
     except Exception:
         return None
 
@@ -223,7 +224,7 @@ PREFILL_WORKLOADS = {"long": 3, "prefill": 2, "varlen": 4}
 
 def prefill_arm(args, dev, world, rank):
     import gated_delta_rule_04_gb300 as kda
-    w = kda_synth.workload(PREFILL_WORKLOADS[args.workload], device=dev)
+    w = kda_synth.workload(PREFILL_WORKLOADS[args.workload], device=dev, H=args.heads)
     H, T, W = w.H, w.total_tokens, w.H * D
     kp = kda.make_params(w.params.conv_w, w.params.A_log, w.params.dt_bias, w.params.norm_w,
                          io_dtype=w.io, algo=args.algo)
@@ -398,6 +399,8 @@ def main():
     ap.add_argument("--workload", default="long", choices=sorted(PREFILL_WORKLOADS),
                     help="prefill workload of the headline line: long (T=32768, H=96; the default), "
                          "prefill (T=4096, H=32) or varlen (8 sequences, H=64); the others are for profiling")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="override the head count of the prefill workload (smaller cases for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -443,7 +446,7 @@ def main():
     src_path = os.path.join(ROOT, "gated_delta_rule_04_gb300", "csrc", srcs[dom])
     roofline = {"bound": "hbm", "kernel": kernels[dom], "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm, "peak_kind": f"{peak_kind} copy bandwidth",
-                "traffic": ncu_traffic(kernels[dom], src_path),
+                "traffic": ncu_traffic(kernels[dom], src_path, T * H),
                 "algorithmic_bytes_per_launch": alg_bytes,
                 "bytes_per_token_head": alg_bytes / (T * H), "ms_per_launch": stage_ms[dom],
                 "stage_ms": dict(zip(stage_names, stage_ms)),
@@ -455,7 +458,7 @@ def main():
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_max"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": kda_synth.describe(w.idx) + ", fp32 state",
+        "config": {"workload": kda_synth.describe(w.idx, w.H) + ", fp32 state",
                    "global_batch": world * w.n_seqs, "seq_len": T, "heads": H, "algo": r["algo_resolved"],
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": f"inputs ({sum(t.numel() * t.element_size() for t in w.tokens.fields()) / 1e9:.2f} GB) larger than L2 (129 MB); no flush"},
@@ -473,7 +476,8 @@ def main():
             "ms_per_step": dr["ms"], "steps": dr["steps"],
             "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                          "frac": gbs / hbm, "peak_kind": f"{peak_kind} copy bandwidth",
-                         "traffic": ncu_traffic("decode_kernel", os.path.join(ROOT, "gated_delta_rule_04_gb300", "csrc", "kda_decode.cu")),
+                         "traffic": ncu_traffic("decode_kernel", os.path.join(ROOT, "gated_delta_rule_04_gb300", "csrc", "kda_decode.cu"),
+                                                dr["sessions"] * dr["H"]),
                          "algorithmic_bytes_per_launch": dr["bytes"]},
         }
     if not args.no_e2e:

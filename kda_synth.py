@@ -40,10 +40,10 @@ WORKLOADS = {
 }
 
 
-def describe(idx: int) -> str:
+def describe(idx: int, H=None) -> str:
     w = WORKLOADS[idx]
     lens = w["lens"] if w["lens"] is not None else varlen_lengths()
-    return (f"{w['name']}: {len(lens)} seq(s), {sum(lens)} tokens, H={w['H']}, d={HEAD_DIM}, "
+    return (f"{w['name']}: {len(lens)} seq(s), {sum(lens)} tokens, H={H or w['H']}, d={HEAD_DIM}, "
             f"{w['io']} I/O, warm-up {w['warmup']} tokens/seq")
 
 
