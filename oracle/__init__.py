@@ -9,7 +9,8 @@ token); this module only marshals numpy arrays through ctypes.  Each entry
 point states the passage it follows:
 
 * ``mixer``  -- the whole layer core: short conv + SiLU, q/k L2 norm, q scale,
-  lower-bounded gate, beta, gated delta recurrence, RMSNormGated
+  lower-bounded gate (or the earlier Kimi-Linear softplus gate), beta, gated
+  delta recurrence, RMSNormGated
   ("Kimi Delta Attention (KDA) -- analysis & C kernel plan", sections
   "The KDA layer, precisely" and "Recurrence"; "ferrox-models 0.8.0, module
   kda", module overview; "Kimi K3 - Retention gate", gate.py excerpt).
@@ -50,6 +51,7 @@ class _Params(ctypes.Structure):
         ("A_log", _dp),
         ("dt_bias", _dp),
         ("norm_w", _dp),
+        ("gate_kind", ctypes.c_int32),
     ]
 
 
@@ -121,13 +123,14 @@ class Params:
     l2_eps: float = 1e-6
     norm_eps: float = 1e-5
     q_scale: float = 0.0
+    gate_kind: int = 0  # 0: lower-bounded sigmoid gate; 1: -exp(A_log) softplus(z + dt_bias)
 
     def _c(self):
         self._keep = [_f64(self.conv_w), _f64(self.A_log), _f64(self.dt_bias), _f64(self.norm_w)]
         cw, al, db, nw = self._keep
         return _Params(
             self.num_heads, self.head_dim, self.gate_lower_bound, self.l2_eps, self.norm_eps,
-            self.q_scale, _ptr(cw), _ptr(al), _ptr(db), _ptr(nw),
+            self.q_scale, _ptr(cw), _ptr(al), _ptr(db), _ptr(nw), int(self.gate_kind),
         )
 
 

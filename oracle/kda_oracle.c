@@ -22,6 +22,9 @@
  *   Conv1d with padding kernel_size-1 and no bias.
  *   "Kimi K3 - Retention gate - OpenModelAtlas", excerpt of gate.py
  *   (naive_kda_lowerbound_gate): g = lower_bound * sigmoid(exp(A_log) * (z + dt_bias)).
+ *   The earlier Kimi-Linear gate (gate_kind 1), "Kimi Delta Attention (KDA) --
+ *   analysis & C kernel plan" (status note and "The KDA layer, precisely":
+ *   fused_kda_gate(..., A_log, bias=dt_bias)): g = -exp(A_log) * softplus(z + dt_bias).
  *
  * Readings where the sources leave a step open (each also listed in the design
  * notes of the repository):
@@ -64,9 +67,12 @@ typedef struct {
     const double* A_log;   /* [H] */
     const double* dt_bias; /* [H*D] */
     const double* norm_w;  /* [D] */
+    int32_t gate_kind;     /* 0: lower-bounded sigmoid gate; 1: -exp(A_log) softplus(z + dt_bias) */
 } kdao_params;
 
 static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+/* log(1 + e^x) without overflow */
+static double softplus(double x) { return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x)); }
 
 /* ------------------------------------------------------------------------ */
 /* Thread pool helper: run fn(i, ctx) for i in [0, n) over nthreads threads. */
@@ -309,7 +315,10 @@ static void prestage_token(const kdao_params* p, int h, const double* xwin /*[3]
     double ea = exp(p->A_log[h]);
     for (int i = 0; i < D; ++i) {
         int ch = h * D + i;
-        g[i] = p->gate_lower_bound * sigmoid(ea * (zrow[i] + p->dt_bias[ch]));
+        if (p->gate_kind == 1) /* Kimi-Linear decay gate, unbounded below */
+            g[i] = -ea * softplus(zrow[i] + p->dt_bias[ch]);
+        else
+            g[i] = p->gate_lower_bound * sigmoid(ea * (zrow[i] + p->dt_bias[ch]));
     }
     *beta = sigmoid(braw);
 }

@@ -328,6 +328,51 @@ def test_p8_gate_bounds_and_special_values():
     assert g.shape == (T, W)
 
 
+def test_p8b_softplus_gate_special_values():
+    """The earlier Kimi-Linear gate g = -exp(A_log) softplus(z + dt_bias):
+    z = -dt_bias gives -exp(A_log) ln 2; z + dt_bias = ln(e - 1) gives
+    -exp(A_log) (softplus = 1); far below zero g is -exp(A_log) e^{z + dt_bias}
+    to first order; far above it is -exp(A_log) (z + dt_bias); always < 0."""
+    rng = np.random.default_rng(81)
+    H, D, T = 2, 4, 5
+    p = rand_params(rng, H, D, gate_kind=1)
+    tk = rand_tokens(rng, T, H, D)
+    ea = np.repeat(np.exp(p.A_log), D)
+    tk["z"][0] = -p.dt_bias
+    tk["z"][1] = np.log(np.e - 1.0) - p.dt_bias
+    tk["z"][2] = -40.0 - p.dt_bias
+    tk["z"][3] = 60.0 - p.dt_bias
+    out = oracle.mixer(p, [0, T], **tk, intermediates=True)
+    g = out["g"]
+    np.testing.assert_allclose(g[0], -ea * math.log(2.0), rtol=1e-15)
+    np.testing.assert_allclose(g[1], -ea, rtol=1e-14)
+    np.testing.assert_allclose(g[2], -ea * math.exp(-40.0), rtol=1e-15)   # e^x - e^{2x}/2 + ...
+    np.testing.assert_allclose(g[3], -ea * 60.0, rtol=1e-15)              # x + e^{-x} - ...
+    assert np.all(g < 0.0)
+    # unbounded below: far past the -5 bound of the other gate
+    assert np.all(g[3] < -5.0)
+
+
+def test_p8c_softplus_gate_decay_only():
+    """With beta = 0 and the softplus gate, the state only decays: after T
+    tokens S = Diag(e^{sum_t g_t}) S0, with every g_t at a closed-form point:
+    z + dt_bias = ln(e - 1) gives g = -exp(A_log), z + dt_bias = 0 gives
+    g = -exp(A_log) ln 2."""
+    rng = np.random.default_rng(82)
+    H, D, T = 2, 4, 4
+    p = rand_params(rng, H, D, gate_kind=1)
+    tk = rand_tokens(rng, T, H, D)
+    tk["b"][:] = -1e4                      # sigmoid underflows to exactly 0 in fp64
+    tk["z"][0::2] = np.log(np.e - 1.0) - p.dt_bias
+    tk["z"][1::2] = -p.dt_bias
+    S0 = rng.standard_normal((1, H, D, D))
+    out = oracle.mixer(p, [0, T], **tk, S_in=S0)
+    ea = np.exp(p.A_log)
+    for h in range(H):
+        G = -ea[h] * (2 * 1.0 + 2 * math.log(2.0))   # two tokens of each kind
+        np.testing.assert_allclose(out["S"][0, h], math.exp(G) * S0[0, h], rtol=1e-13)
+
+
 def test_p9_rmsnorm_gated_constant_and_scale():
     """Constant input a with w = 1 and gate logit 0 gives a / sqrt(a^2+eps) / 2."""
     H, D = 2, 8
