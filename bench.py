@@ -218,6 +218,14 @@ def decode_bytes_per_session_head(io_bytes):
     return 2 * D * D * 4 + 5 * D * io_bytes + io_bytes + D * io_bytes + 2 * 3 * 3 * D * io_bytes
 
 
+VERIFY_TOKENS = 4  # tokens per session in the verify-round measurement (K = 3 drafted + 1)
+
+
+def verify_bytes_per_session_head(io_bytes, n_tok):
+    # S read + written once; per token q,k,v,z,gout + b in, o out; ring read + written once
+    return 2 * D * D * 4 + n_tok * (6 * D * io_bytes + io_bytes) + 2 * 3 * 3 * D * io_bytes
+
+
 # ------------------------------------------------------------------- arms
 PREFILL_WORKLOADS = {"long": 3, "prefill": 2, "varlen": 4}
 
@@ -332,7 +340,22 @@ def decode_arm(args, dev):
     torch.cuda.synchronize()
     ms = start.elapsed_time(end) / steps
     n_units = w.n_seqs * w.H
-    return dict(ms=ms, sessions=w.n_seqs, H=w.H, bytes=n_units * decode_bytes_per_session_head(2) , steps=steps)
+    # a speculative verify round: VERIFY_TOKENS tokens per session in one call, in place
+    n = w.n_seqs
+    vt = kda_synth.draw_tokens(n * VERIFY_TOKENS, w.H, 1000 + 1 + 300_000, kda_synth.io_dtype(w.io), dev)
+    vrounds = [t.reshape(n, VERIFY_TOKENS, *t.shape[1:]).contiguous() for t in vt.fields()]
+    vo = torch.empty_like(vrounds[0])
+    for _ in range(args.warmup):
+        kda.kda_decode_multi(kp, *vrounds, S, ring, o=vo, stream=stream)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        kda.kda_decode_multi(kp, *vrounds, S, ring, o=vo, stream=stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    vms = start.elapsed_time(end) / steps
+    return dict(ms=ms, sessions=w.n_seqs, H=w.H, bytes=n_units * decode_bytes_per_session_head(2), steps=steps,
+                verify_ms=vms, verify_bytes=n_units * verify_bytes_per_session_head(2, VERIFY_TOKENS))
 
 
 def cpu_baseline(args, sample_heads=48, sample_tokens=32768):
@@ -479,6 +502,13 @@ def main():
                          "traffic": ncu_traffic("decode_kernel", os.path.join(ROOT, "gated_delta_rule_04_gb300", "csrc", "kda_decode.cu"),
                                                 dr["sessions"] * dr["H"]),
                          "algorithmic_bytes_per_launch": dr["bytes"]},
+            "verify": {
+                "workload": f"verify round: {VERIFY_TOKENS} tokens per session in one call (kda_decode_multi), "
+                            "same sessions and state",
+                "value": dr["sessions"] * VERIFY_TOKENS * world / (allreduce_max(dr["verify_ms"], world) / 1e3),
+                "unit": "session*tokens/s", "ms_per_step": dr["verify_ms"],
+                "hbm_frac": dr["verify_bytes"] / (dr["verify_ms"] / 1e3) / 1e9 / hbm,
+                "algorithmic_bytes_per_launch": dr["verify_bytes"]},
         }
     if not args.no_e2e:
         ms, h2d, d2h = e2e_arm(args, dev, w, r["kp"])

@@ -54,6 +54,7 @@ class kda_params(ctypes.Structure):
         ("A_log", _vp),
         ("dt_bias", _vp),
         ("norm_w", _vp),
+        ("gate_kind", ctypes.c_int32),
     ]
 
 
@@ -80,6 +81,8 @@ def lib():
         L.kda_prefill_with_events.restype = ctypes.c_int
         L.kda_decode.argtypes = [P, i32] + [_vp] * 6 + [_vp] * 3 + [_vp]
         L.kda_decode.restype = ctypes.c_int
+        L.kda_decode_multi.argtypes = [P, i32, i32] + [_vp] * 6 + [_vp, i32] + [_vp] * 5 + [_vp]
+        L.kda_decode_multi.restype = ctypes.c_int
         L.kda_workspace_status.argtypes = [_vp, _vp]
         L.kda_workspace_status.restype = ctypes.c_int
         L.kda_status_str.argtypes = [ctypes.c_int]
@@ -123,15 +126,21 @@ class Params:
         return ctypes.byref(self.struct)
 
 
+KDA_GATE_BOUNDED, KDA_GATE_SOFTPLUS = 0, 1
+_GATES = {"bounded": KDA_GATE_BOUNDED, "softplus": KDA_GATE_SOFTPLUS}
+
+
 def make_params(conv_w, A_log, dt_bias, norm_w, *, io_dtype: str = "bf16", algo: str = "auto",
                 gate_lower_bound: float = -5.0, l2_eps: float = 1e-6, norm_eps: float = 1e-5,
-                q_scale: float = 0.0) -> Params:
-    """conv_w [3][H*128][4], A_log [H], dt_bias [H*128], norm_w [128]: fp32 CUDA tensors."""
+                q_scale: float = 0.0, gate: str = "bounded") -> Params:
+    """conv_w [3][H*128][4], A_log [H], dt_bias [H*128], norm_w [128]: fp32 CUDA tensors.
+    gate: "bounded" (g = lb sigmoid(e^A (z + dt_bias))) or "softplus"
+    (g = -e^A softplus(z + dt_bias), unbounded below)."""
     H = int(A_log.shape[0])
     dt = {"f32": KDA_DTYPE_F32, "bf16": KDA_DTYPE_BF16}[io_dtype]
     tensors = tuple(t.contiguous() for t in (conv_w, A_log, dt_bias, norm_w))
     st = kda_params(H, 128, 4, dt, _ALGOS[algo], gate_lower_bound, l2_eps, norm_eps, q_scale,
-                    *[t.data_ptr() for t in tensors])
+                    *[t.data_ptr() for t in tensors], _GATES[gate])
     return Params(st, tensors, H, dt)
 
 
@@ -203,6 +212,32 @@ def kda_decode(params: Params, q, k, v, z, b, gout, S, ring, o=None, stream=None
                           _ptr(S), _ptr(ring), _ptr(o), _stream(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_decode")
+    return o
+
+
+KDA_DECODE_MAX_TOKENS = 64
+
+
+def kda_decode_multi(params: Params, q, k, v, z, b, gout, S_in, ring_in, S_out=None, ring_out=None,
+                     slots=None, o=None, stream=None):
+    """n_tokens consecutive tokens per session (a speculative verify round).
+    q, k, v, z, gout: [n][n_tokens][H*128]; b: [n][n_tokens][H].  S_in /
+    ring_in are state / ring pools [n_slots][...]; S_out / ring_out default to
+    them (in-place).  ``slots`` (int32 CUDA tensor [n]) maps sessions to pool
+    slots.  Keeping S_in / ring_in (separate outputs) allows a rollback: call
+    again with the accepted prefix of the tokens.  Returns o."""
+    import torch
+    n, n_tok = int(q.shape[0]), int(q.shape[1])
+    S_out = S_in if S_out is None else S_out
+    ring_out = ring_in if ring_out is None else ring_out
+    if o is None:
+        o = torch.empty_like(q)
+    n_slots = int(S_in.shape[0])
+    st = lib().kda_decode_multi(params.ref, n, n_tok, _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(b), _ptr(gout),
+                                _ptr(slots), n_slots, _ptr(S_in), _ptr(S_out), _ptr(ring_in), _ptr(ring_out),
+                                _ptr(o), _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode_multi")
     return o
 
 

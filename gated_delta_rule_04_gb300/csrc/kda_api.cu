@@ -34,7 +34,8 @@ bool chunked_available() { return chunked_kernel_built(); }
 
 kda_status resolve_algo(const kda_params* p, Algo* out) {
     const bool bf16 = p->io_dtype == KDA_DTYPE_BF16;
-    const bool bound_ok = p->gate_lower_bound >= -5.5f;  // 16 * 5.5 = 88 < ln(FLT_MAX)
+    // 16 * 5.5 = 88 < ln(FLT_MAX); the unbounded gate has no such bound
+    const bool bound_ok = p->gate_kind == KDA_GATE_BOUNDED && p->gate_lower_bound >= -5.5f;
     switch (p->algo) {
         case KDA_ALGO_SCAN: *out = Algo::Scan; return KDA_OK;
         case KDA_ALGO_CHUNKED:
@@ -53,7 +54,9 @@ kda_status check_params(const kda_params* p) {
     if (p->num_heads < 1 || p->num_heads > (1 << 16)) return KDA_ERR_INVALID_ARG;
     if (p->head_dim != D || p->conv_kernel != CONV_K) return KDA_ERR_UNSUPPORTED;
     if (p->io_dtype != KDA_DTYPE_F32 && p->io_dtype != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARG;
-    if (!(p->gate_lower_bound < 0.f) || !isfinite(p->gate_lower_bound)) return KDA_ERR_INVALID_ARG;
+    if (p->gate_kind != KDA_GATE_BOUNDED && p->gate_kind != KDA_GATE_SOFTPLUS) return KDA_ERR_INVALID_ARG;
+    if (p->gate_kind == KDA_GATE_BOUNDED && (!(p->gate_lower_bound < 0.f) || !isfinite(p->gate_lower_bound)))
+        return KDA_ERR_INVALID_ARG;
     if (!(p->l2_eps >= 0.f) || !(p->norm_eps >= 0.f) || !isfinite(p->l2_eps) || !isfinite(p->norm_eps))
         return KDA_ERR_INVALID_ARG;
     if (!isfinite(p->q_scale)) return KDA_ERR_INVALID_ARG;
@@ -231,7 +234,7 @@ kda_status prefill_impl(const kda_params* p, const void* q, const void* k, const
     float* ocore = reinterpret_cast<float*>(ws + L.ocore);
 
     PrestageArgs pa{q, k, v, z, b, p->conv_w, p->A_log, p->dt_bias, ring_in, d_cu, d_chunks,
-                    (int32_t)n_chunks, H, p->gate_lower_bound, p->l2_eps, qs,
+                    (int32_t)n_chunks, H, p->gate_lower_bound, p->l2_eps, qs, p->gate_kind,
                     ws + L.qh, ws + L.kh, ws + L.vh, gbuf, beta};
     if (algo == Algo::Scan) {
         e = launch_prestage(pa, io_bf16, /*out_fp16=*/0, /*cumsum=*/0, s);
@@ -292,22 +295,31 @@ kda_status kda_prefill_with_events(const kda_params* p, const void* q, const voi
                         ring_in, ring_out, o, workspace, workspace_bytes, stream, stage_events);
 }
 
-kda_status kda_decode(const kda_params* p, int32_t n_sessions, const void* q, const void* k,
-                      const void* v, const void* z, const void* b, const void* gout, float* S,
-                      void* ring, void* o, void* stream_) {
+kda_status kda_decode_multi(const kda_params* p, int32_t n_sessions, int32_t n_tokens, const void* q,
+                            const void* k, const void* v, const void* z, const void* b, const void* gout,
+                            const int32_t* slots, int32_t n_slots, const float* S_in, float* S_out,
+                            const void* ring_in, void* ring_out, void* o, void* stream_) {
     kda_status st = check_params(p);
     if (st != KDA_OK) return st;
-    if (n_sessions < 0) return KDA_ERR_INVALID_ARG;
+    if (n_sessions < 0 || n_tokens < 1 || n_tokens > KDA_DECODE_MAX_TOKENS || n_slots < 0) return KDA_ERR_INVALID_ARG;
     if (n_sessions == 0) return KDA_OK;
-    const void* ptrs[8] = {q, k, v, z, gout, o, S, ring};
-    for (int i = 0; i < 8; ++i)
+    if (slots == nullptr && n_slots < n_sessions) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[10] = {q, k, v, z, gout, o, S_in, S_out, ring_in, ring_out};
+    for (int i = 0; i < 10; ++i)
         if (ptrs[i] == nullptr || !aligned16(ptrs[i])) return KDA_ERR_INVALID_ARG;
     if (b == nullptr) return KDA_ERR_INVALID_ARG;
     if ((int64_t)n_sessions * p->num_heads > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
-    DecodeArgs da{q, k, v, z, b, gout, p->conv_w, p->A_log, p->dt_bias, p->norm_w, S, ring, o,
-                  n_sessions, p->num_heads, p->gate_lower_bound, p->l2_eps, p->norm_eps,
-                  resolved_q_scale(p)};
+    DecodeArgs da{q, k, v, z, b, gout, p->conv_w, p->A_log, p->dt_bias, p->norm_w, slots, S_in, S_out, ring_in,
+                  ring_out, o, n_sessions, p->num_heads, n_tokens, n_slots, p->gate_lower_bound, p->l2_eps,
+                  p->norm_eps, resolved_q_scale(p), p->gate_kind};
     return cuda_status(launch_decode(da, p->io_dtype == KDA_DTYPE_BF16, static_cast<cudaStream_t>(stream_)));
+}
+
+kda_status kda_decode(const kda_params* p, int32_t n_sessions, const void* q, const void* k,
+                      const void* v, const void* z, const void* b, const void* gout, float* S,
+                      void* ring, void* o, void* stream_) {
+    return kda_decode_multi(p, n_sessions, 1, q, k, v, z, b, gout, nullptr, n_sessions, S, S, ring, ring, o,
+                            stream_);
 }
 
 kda_status kda_workspace_status(void* workspace, void* stream_) {

@@ -104,6 +104,13 @@ __device__ __forceinline__ void lds8(const __nv_bfloat16* p, float (&x)[8]) {
 __device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 __device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
+// The decay gate g of channel value z + dt_bias (e_a = exp(A_log)): the
+// lower-bounded sigmoid gate (kind 0) or -e_a softplus(z + dt_bias) (kind 1).
+__device__ __forceinline__ float decay_gate(int kind, float lb, float e_a, float zb) {
+    if (kind == 1) return -e_a * (zb > 20.f ? zb : log1pf(expf(zb)));
+    return lb / (1.0f + expf(-e_a * zb));
+}
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -148,6 +155,7 @@ struct PrestageArgs {
     const ChunkDesc* chunks;  // device [n_chunks]
     int32_t n_chunks, H;
     float lb, l2_eps, q_scale;
+    int32_t gate_kind;        // kda_gate
     void *qh, *kh, *vh;       // outputs, fp16 (chunked path) or fp32 (scan path)
     float *gbuf, *beta;       // gate (raw g, or chunk-local cumulative sum) and beta
 };
@@ -188,13 +196,17 @@ cudaError_t launch_epilogue(const EpilogueArgs& a, int io_bf16, cudaStream_t s);
 bool chunked_kernel_built();
 
 struct DecodeArgs {
-    const void *q, *k, *v, *z, *b, *gout;
+    const void *q, *k, *v, *z, *b, *gout;   // [n][n_tok][H*128]; b [n][n_tok][H]
     const float *conv_w, *A_log, *dt_bias, *norm_w;
-    float* S;
-    void* ring;
-    void* o;
-    int32_t n, H;
+    const int32_t* slots;                   // [n] state-pool slot per session, or NULL (slot = session)
+    const float* S_in;                      // pools [n_slots][H][128][128]; S_out may alias S_in
+    float* S_out;
+    const void* ring_in;                    // pools [n_slots][3][3][H*128]; ring_out may alias ring_in
+    void* ring_out;
+    void* o;                                // [n][n_tok][H*128]
+    int32_t n, H, n_tok, n_slots;
     float lb, l2_eps, norm_eps, q_scale;
+    int32_t gate_kind;                      // kda_gate
 };
 cudaError_t launch_decode(const DecodeArgs& a, int io_bf16, cudaStream_t s);
 

@@ -174,7 +174,7 @@ extern "C" kda_status kda_prefill_noalloc(const kda_params* p, const void* q, co
     float* ocore = reinterpret_cast<float*>(ws + L.ocore);
     int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
     PrestageArgs pa{q, k, v, z, b, p->conv_w, p->A_log, p->dt_bias, ring_in, d_cu, d_chunks,
-                    (int32_t)nc, H, p->gate_lower_bound, p->l2_eps, qs,
+                    (int32_t)nc, H, p->gate_lower_bound, p->l2_eps, qs, p->gate_kind,
                     ws + L.qh, ws + L.kh, ws + L.vh, gbuf, beta};
     if (!chunked) {
         if (launch_prestage(pa, io_bf16, 0, 0, s) != cudaSuccess) return KDA_ERR_CUDA;

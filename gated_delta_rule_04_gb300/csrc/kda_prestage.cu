@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(PS_THREADS, 2) prestage_kernel(PrestageArgs a,
         if (tau < len) lds8(zs + (size_t)tau * D + cb, z8);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            float g = tau < len ? a.lb * sigmoid_fast(eA * (z8[e] + dtb[e])) : 0.f;
+            float g = tau < len ? decay_gate(a.gate_kind, a.lb, eA, z8[e] + dtb[e]) : 0.f;
             run[e] += g;
             gv[j][e] = cumsum ? run[e] : g;
         }

@@ -59,10 +59,23 @@ typedef enum {
 
 typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
 
-/* Prefill algorithm.  AUTO picks CHUNKED for bf16 I/O with a gate bound
- * >= -5.5 (the tensor-core form needs every 16-token rescaling factor below
- * e^88) and SCAN otherwise.  SCAN is the fp32 sequential recurrence. */
+/* Prefill algorithm.  AUTO picks CHUNKED for bf16 I/O with the bounded gate
+ * and a bound >= -5.5 (the tensor-core form needs every 16-token rescaling
+ * factor below e^88) and SCAN otherwise.  SCAN is the fp32 sequential
+ * recurrence. */
 typedef enum { KDA_ALGO_AUTO = 0, KDA_ALGO_SCAN = 1, KDA_ALGO_CHUNKED = 2 } kda_algo;
+
+/* Decay gate.
+ *   BOUNDED: g = gate_lower_bound * sigmoid(exp(A_log) (z + dt_bias)), in
+ *     (lb, 0). This is the Kimi K3 gate ("Kimi K3 - Retention gate -
+ *     OpenModelAtlas", gate formula).
+ *   SOFTPLUS: g = -exp(A_log) softplus(z + dt_bias), unbounded below. This is
+ *     the earlier Kimi-Linear gate ("Kimi Delta Attention (KDA) -- analysis &
+ *     C kernel plan", status note; fused_kda_gate with bias = dt_bias). With it
+ *     gate_lower_bound is ignored and prefill runs the fp32 scan: the
+ *     tensor-core chunk form needs the bound to keep its rescaling factors
+ *     finite. */
+typedef enum { KDA_GATE_BOUNDED = 0, KDA_GATE_SOFTPLUS = 1 } kda_gate;
 
 typedef struct {
     int32_t num_heads;      /* H >= 1 */
@@ -78,6 +91,7 @@ typedef struct {
     const float* A_log;     /* device [H] fp32 */
     const float* dt_bias;   /* device [H*128] fp32 */
     const float* norm_w;    /* device [128] fp32, shared by all heads */
+    int32_t gate_kind;      /* kda_gate */
 } kda_params;
 
 /* The prefill algorithm (KDA_ALGO_SCAN or KDA_ALGO_CHUNKED) that kda_prefill
@@ -150,6 +164,48 @@ kda_status kda_decode(const kda_params* p, int32_t n_sessions,
                       const void* q, const void* k, const void* v, const void* z,
                       const void* b, const void* gout,
                       float* S, void* ring, void* o, void* stream);
+
+/*
+ * Multi-token decode (speculative verify) over a state pool.
+ *
+ * Each of the n_sessions sessions advances by n_tokens consecutive tokens,
+ * 1 <= n_tokens <= KDA_DECODE_MAX_TOKENS, and produces one output row per
+ * token. The recurrence stays sequential over the register-resident state
+ * inside one launch. This follows the batched verify-rows call and its
+ * rollback on "memra-engine 0.124.0, module kda" (kda_verify_rows_cached,
+ * kda_verify_rollback_rows, KdaRowsStash). The step per token is the decode
+ * step above.
+ *
+ *   q,k,v,z,gout : device [n_sessions][n_tokens][H*128] io_dtype
+ *   b            : device [n_sessions][n_tokens][H] io_dtype
+ *   slots        : device int32 [n_sessions], the pool slot of each session,
+ *                  or NULL (session i uses slot i).
+ *                  - Slots must be distinct.
+ *                  - A slot outside [0, n_slots) skips its session: its
+ *                    state, ring and output rows are left untouched.
+ *   S_in, S_out  : device state pools [n_slots][H][128][128] fp32. S_in is
+ *                  read and S_out written; they may alias (in-place update).
+ *   ring_in, ring_out : device ring pools [n_slots][3][3][H*128] io_dtype,
+ *                  slot 0 oldest. They may alias.
+ *   o            : device [n_sessions][n_tokens][H*128] io_dtype
+ *
+ * Rollback (snapshot and replay). Keep S_in and ring_in, i.e. write to
+ * separate S_out and ring_out. If only the first j tokens of a round are
+ * accepted, call again with those j tokens from S_in and ring_in. This gives
+ * the state after token j-1, equal to kda_prefill over the same tokens up to
+ * rounding.
+ *
+ * Errors:
+ *   - KDA_ERR_INVALID_ARG: n_tokens out of range, null or misaligned pointers,
+ *     or n_slots < n_sessions without slots.
+ *   - KDA_ERR_UNSUPPORTED: head_dim or conv_kernel not supported.
+ */
+#define KDA_DECODE_MAX_TOKENS 64
+kda_status kda_decode_multi(const kda_params* p, int32_t n_sessions, int32_t n_tokens,
+                            const void* q, const void* k, const void* v, const void* z,
+                            const void* b, const void* gout, const int32_t* slots, int32_t n_slots,
+                            const float* S_in, float* S_out, const void* ring_in, void* ring_out,
+                            void* o, void* stream);
 
 /*
  * kda_prefill without a workspace, for callers that cannot allocate device

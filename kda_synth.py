@@ -72,11 +72,12 @@ class Params:
     l2_eps: float = 1e-6
     norm_eps: float = 1e-5
     q_scale: float = 0.0
+    gate_kind: int = 0     # 0: lower-bounded sigmoid gate; 1: -exp(A_log) softplus(z + dt_bias)
 
     def to(self, device) -> "Params":
         return Params(self.num_heads, self.head_dim, self.conv_w.to(device), self.A_log.to(device),
                       self.dt_bias.to(device), self.norm_w.to(device), self.gate_lower_bound,
-                      self.l2_eps, self.norm_eps, self.q_scale)
+                      self.l2_eps, self.norm_eps, self.q_scale, self.gate_kind)
 
     def head_slice(self, heads) -> "Params":
         """Parameters of a subset of heads (heads are independent)."""
@@ -85,7 +86,7 @@ class Params:
         ch = (idx[:, None] * D + torch.arange(D, device=idx.device)[None, :]).reshape(-1)
         return Params(len(heads), D, self.conv_w[:, ch, :].contiguous(), self.A_log[idx].contiguous(),
                       self.dt_bias[ch].contiguous(), self.norm_w.clone(), self.gate_lower_bound,
-                      self.l2_eps, self.norm_eps, self.q_scale)
+                      self.l2_eps, self.norm_eps, self.q_scale, self.gate_kind)
 
 
 def draw_params(H: int, seed: int, device="cpu", D: int = HEAD_DIM) -> Params:

@@ -38,7 +38,7 @@ def oracle_params(p: kda_synth.Params) -> oracle.Params:
     return oracle.Params(p.num_heads, p.head_dim, p.conv_w.double().cpu().numpy(),
                          p.A_log.double().cpu().numpy(), p.dt_bias.double().cpu().numpy(),
                          p.norm_w.double().cpu().numpy(), p.gate_lower_bound, p.l2_eps, p.norm_eps,
-                         p.q_scale)
+                         p.q_scale, p.gate_kind)
 
 
 def kda_params(p: kda_synth.Params, io: str, algo: str = "auto", device="cuda"):
@@ -46,7 +46,8 @@ def kda_params(p: kda_synth.Params, io: str, algo: str = "auto", device="cuda"):
     return kda.make_params(p.conv_w.to(device), p.A_log.to(device), p.dt_bias.to(device),
                            p.norm_w.to(device), io_dtype=io, algo=algo,
                            gate_lower_bound=p.gate_lower_bound, l2_eps=p.l2_eps,
-                           norm_eps=p.norm_eps, q_scale=p.q_scale)
+                           norm_eps=p.norm_eps, q_scale=p.q_scale,
+                           gate=("bounded", "softplus")[p.gate_kind])
 
 
 def to_np(t):

@@ -157,3 +157,33 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(kda, "_lib", None)
     with pytest.raises(kda.KdaLibraryMissing):
         kda.lib()
+
+
+def test_decode_multi_validation(L):
+    p = params()
+    f = FAKE
+
+    def call(n=4, n_tok=3, slots=None, n_slots=4, S_in=f, S_out=f, ring_in=f, ring_out=f, q=f, b=f):
+        return L.kda_decode_multi(ctypes.byref(p), n, n_tok, q, f, f, f, b, f, slots, n_slots, S_in, S_out,
+                                  ring_in, ring_out, f, None)
+
+    assert call(n=0) == kda.KDA_OK
+    assert call(n_tok=0) == kda.KDA_ERR_INVALID_ARG
+    assert call(n_tok=kda.KDA_DECODE_MAX_TOKENS + 1) == kda.KDA_ERR_INVALID_ARG
+    assert call(n=-1) == kda.KDA_ERR_INVALID_ARG
+    assert call(n_slots=3) == kda.KDA_ERR_INVALID_ARG          # identity slots need n_slots >= n
+    assert call(S_in=None) == kda.KDA_ERR_INVALID_ARG
+    assert call(ring_out=None) == kda.KDA_ERR_INVALID_ARG
+    assert call(S_out=f + 8) == kda.KDA_ERR_INVALID_ARG
+    assert call(b=None) == kda.KDA_ERR_INVALID_ARG
+    bad = params(head_dim=64)
+    assert L.kda_decode_multi(ctypes.byref(bad), 4, 3, f, f, f, f, f, f, None, 4, f, f, f, f, f,
+                              None) == kda.KDA_ERR_UNSUPPORTED
+
+
+def test_gate_kind_validation(L):
+    assert L.kda_prefill_algo(ctypes.byref(params(gate_kind=1))) == kda.KDA_ALGO_SCAN
+    assert prefill(L, params(gate_kind=1, algo=kda.KDA_ALGO_CHUNKED), [0, 64]) == kda.KDA_ERR_UNSUPPORTED
+    assert prefill(L, params(gate_kind=2), [0, 64]) == kda.KDA_ERR_INVALID_ARG
+    # the lower bound is not used by the softplus gate
+    assert L.kda_prefill_algo(ctypes.byref(params(gate_kind=1, gate_lower_bound=0.5))) == kda.KDA_ALGO_SCAN

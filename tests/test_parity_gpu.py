@@ -219,3 +219,32 @@ def test_zero_tokens_copies_state():
     torch.cuda.synchronize()
     assert torch.equal(S.cpu(), S_in)
     assert torch.equal(ring.cpu(), ring_in)
+
+
+# ---------------------------------------------------------------- softplus gate
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_softplus_gate_prefill_and_verify(io):
+    """The earlier Kimi-Linear gate (unbounded below) on the scan prefill and
+    on a multi-token decode round continuing from it."""
+    lens = [70, 3, 131]
+    p, tk, cu = small_case(io, lens, seed=91)
+    p.gate_kind = 1
+    n, H = len(lens), p.num_heads
+    kp = kda_params(p, io)
+    assert kda.kda_prefill_algo(kp) == "scan"
+    g = torch.Generator().manual_seed(92)
+    S_in = torch.randn(n, H, 128, 128, generator=g) * 0.05
+    ring_in = torch.randn(n, 3, 3, H * 128, generator=g).to(kda_synth.io_dtype(io))
+    o, S, ring = run_prefill(p, tk, cu, io, S_in=S_in, ring_in=ring_in)
+    ref = check_against_oracle(p, tk, cu, io, o, S, ring, S_in=S_in, ring_in=ring_in)
+    # a 3-token round per session from the prefill's state
+    n_tok = 3
+    vt = kda_synth.draw_tokens(n * n_tok, H, 93, kda_synth.io_dtype(io))
+    rounds = [t.reshape(n, n_tok, *t.shape[1:]).contiguous().to(DEV) for t in vt.fields()]
+    o2 = kda.kda_decode_multi(kp, *rounds, S, ring)
+    torch.cuda.synchronize()
+    ref2 = oracle_run(p, vt, list(range(0, n * n_tok + 1, n_tok)), S_in=torch.from_numpy(ref["S"]).float(),
+                      ring_in=torch.from_numpy(ref["ring"]).to(kda_synth.io_dtype(io)))
+    tol = tol_for(io)
+    assert_close("o", o2.reshape(n * n_tok, -1), ref2["o"], tol)
+    assert_close("S", S, ref2["S"], tol)
