@@ -7,8 +7,9 @@ d=128, bf16 I/O, fp32 state): one step is one kda_prefill call (pre-stage,
 recurrence, RMSNormGated epilogue, ring update) over the whole sequence, with
 inputs resident in HBM.  Alongside it:
   decode     batched decode of 256 sessions x 32 heads (state GB/s, session*tokens/s)
-  e2e        the same prefill through the C ABI from pinned HOST buffers,
-             host->device copies and the device->host read of o inside the timed region
+  e2e        the same prefill from pinned HOST buffers (kda_prefill_host: token
+             segments whose host->device copies and device->host read of o overlap
+             the kernels), all copies inside the timed region
   roofline   the dominant kernel's achieved HBM bandwidth vs the measured peak
   cpu_baseline  the fp64 oracle on a bounded sample of the same workload
 
@@ -285,23 +286,24 @@ def prefill_arm(args, dev, world, rank):
 
 
 def e2e_arm(args, dev, w, kp):
-    """Same prefill through the C ABI from pinned host buffers."""
+    """The same prefill from pinned HOST buffers through kda_prefill_host: the
+    library copies token segments in, runs them and copies o back, with the
+    copies of one segment overlapping the kernels of its neighbours."""
     import gated_delta_rule_04_gb300 as kda
     H, T, W = w.H, w.total_tokens, w.H * D
     host = [t.cpu().pin_memory() for t in w.tokens.fields()]
-    dbuf = [torch.empty_like(t, device=dev) for t in host]
-    o = torch.empty(T, W, dtype=torch.bfloat16, device=dev)
     o_host = torch.empty(T, W, dtype=torch.bfloat16).pin_memory()
-    S_out = torch.empty(1, H, D, D, device=dev)
-    ring_out = torch.empty(1, 3, 3, W, dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(kda.kda_prefill_workspace_bytes(kp, 1, T), dtype=torch.uint8, device=dev)
+    S_out = torch.empty(w.n_seqs, H, D, D, device=dev)
+    ring_out = torch.empty(w.n_seqs, 3, 3, W, dtype=torch.bfloat16, device=dev)
+    seg = args.segment
+    scratch = torch.empty(kda.kda_prefill_host_scratch_bytes(kp, w.cu_seqlens, seg), dtype=torch.uint8,
+                          device=dev)
     stream = torch.cuda.current_stream()
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
 
     def step():
-        for d_, h_ in zip(dbuf, host):
-            d_.copy_(h_, non_blocking=True)
-        kda.kda_prefill(kp, *dbuf, w.cu_seqlens, S_out=S_out, ring_out=ring_out, o=o, workspace=ws, stream=stream)
-        o_host.copy_(o, non_blocking=True)
+        kda.kda_prefill_host(kp, *host, w.cu_seqlens, S_out=S_out, ring_out=ring_out, o=o_host,
+                             segment_tokens=seg, scratch=scratch, stream=stream, h2d_stream=h2d, d2h_stream=d2h)
 
     for _ in range(max(1, args.warmup)):
         step()
@@ -313,9 +315,9 @@ def e2e_arm(args, dev, w, kp):
     end.record(stream)
     torch.cuda.synchronize()
     ms = start.elapsed_time(end) / args.steps
-    h2d = sum(t.numel() * t.element_size() for t in host)
-    d2h = o_host.numel() * o_host.element_size()
-    return ms, h2d, d2h
+    h2d_bytes = sum(t.numel() * t.element_size() for t in host)
+    d2h_bytes = o_host.numel() * o_host.element_size()
+    return ms, h2d_bytes, d2h_bytes, kda.kda_workspace_status(scratch, stream)
 
 
 def decode_arm(args, dev):
@@ -425,6 +427,8 @@ def main():
     ap.add_argument("--heads", type=int, default=None,
                     help="override the head count of the prefill workload (smaller cases for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--segment", type=int, default=4096,
+                    help="tokens per segment of the host-buffer (e2e) prefill")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
@@ -511,10 +515,11 @@ def main():
                 "algorithmic_bytes_per_launch": dr["verify_bytes"]},
         }
     if not args.no_e2e:
-        ms, h2d, d2h = e2e_arm(args, dev, w, r["kp"])
+        ms, h2d, d2h, e2e_status = e2e_arm(args, dev, w, r["kp"])
         ms = allreduce_max(ms, world)
         line["e2e"] = {"value": whole_job_value(T, ms, world), "unit": "tokens/s/layer", "ms_per_step": ms,
-                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "api": f"kda_prefill_host, {args.segment}-token segments", "workspace_status": e2e_status}
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args)
     if rank == 0:

@@ -5,7 +5,8 @@ behind the C ABI declared in ``include/kda.h``; PyTorch supplies device
 memory and the stream.  The functions carry the C names:
 
     kda_prefill_algo, kda_prefill_workspace_bytes, kda_prefill,
-    kda_prefill_with_events (as kda_prefill(..., stage_events=...)), kda_decode,
+    kda_prefill_with_events (as kda_prefill(..., stage_events=...)),
+    kda_prefill_host_scratch_bytes, kda_prefill_host, kda_decode, kda_decode_multi,
     kda_workspace_status, kda_status_str
 
 There is no fallback: if ``libkda.so`` is missing the import of this package
@@ -83,6 +84,11 @@ def lib():
         L.kda_decode.restype = ctypes.c_int
         L.kda_decode_multi.argtypes = [P, i32, i32] + [_vp] * 6 + [_vp, i32] + [_vp] * 5 + [_vp]
         L.kda_decode_multi.restype = ctypes.c_int
+        L.kda_prefill_host_scratch_bytes.argtypes = [P, ctypes.POINTER(ctypes.c_int64), i32, i64, i64]
+        L.kda_prefill_host_scratch_bytes.restype = sz
+        L.kda_prefill_host.argtypes = ([P] + [_vp] * 6 + [ctypes.POINTER(ctypes.c_int64), i32, i64] + [_vp] * 5
+                                       + [i64, _vp, sz, _vp, _vp, _vp])
+        L.kda_prefill_host.restype = ctypes.c_int
         L.kda_workspace_status.argtypes = [_vp, _vp]
         L.kda_workspace_status.restype = ctypes.c_int
         L.kda_status_str.argtypes = [ctypes.c_int]
@@ -199,6 +205,43 @@ def kda_prefill(params: Params, q, k, v, z, b, gout, cu_seqlens, S_in=None, S_ou
         st = lib().kda_prefill_with_events(*args, evs)
     if st != KDA_OK:
         raise KdaError(st, "kda_prefill")
+    return o, S_out, ring_out
+
+
+def kda_prefill_host_scratch_bytes(params: Params, cu_seqlens, segment_tokens: int) -> int:
+    cu, n, T = _cu_array(cu_seqlens)
+    return int(lib().kda_prefill_host_scratch_bytes(params.ref, cu, n, T, int(segment_tokens)))
+
+
+def kda_prefill_host(params: Params, q, k, v, z, b, gout, cu_seqlens, S_in=None, S_out=None,
+                     ring_in=None, ring_out=None, o=None, segment_tokens: int = 4096, scratch=None,
+                     stream=None, h2d_stream=None, d2h_stream=None, device=None):
+    """Prefill from HOST tensors (page-locked for the copies to overlap): the
+    library copies token segments in on ``h2d_stream``, runs them on
+    ``stream`` and copies the output back on ``d2h_stream``.  S_in / ring_in /
+    S_out / ring_out and ``scratch`` are CUDA tensors; missing ones are
+    allocated (``o`` as pinned host memory).  Synchronise ``stream`` before
+    reading ``o``.  Returns (o, S_out, ring_out)."""
+    import torch
+    cu, n, T = _cu_array(cu_seqlens)
+    H = params.num_heads
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if o is None:
+        o = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    if S_out is None:
+        S_out = torch.empty(n, H, 128, 128, dtype=torch.float32, device=dev)
+    if ring_out is None:
+        ring_out = torch.empty(n, 3, 3, H * 128, dtype=q.dtype, device=dev)
+    if scratch is None:
+        nbytes = int(lib().kda_prefill_host_scratch_bytes(params.ref, cu, n, T, int(segment_tokens)))
+        scratch = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    st = lib().kda_prefill_host(params.ref, _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(b), _ptr(gout),
+                                cu, n, T, _ptr(S_in), _ptr(S_out), _ptr(ring_in), _ptr(ring_out), _ptr(o),
+                                int(segment_tokens), _ptr(scratch), scratch.numel() * scratch.element_size(),
+                                _stream(stream), None if h2d_stream is None else _stream(h2d_stream),
+                                None if d2h_stream is None else _stream(d2h_stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prefill_host")
     return o, S_out, ring_out
 
 

@@ -163,12 +163,23 @@ cudaError_t mark(void* const* ev, int i, cudaStream_t s) {
     return cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s);
 }
 
-kda_status prefill_impl(const kda_params* p, const void* q, const void* k, const void* v,
-                        const void* z, const void* b, const void* gout,
-                        const int64_t* cu_seqlens_host, int32_t n_seqs, int64_t total_tokens,
-                        const float* S_in, float* S_out, const void* ring_in, void* ring_out,
-                        void* o, void* workspace, size_t workspace_bytes, void* stream_,
-                        void* const* ev) {
+}  // namespace
+
+namespace kda {
+
+kda_status prefill_check(const kda_params* p) {
+    kda_status st = check_params(p);
+    if (st != KDA_OK) return st;
+    Algo algo;
+    return resolve_algo(p, &algo);
+}
+
+kda_status prefill_run(const kda_params* p, const void* q, const void* k, const void* v,
+                       const void* z, const void* b, const void* gout,
+                       const int64_t* cu_seqlens_host, int32_t n_seqs, int64_t total_tokens,
+                       const float* S_in, float* S_out, const void* ring_in, void* ring_out,
+                       void* o, void* workspace, size_t workspace_bytes, void* stream_,
+                       void* const* ev, bool reset_status) {
     kda_status st = check_params(p);
     if (st != KDA_OK) return st;
     Algo algo;
@@ -221,8 +232,9 @@ kda_status prefill_impl(const kda_params* p, const void* q, const void* k, const
     const int64_t* d_coff = reinterpret_cast<const int64_t*>(ws + L.meta + L.off_chunk_off);
     const int32_t* d_order = reinterpret_cast<const int32_t*>(ws + L.meta + L.off_order);
     const ChunkDesc* d_chunks = reinterpret_cast<const ChunkDesc*>(ws + L.meta + L.off_chunks);
-    // the status word reports bounded-wait timeouts of this call only
-    cudaError_t e = cudaMemsetAsync(ws + L.status, 0, WS_ALIGN, s);
+    // the status word reports bounded-wait timeouts of this call only (of
+    // the whole segmented call when the caller clears it once)
+    cudaError_t e = reset_status ? cudaMemsetAsync(ws + L.status, 0, WS_ALIGN, s) : cudaSuccess;
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     e = cudaMemcpyAsync(ws + L.meta, meta.data(), L.meta_bytes, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
@@ -272,7 +284,7 @@ kda_status prefill_impl(const kda_params* p, const void* q, const void* k, const
     return KDA_OK;
 }
 
-}  // namespace
+}  // namespace kda
 
 extern "C" {
 
@@ -281,8 +293,8 @@ kda_status kda_prefill(const kda_params* p, const void* q, const void* k, const 
                        const int64_t* cu_seqlens_host, int32_t n_seqs, int64_t total_tokens,
                        const float* S_in, float* S_out, const void* ring_in, void* ring_out,
                        void* o, void* workspace, size_t workspace_bytes, void* stream) {
-    return prefill_impl(p, q, k, v, z, b, gout, cu_seqlens_host, n_seqs, total_tokens, S_in, S_out,
-                        ring_in, ring_out, o, workspace, workspace_bytes, stream, nullptr);
+    return prefill_run(p, q, k, v, z, b, gout, cu_seqlens_host, n_seqs, total_tokens, S_in, S_out, ring_in,
+                       ring_out, o, workspace, workspace_bytes, stream, nullptr, true);
 }
 
 kda_status kda_prefill_with_events(const kda_params* p, const void* q, const void* k, const void* v,
@@ -291,8 +303,8 @@ kda_status kda_prefill_with_events(const kda_params* p, const void* q, const voi
                                    int64_t total_tokens, const float* S_in, float* S_out,
                                    const void* ring_in, void* ring_out, void* o, void* workspace,
                                    size_t workspace_bytes, void* stream, void* const* stage_events) {
-    return prefill_impl(p, q, k, v, z, b, gout, cu_seqlens_host, n_seqs, total_tokens, S_in, S_out,
-                        ring_in, ring_out, o, workspace, workspace_bytes, stream, stage_events);
+    return prefill_run(p, q, k, v, z, b, gout, cu_seqlens_host, n_seqs, total_tokens, S_in, S_out, ring_in,
+                       ring_out, o, workspace, workspace_bytes, stream, stage_events, true);
 }
 
 kda_status kda_decode_multi(const kda_params* p, int32_t n_sessions, int32_t n_tokens, const void* q,

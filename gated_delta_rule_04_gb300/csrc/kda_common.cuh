@@ -210,4 +210,17 @@ struct DecodeArgs {
 };
 cudaError_t launch_decode(const DecodeArgs& a, int io_bf16, cudaStream_t s);
 
+// The parameter checks of kda_prefill: KDA_OK or the status it would return.
+kda_status prefill_check(const kda_params* p);
+
+// The checks and launch sequence of kda_prefill (ev: optional stage events).
+// reset_status = false leaves the workspace's error word as earlier calls
+// left it, so a caller that runs one problem as several calls on one
+// workspace reads the timeouts of all of them.
+kda_status prefill_run(const kda_params* p, const void* q, const void* k, const void* v, const void* z,
+                       const void* b, const void* gout, const int64_t* cu_seqlens_host, int32_t n_seqs,
+                       int64_t total_tokens, const float* S_in, float* S_out, const void* ring_in, void* ring_out,
+                       void* o, void* workspace, size_t workspace_bytes, void* stream, void* const* ev,
+                       bool reset_status);
+
 }  // namespace kda

@@ -233,6 +233,55 @@ kda_status kda_prefill_noalloc(const kda_params* p,
                                const float* S_in, float* S_out,
                                const void* ring_in, void* ring_out, void* o, void* stream);
 
+/*
+ * Prefill of a packed batch held in HOST memory, with the host<->device
+ * copies overlapped with the kernels.  An interface addition of this library:
+ * the sources time the mixer with its inputs already on the device.
+ *
+ * The batch is cut into segments of segment_tokens consecutive tokens.  Each
+ * segment runs as kda_prefill over the pieces of the sequences inside it,
+ * continuing every sequence from the state and ring its previous piece left
+ * in S_out / ring_out.  The result equals kda_prefill of the whole batch up
+ * to rounding (the chunk boundaries move with the segment boundaries).  Three
+ * staging sets in `scratch` rotate: while `stream` runs segment s,
+ * `h2d_stream` copies segment s+1 in and `d2h_stream` copies the output of
+ * segment s-1 out.
+ *
+ *   q,k,v,z,gout : HOST [total_tokens][H*128] io_dtype
+ *   b            : HOST [total_tokens][H] io_dtype
+ *   o            : HOST [total_tokens][H*128] io_dtype, written
+ *                  The host arrays should be page-locked (cudaHostAlloc or
+ *                  cudaHostRegister); pageable memory gives correct results
+ *                  but the copies then do not overlap.
+ *   cu_seqlens_host, n_seqs, total_tokens : as for kda_prefill
+ *   S_in, ring_in : device, as for kda_prefill (NULL = zero); may alias the outputs
+ *   S_out, ring_out : device, as for kda_prefill; both required (they carry
+ *                  each sequence across segments)
+ *   segment_tokens : tokens per segment, >= 1
+ *   scratch      : device, >= kda_prefill_host_scratch_bytes(), 256-byte
+ *                  aligned.  Its first 256 bytes are the error word that
+ *                  kda_workspace_status(scratch, stream) reads; it covers
+ *                  every segment of the call.
+ *   stream       : the work starts after what is already queued on it, and it
+ *                  is ordered after every copy when the call returns:
+ *                  synchronise it before reading o.
+ *   h2d_stream, d2h_stream : caller-created streams for the copies, or NULL
+ *                  (then the copies run on `stream` and nothing overlaps).
+ *
+ * Errors: the checks of kda_prefill plus KDA_ERR_INVALID_ARG for a NULL
+ * S_out or ring_out or segment_tokens < 1, and KDA_ERR_WORKSPACE for missing,
+ * short or misaligned scratch.  Every check runs before anything is queued.
+ */
+size_t kda_prefill_host_scratch_bytes(const kda_params* p, const int64_t* cu_seqlens_host, int32_t n_seqs,
+                                      int64_t total_tokens, int64_t segment_tokens);
+kda_status kda_prefill_host(const kda_params* p,
+                            const void* q, const void* k, const void* v, const void* z,
+                            const void* b, const void* gout,
+                            const int64_t* cu_seqlens_host, int32_t n_seqs, int64_t total_tokens,
+                            const float* S_in, float* S_out, const void* ring_in, void* ring_out,
+                            void* o, int64_t segment_tokens, void* scratch, size_t scratch_bytes,
+                            void* stream, void* h2d_stream, void* d2h_stream);
+
 /* Synchronises `stream` and reads the error word the prefill kernels keep in
  * `workspace`: KDA_OK, or KDA_ERR_TIMEOUT when a bounded in-kernel wait gave
  * up during an earlier call on that workspace (the word is then cleared). */

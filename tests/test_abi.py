@@ -187,3 +187,89 @@ def test_gate_kind_validation(L):
     assert prefill(L, params(gate_kind=2), [0, 64]) == kda.KDA_ERR_INVALID_ARG
     # the lower bound is not used by the softplus gate
     assert L.kda_prefill_algo(ctypes.byref(params(gate_kind=1, gate_lower_bound=0.5))) == kda.KDA_ALGO_SCAN
+
+
+# ---------------------------------------------------------------- kda_prefill_host
+STAGE_ALIGN = 256
+
+
+def _up(x):
+    return (x + STAGE_ALIGN - 1) // STAGE_ALIGN * STAGE_ALIGN
+
+
+def segment_piece_counts(cu, seg):
+    """Sequences that hold tokens of each segment [t0, t0 + seg), with the
+    empty sequences that start inside it: the piece count of every segment."""
+    T = cu[-1]
+    out = []
+    for t0 in range(0, T, seg):
+        t1 = min(T, t0 + seg)
+        first = next(i for i in range(len(cu) - 1) if cu[i + 1] > t0)
+        last = max(i for i in range(len(cu) - 1) if i == first or cu[i] < t1)
+        out.append((last - first + 1, t1 - t0))
+    return out
+
+
+def host_scratch(L, p, cu, seg):
+    arr = (ctypes.c_int64 * len(cu))(*cu)
+    return L.kda_prefill_host_scratch_bytes(ctypes.byref(p), arr, len(cu) - 1, cu[-1], seg)
+
+
+@pytest.mark.parametrize("cu, seg", [
+    ([0, 64], 64), ([0, 300], 100), ([0, 10, 10, 200, 700], 128), ([0, 5, 9, 13, 1000], 4),
+    ([0, 0, 0, 130, 130], 64),
+])
+def test_host_scratch_bytes(L, cu, seg):
+    """Scratch = the largest per-segment workspace + three staging sets."""
+    p = params()
+    H, es = 2, 2
+    ws = max(L.kda_prefill_workspace_bytes(ctypes.byref(p), n, t) for n, t in segment_piece_counts(cu, seg))
+    s = min(seg, cu[-1])
+    stage = 6 * _up(s * H * 128 * es) + _up(s * H * es)
+    assert host_scratch(L, p, cu, seg) == _up(ws) + 3 * stage
+
+
+def test_host_scratch_bytes_rejects(L):
+    p = params()
+    assert host_scratch(L, p, [0, 64], 0) == 0
+    assert host_scratch(L, p, [0], 64) == 0
+    assert host_scratch(L, params(head_dim=64), [0, 64], 64) == 0
+    assert host_scratch(L, p, [0, 64, 32], 64) == 0
+
+
+def prefill_host(L, p, cu, T=None, seg=64, scratch=FAKE, scratch_bytes=1 << 40, **ptrs):
+    arr = (ctypes.c_int64 * len(cu))(*cu)
+    n = len(cu) - 1
+    T = cu[-1] if T is None else T
+    a = dict(q=FAKE, k=FAKE, v=FAKE, z=FAKE, b=FAKE, gout=FAKE, S_in=None, S_out=FAKE,
+             ring_in=None, ring_out=FAKE, o=FAKE)
+    a.update(ptrs)
+    return L.kda_prefill_host(ctypes.byref(p), a["q"], a["k"], a["v"], a["z"], a["b"], a["gout"], arr, n, T,
+                              a["S_in"], a["S_out"], a["ring_in"], a["ring_out"], a["o"], seg, scratch,
+                              scratch_bytes, None, None, None)
+
+
+@pytest.mark.parametrize("kw, want", [
+    (dict(head_dim=64), kda.KDA_ERR_UNSUPPORTED),
+    (dict(num_heads=0), kda.KDA_ERR_INVALID_ARG),
+    (dict(algo=kda.KDA_ALGO_CHUNKED, io_dtype=kda.KDA_DTYPE_F32), kda.KDA_ERR_UNSUPPORTED),
+])
+def test_host_bad_params(L, kw, want):
+    assert prefill_host(L, params(**kw), [0, 64]) == want
+
+
+def test_host_validation(L):
+    p = params()
+    assert prefill_host(L, p, [1, 64]) == kda.KDA_ERR_INVALID_ARG
+    assert prefill_host(L, p, [0, 64], T=65) == kda.KDA_ERR_INVALID_ARG
+    assert prefill_host(L, p, [0, 64], seg=0) == kda.KDA_ERR_INVALID_ARG
+    assert prefill_host(L, p, [0, 64], seg=1 << 40) == kda.KDA_ERR_UNSUPPORTED
+    for name in ("S_out", "ring_out", "q", "b", "gout", "o"):
+        assert prefill_host(L, p, [0, 64], **{name: None}) == kda.KDA_ERR_INVALID_ARG, name
+    for name in ("S_out", "ring_out", "S_in", "ring_in"):
+        assert prefill_host(L, p, [0, 64], **{name: FAKE + 8}) == kda.KDA_ERR_INVALID_ARG, name
+    need = host_scratch(L, p, [0, 64], 64)
+    assert prefill_host(L, p, [0, 64], scratch_bytes=need - 1) == kda.KDA_ERR_WORKSPACE
+    assert prefill_host(L, p, [0, 64], scratch=None) == kda.KDA_ERR_WORKSPACE
+    assert prefill_host(L, p, [0, 64], scratch=FAKE + 16) == kda.KDA_ERR_WORKSPACE
+    assert prefill_host(L, p, [0], T=0) == kda.KDA_OK
