@@ -427,7 +427,7 @@ def main():
     ap.add_argument("--heads", type=int, default=None,
                     help="override the head count of the prefill workload (smaller cases for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--segment", type=int, default=4096,
+    ap.add_argument("--segment", type=int, default=2048,
                     help="tokens per segment of the host-buffer (e2e) prefill")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

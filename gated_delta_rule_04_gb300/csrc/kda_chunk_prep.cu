@@ -76,12 +76,19 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr uint32_t S_RQ = 0;                               // bf16 [67][128] raw q (row 0 = token t0 - 3)
 constexpr uint32_t S_RK = S_RQ + RAW_ROWS * ROW_B;
 constexpr uint32_t S_RV = S_RK + RAW_ROWS * ROW_B;
+constexpr uint32_t S_WUSTAGE = S_RQ;                       // between the conv stage and the next raw rows:
+                                                           //   the previous item's W and U0^T (2 x 16 KiB)
+constexpr uint32_t S_KTSTAGE = S_RQ + 32768;               //   and Kt (16 KiB), staged for bulk stores
 constexpr uint32_t S_OPS = 52224;                          // operand region (1 KiB aligned)
 constexpr uint32_t S_LAP = S_OPS;                          //   bf16 2 x [128 rows][128 keys]
 constexpr uint32_t S_QD = S_OPS + 65536;                   //   bf16 [128][128]: rows 0-63 hi, 64-127 lo
 constexpr uint32_t S_RHL = S_OPS + 98304;                  //   bf16 [128][128 keys] R: rows 0-63 hi, 64-127 lo
 constexpr uint32_t S_AM = S_OPS;                           // after the first MMAs: fp32 [64][68] A
 constexpr uint32_t S_XM = S_OPS + 17408;                   //   fp32 [64][68] X = (I + A)^{-1}
+constexpr uint32_t S_TAPS = S_OPS + 36864;                 //   the next item's conv taps [3][128][4] and
+                                                           //   dt_bias [128] (fp32), arriving with its raw rows
+constexpr uint32_t TAPS_BYTES = 3 * 2048 + 512;
+constexpr uint32_t S_PSTAGE = S_RHL;                       //   P (8 KiB), staged for a bulk store
 constexpr uint32_t S_TT = S_OPS + 131072;                  // fp16 [64 r][64 s] T; the W product reads it as
                                                            //   128 A rows, rows 64-127 being the first 8 KiB of
                                                            //   the next tile (their output lanes are unused)
@@ -93,7 +100,9 @@ constexpr uint32_t S_BT = S_TOT + 4096;                    // fp32 [64] beta
 constexpr uint32_t S_BAR = S_BT + 256;                     // 3 mbarriers, TMEM slot, abort flag
 constexpr uint32_t SMEM_BYTES = S_BAR + 64 + 1024;
 static_assert(S_RV + RAW_ROWS * ROW_B <= S_OPS, "raw rows overlap the operand region");
-static_assert(S_XM + 64 * LDS * 4 <= S_OPS + 131072, "solve tiles overflow the operand region");
+static_assert(S_KTSTAGE + 16384 <= S_RV + RAW_ROWS * ROW_B, "Kt staging stays inside the raw rows");
+static_assert(S_XM + 64 * LDS * 4 <= S_TAPS && S_TAPS + TAPS_BYTES <= S_QD, "solve tiles, taps");
+static_assert(S_PSTAGE + 8192 <= S_OPS + 131072, "P staging");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 static_assert(S_TT + 16384 <= S_VT, "the W product's A rows stay inside the T and (k e^G)^T tiles");
 
@@ -209,18 +218,22 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // copies by the warp, awaited with cp.async.wait) or are zero (left unloaded
 // and read as zero).  Rows past the end of the tensor read as zero;
 // rows past the chunk are never used.
-__device__ __forceinline__ void issue_raw(const PrepArgs& a, int item, uint32_t base, uint32_t bar, int lane) {
-    const int H = a.H, W = H * D;
-    const ChunkDesc cd = a.chunks[item / H];
-    const int h = item % H;
+__device__ __forceinline__ void issue_raw(const PrepArgs& a, const ChunkDesc& cd, int h, uint32_t base, uint32_t bar,
+                                          int lane) {
+    const int W = a.H * D;
     if (lane == 0) {
+        // one arrival on the barrier, expecting every byte below
+        ptx::mbar_expect_tx(bar, TAPS_BYTES + (cd.pos > 0 ? 3u * RAW_ROWS * ROW_B : 3u * C * ROW_B));
+        // the head's conv taps and dt_bias
+#pragma unroll
+        for (int pl = 0; pl < 3; ++pl)
+            ptx::bulk_g2s(base + S_TAPS + pl * 2048, a.conv_w + ((size_t)pl * W + h * D) * CONV_K, 2048, bar);
+        ptx::bulk_g2s(base + S_TAPS + 3 * 2048, a.dt_bias + h * D, 512, bar);
         if (cd.pos > 0) {
-            ptx::mbar_expect_tx(bar, 3u * RAW_ROWS * ROW_B);
 #pragma unroll
             for (int pl = 0; pl < 3; ++pl)
                 ptx::tma_load_2d(base + S_RQ + (uint32_t)pl * RAW_ROWS * ROW_B, &a.map67[pl], h * D, cd.t0 - RING, bar);
         } else {
-            ptx::mbar_expect_tx(bar, 3u * C * ROW_B);
 #pragma unroll
             for (int pl = 0; pl < 3; ++pl)
                 ptx::tma_load_2d(base + S_RQ + (uint32_t)pl * RAW_ROWS * ROW_B + RING * ROW_B, &a.map64[pl], h * D,
@@ -282,80 +295,103 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
     // gate inputs (this thread's tokens and channels) and the beta logit of an
     // item, loaded into registers one item ahead of use
     uint32_t zr[8];
-    float b_raw = 0.f;
-    auto load_zb = [&](int it) {
-        const ChunkDesc cn = a.chunks[it / H];
-        const int hn = it % H;
+    unsigned short b_raw = 0;   // bf16 bits
+
+    auto load_zb = [&](const ChunkDesc& cn, int hn) {
         const uint32_t* zp = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.z) +
                                                                (size_t)(cn.t0 + tok0) * W + hn * D + c0);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) zr[j] = tok0 + j < cn.len ? __ldg(zp + (size_t)j * (W / 2)) : 0u;
-        b_raw = tid < cn.len ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.b)[(size_t)(cn.t0 + tid) * H + hn])
-                             : 0.f;
+        for (int j = 0; j < 8; ++j) zr[j] = tok0 + j < cn.len ? __ldcg(zp + (size_t)j * (W / 2)) : 0u;
+        b_raw = tid < cn.len ? static_cast<const unsigned short*>(a.b)[(size_t)(cn.t0 + tid) * H + hn] : 0;
     };
-    if ((int)blockIdx.x < n_items) {
-        if (warp == PT / 32 - 1) issue_raw(a, blockIdx.x, base, bar_raw, lane);
-        load_zb(blockIdx.x);
+
+    // chunk descriptor of the current item, carried from the previous iteration
+    // This CTA's items: a contiguous range in head-major order (item j is chunk
+    // j % n_chunks of head j / n_chunks), so consecutive items share their
+    // head's conv taps and gate constants, which then stay in L1.
+    const int NC = a.n_chunks;
+    const int j_begin = (int)(((int64_t)blockIdx.x * n_items) / gridDim.x);
+    const int j_end = (int)(((int64_t)(blockIdx.x + 1) * n_items) / gridDim.x);
+    ChunkDesc cd = j_begin < j_end ? a.chunks[j_begin % NC] : ChunkDesc{0, 0, 0, 0};
+    if (j_begin < j_end) {
+        if (warp == PT / 32 - 1) issue_raw(a, cd, j_begin / NC, base, bar_raw, lane);
+        load_zb(cd, j_begin / NC);
     }
     // in-flight bookkeeping for the drain after a timeout: a raw load issued by
     // the last warp and not yet consumed (flag in that warp's lane 0), and the
     // MMAs of thread 0 (1 = bar_mma1, 2 = bar_mma2 in flight)
-    int pend_raw = (int)blockIdx.x < n_items && tid == PT - 32;
+    int pend_raw = j_begin < j_end && tid == PT - 32;
     uint32_t raw_par = 0;                           // phase parity of that load
     int mma_pending = 0;
     uint32_t mma_par = 0;                           // phase parity of those MMAs
     uint32_t k_iter = 0;
 
     // W (lanes = tokens 0-63) and U0^T (lanes = values) of an item, from TMEM to its
-    // record, spread over all 16 warps: warp w reads TMEM lane quarter w % 4 and
-    // column group g = w / 4 (W: 32 keys 32g.., quarters 0-1 only; U0^T: 16 tokens 16g..)
+    // record, by warps 4-15 (warps 0-3 issue the first MMAs meanwhile): warp w reads TMEM
+    // lane quarter w % 4 and, with gq = w / 4 - 1, the 16-column groups
+    // W: 3gq .. 3gq+2 (gq 2: 6-7; quarters 0-1 only), U0^T: {0,1}, {2}, {3}.
+    // The two tiles are assembled in shared memory in their record image and
+    // leave as two contiguous 16 KiB bulk stores (16-byte pieces scattered over
+    // 128-byte lines would cost one memory transaction each).  Every caller is
+    // CTA-uniform; warps 4-15 meet at named barrier 2.
     unsigned char* rec_prev = nullptr;
     auto wu_out = [&](unsigned char* rp) {
-        const int qd = warp & 3, g = warp >> 2;
+        if (warp < 4) return;
+        const int qd = warp & 3, gq = (warp >> 2) - 1;
         const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
-        if (qd < 2) {
-            const int r = 32 * qd + lane;
-            float v[32];
-            ptx::tmem_ld32(tl + TM_W + 32 * g, v);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4*>(rp + REC_W + sw128_off(r, 32 * g + 8 * q, C)) = pack8_f16(v + 8 * q);
-        }
-        {
-            const int vrow = 32 * qd + lane;
+        auto group_out = [&](uint32_t tcol, unsigned char* dst, int row, int col, int rows) {
             float v[16];
-            tmem_ld16(tl + TM_U + 16 * g, v);
-            *reinterpret_cast<uint4*>(rp + REC_UT + sw128_off(vrow, 16 * g, 128)) = pack8_f16(v);
-            *reinterpret_cast<uint4*>(rp + REC_UT + sw128_off(vrow, 16 * g + 8, 128)) = pack8_f16(v + 8);
+            tmem_ld16(tl + tcol, v);
+            *reinterpret_cast<uint4*>(dst + sw128_off(row, col, rows)) = pack8_f16(v);
+            *reinterpret_cast<uint4*>(dst + sw128_off(row, col + 8, rows)) = pack8_f16(v + 8);
+        };
+        if (qd < 2) {
+            const int wend = gq == 2 ? 8 : 3 * gq + 3;
+#pragma unroll 1
+            for (int c = 3 * gq; c < wend; ++c) group_out(TM_W + 16 * c, sb + S_WUSTAGE, 32 * qd + lane, 16 * c, C);
+        }
+#pragma unroll 1
+        for (int c = gq == 0 ? 0 : gq + 1; c < gq + 2; ++c)
+            group_out(TM_U + 16 * c, sb + S_WUSTAGE + 16384, 32 * qd + lane, 16 * c, 128);
+        ptx::fence_async_smem();
+        bar_sync_n(2, PT - 128);
+        if (tid == PT - 32) {
+            ptx::bulk_s2g(rp + REC_W, base + S_WUSTAGE, 16384);
+            ptx::bulk_s2g(rp + REC_UT, base + S_WUSTAGE + 16384, 16384);
+            ptx::bulk_commit();
         }
     };
 
 #pragma unroll 1
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++k_iter) {
+    for (int jt = j_begin; jt < j_end; ++jt, ++k_iter) {
         const uint32_t par = k_iter & 1u;
-        const ChunkDesc cd = a.chunks[item / H];
-        const int h = item % H, len = cd.len;
-        unsigned char* rec = static_cast<unsigned char*>(a.records) + (size_t)item * REC_BYTES;
+        const int h = jt / NC, len = cd.len;
+        // the next item's descriptor, read now so that nothing waits on it later
+        const int next = jt + 1;
+        const bool has_next = next < j_end;
+        const ChunkDesc cn = a.chunks[(has_next ? next : jt) % NC];
+        const int hn = next / NC;
+        unsigned char* rec = static_cast<unsigned char*>(a.records) + ((size_t)(jt % NC) * H + h) * REC_BYTES;
 
-        // ---- per-item constants (issued before the wait)
-        float2 wt[3][4];   // conv taps of the two channels
-#pragma unroll
-        for (int pl = 0; pl < 3; ++pl) {
-            const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.conv_w + ((size_t)pl * W + h * D + c0) * CONV_K));
-            const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.conv_w + ((size_t)pl * W + h * D + c0 + 1) * CONV_K));
-            // taps times 1/2: the conv yields x/2, the argument of tanh in the SiLU
-            wt[pl][0] = make_float2(0.5f * w0.x, 0.5f * w1.x); wt[pl][1] = make_float2(0.5f * w0.y, 0.5f * w1.y);
-            wt[pl][2] = make_float2(0.5f * w0.z, 0.5f * w1.z); wt[pl][3] = make_float2(0.5f * w0.w, 0.5f * w1.w);
-        }
-        const float2 dtb = __ldg(reinterpret_cast<const float2*>(a.dt_bias + h * D + c0));
-        const float eA = __expf(__ldg(a.A_log + h));
+        const float eA = __expf(__ldg(a.A_log + h));   // used late in the conv stage
         const bool zero_halo = cd.pos == 0 && a.ring_in == nullptr;
 
+        // raw rows, conv taps and dt_bias of this item
         if (!ptx::mbar_wait(bar_raw, par, WAIT_LIMIT_NS)) *abort_flag = 1;
         else pend_raw = 0;
         cp_async_wait_all();   // ring rows at a sequence start
         __syncthreads();
         if (*abort_flag) break;
+        float2 wt[3][4];   // conv taps of the two channels
+#pragma unroll
+        for (int pl = 0; pl < 3; ++pl) {
+            const float4 w0 = *reinterpret_cast<const float4*>(sb + S_TAPS + pl * 2048 + 16 * c0);
+            const float4 w1 = *reinterpret_cast<const float4*>(sb + S_TAPS + pl * 2048 + 16 * c0 + 16);
+            // taps times 1/2: the conv yields x/2, the argument of tanh in the SiLU
+            wt[pl][0] = make_float2(0.5f * w0.x, 0.5f * w1.x); wt[pl][1] = make_float2(0.5f * w0.y, 0.5f * w1.y);
+            wt[pl][2] = make_float2(0.5f * w0.z, 0.5f * w1.z); wt[pl][3] = make_float2(0.5f * w0.w, 0.5f * w1.w);
+        }
+        const float2 dtb = *reinterpret_cast<const float2*>(sb + S_TAPS + 3 * 2048 + 4 * c0);
 
         // ---- 1. conv + SiLU of q, k, v (kept as fp16 pairs); gate; sums of squares.
         // Octets inside the chunk (all but a ragged tail) skip the token masks.
@@ -437,7 +473,9 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], 1);
         if ((lane & 1) == 0) nrm[warp * 16 + (lane >> 1)] = sq[0];
         *reinterpret_cast<float2*>(tot + o * D + c0) = run;
-        if (tid < C) bt[tid] = tid < len ? rcpf(1.f + ex2f(-b_raw * LOG2E)) : 0.f;
+        if (tid < C) bt[tid] = tid < len ? rcpf(1.f + ex2f(-__uint_as_float((uint32_t)b_raw << 16) * LOG2E)) : 0.f;
+        // the previous item's staged P has left the operand region
+        if (tid == PT - 32) ptx::bulk_wait_read_all();
         __syncthreads();
 
         // ---- norms (lane 2v, 2v+1 computes value v; then broadcast)
@@ -549,7 +587,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         if (k_iter > 0 && !ptx::mbar_wait(bar_mma2, par ^ 1u, WAIT_LIMIT_NS)) *abort_flag = 1;
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            *reinterpret_cast<uint4*>(rec + REC_KT + sw128_off(c0 + e, tok0, 128)) =
+            *reinterpret_cast<uint4*>(sb + S_KTSTAGE + sw128_off(c0 + e, tok0, 128)) =
                 make_uint4(kt[e][0], kt[e][1], kt[e][2], kt[e][3]);
             *reinterpret_cast<uint4*>(sb + S_KPT + sw128_off(c0 + e, tok0, 128)) =
                 make_uint4(kp[e][0], kp[e][1], kp[e][2], kp[e][3]);
@@ -559,6 +597,13 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         ptx::fence_async_smem();
         ptx::tc_fence_before();
         __syncthreads();
+        if (tid == PT - 32) {
+            ptx::bulk_s2g(rec + REC_KT, base + S_KTSTAGE, 16384);
+            ptx::bulk_commit();
+        }
+        // no one sets the abort flag between here and the first-MMA wait, so this
+        // read is the same in every thread
+        const bool live = !*abort_flag;
 
         // ---- 3. A, off-diagonal P, diagonal P on the tensor cores
         constexpr uint32_t IDESC_BF16_N64 = ptx::idesc_bf16_f32(128, 64);
@@ -584,12 +629,13 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
             mma_pending = 1;
             mma_par = par;
         }
-        // the next item's gate inputs; its raw rows follow after the readout
-        if (item + (int)gridDim.x < n_items) load_zb(item + gridDim.x);
-        if (k_iter > 0 && !*abort_flag) {
+        // the previous item's W and U0^T (warps 4-15) while the MMAs run; then the
+        // next item's gate inputs
+        if (k_iter > 0 && live) {
             ptx::tc_fence_after();
-            wu_out(rec_prev);       // the previous item's W / U0 (its MMAs completed, see above)
+            wu_out(rec_prev);
         }
+        if (has_next) load_zb(cn, hn);
         if (!ptx::mbar_wait(bar_mma1, par, WAIT_LIMIT_NS)) *abort_flag = 1;
         ptx::tc_fence_after();
         if (tid == 0 && !*abort_flag) mma_pending = 0;
@@ -608,8 +654,8 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                     tmem_ld16(taddr + 16 * q4, v);
                     if (q4 == b) {
                         if (isP) {
-                            *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * b, C)) = pack8_f16(v);
-                            *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * b + 8, C)) = pack8_f16(v + 8);
+                            *reinterpret_cast<uint4*>(sb + S_PSTAGE + sw128_off(r, 16 * b, C)) = pack8_f16(v);
+                            *reinterpret_cast<uint4*>(sb + S_PSTAGE + sw128_off(r, 16 * b + 8, C)) = pack8_f16(v + 8);
                         } else {  // beta_r A, strictly lower part (zeros above in the diagonal block)
                             const float be = bt[r];
 #pragma unroll
@@ -667,24 +713,34 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
 #pragma unroll
                             for (int jj = 0; jj < 16; ++jj)
                                 if (16 * ta + jj > r) v[jj] = 0.f;
-                            *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * ta, C)) = pack8_f16(v);
-                            *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * ta + 8, C)) = pack8_f16(v + 8);
+                            *reinterpret_cast<uint4*>(sb + S_PSTAGE + sw128_off(r, 16 * ta, C)) = pack8_f16(v);
+                            *reinterpret_cast<uint4*>(sb + S_PSTAGE + sw128_off(r, 16 * ta + 8, C)) = pack8_f16(v + 8);
                         }
                     }
                     for (int tb = ta + 1; tb < 4; ++tb) {
-                        *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * tb, C)) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4*>(rec + REC_P + sw128_off(r, 16 * tb + 8, C)) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(sb + S_PSTAGE + sw128_off(r, 16 * tb, C)) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(sb + S_PSTAGE + sw128_off(r, 16 * tb + 8, C)) = make_uint4(0, 0, 0, 0);
                     }
                 }
             }
         }
+        ptx::fence_async_smem();
         ptx::tc_fence_before();
         __syncthreads();
         if (*abort_flag) break;
-        // the raw rows are consumed: the last warp (idle in the solve) fetches the next item's
-        if (warp == PT / 32 - 1 && item + (int)gridDim.x < n_items) {
-            issue_raw(a, item + gridDim.x, base, bar_raw, lane);
-            if (lane == 0) { pend_raw = 1; raw_par = (k_iter + 1) & 1u; }
+        // the last warp (idle in the solve) stores P and fetches the next item's raw
+        // rows and taps, once the staged W, U0^T and Kt have been read from that memory
+        if (warp == PT / 32 - 1) {
+            if (lane == 0) {
+                ptx::bulk_s2g(rec + REC_P, base + S_PSTAGE, 8192);
+                ptx::bulk_commit();
+                ptx::bulk_wait_read_all();
+            }
+            __syncwarp();
+            if (has_next) {
+                issue_raw(a, cn, hn, base, bar_raw, lane);
+                if (lane == 0) { pend_raw = 1; raw_par = (k_iter + 1) & 1u; }
+            }
         }
 
         // ---- 5. X = (I + A)^{-1}: diagonal 16 x 16 inverses by forward substitution
@@ -694,10 +750,18 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
             float x[16];
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
-                float t = (r == j) ? 1.f : 0.f;
+                // x_r = e_j - sum_{s<r} A[r][s] x_s, as four interleaved partial sums
+                const float* Lr = Am + (ob + r) * LDS + ob;
+                float p[4] = {(r == j) ? 1.f : 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int s = 0; s < r; ++s) t = fmaf(-Am[(ob + r) * LDS + ob + s], x[s], t);
-                x[r] = (r < j) ? 0.f : t;
+                for (int q = 0; 4 * q < r; ++q) {
+                    const float4 l4 = *reinterpret_cast<const float4*>(Lr + 4 * q);
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (4 * q + e < r) p[e] = fmaf(-lv[e], x[4 * q + e], p[e]);
+                }
+                x[r] = (r < j) ? 0.f : (p[0] + p[1]) + (p[2] + p[3]);
             }
 #pragma unroll
             for (int r = 0; r < 16; ++r) Xm[(ob + r) * LDS + ob + j] = x[r];
@@ -738,17 +802,22 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         }
         // W and U0^T of this item are read out while the next item's first MMAs run
         rec_prev = rec;
+        cd = cn;
         ptx::tc_fence_before();
         __syncthreads();
         if (*abort_flag) break;
     }
 
+    // (the loop leaves right after a barrier, so the flag reads the same everywhere)
     if (!*abort_flag && rec_prev != nullptr) {
         if (!ptx::mbar_wait(bar_mma2, (k_iter - 1) & 1u, WAIT_LIMIT_NS)) *abort_flag = 1;
         ptx::tc_fence_after();
+        if (tid == PT - 32) ptx::bulk_wait_read_all();   // the staging tiles are free
+        __syncthreads();
         if (!*abort_flag) wu_out(rec_prev);
         if (tid == 0 && !*abort_flag) mma_pending = 0;
     }
+    if (tid == PT - 32) ptx::bulk_wait_all();   // the staged record stores have landed
     cp_async_wait_all();  // this thread's copies of a prefetch that was not consumed
     if (*abort_flag && pend_raw) ptx::mbar_wait(bar_raw, raw_par, WAIT_LIMIT_NS);
     if (*abort_flag && tid == 0) {
