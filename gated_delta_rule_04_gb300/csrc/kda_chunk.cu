@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
     const uint32_t bar_mma23_0 = base + OFF_BAR + 24;    // + 8 * buffer (3)
     const uint32_t bar_ofree0 = base + OFF_BAR + 48;     // + 8 * buffer (3): D[b] read by the output warps
     const uint32_t bar_drain = base + OFF_BAR + 104;     // completion of in-flight MMAs after a timeout
+    const uint32_t bar_state = base + OFF_BAR + 112;     // MMA2 (the state update) of a chunk finished
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sb + OFF_BAR + 72);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sb + OFF_BAR + 76);
     // in-flight bookkeeping for the drain after a timeout (written by the issuing
@@ -125,6 +126,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
             ptx::mbar_init(bar_ofree0 + 8 * b, 1);
         }
         ptx::mbar_init(bar_drain, 1);
+        ptx::mbar_init(bar_state, 1);
         *abort_flag = 0;
         for (int i = 0; i < 6; ++i) pend[i] = 0;
         ptx::fence_mbar_init();
@@ -197,18 +199,25 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
             ptx::fence_async_smem();
             ptx::tc_fence_before();
             bar_sync(1, NSTATE);
-            // MMA1a (the chain's critical path): D[buf][:, 0:64] = S^T W^T
+            // MMA1: D[buf] = S^T [W; Q+]^T (columns 0-63: S^T W^T, 64-127: S^T Q+^T), once
+            // the output warps have read D[buf] of chunk c - NBUF
             if (tid == 0) {
-                ptx::tc_fence_after();
+                bool ok = true;
+                if (c >= NBUF) ok = ptx::mbar_wait(bar_ofree0 + 8 * buf, use ^ 1u, WAIT_LIMIT_NS);
+                if (!ok) {
+                    *abort_flag = 1;
+                } else {
+                    ptx::tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t koff = (kk & 3) * 32;  // 16 fp16 of K inside the 128-byte row
-                    const uint64_t ad = ptx::sdesc_sw128(base + OFF_ST + (kk >> 2) * 16384 + koff);
-                    const uint64_t bw = ptx::sdesc_sw128(stg + REC_W + (kk >> 2) * 8192 + koff);
-                    ptx::mma_f16(tmem + dcol, ad, bw, IDESC_N64, kk > 0);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t koff = (kk & 3) * 32;  // 16 fp16 of K inside the 128-byte row
+                        const uint64_t ad = ptx::sdesc_sw128(base + OFF_ST + (kk >> 2) * 16384 + koff);
+                        const uint64_t bwq = ptx::sdesc_sw128(stg + REC_W + (kk >> 2) * REC_PANEL + koff);
+                        ptx::mma_f16(tmem + dcol, ad, bwq, IDESC_N128, kk > 0);
+                    }
+                    ptx::mma_commit(bar_mma1);
+                    pend[4] = 1;
                 }
-                ptx::mma_commit(bar_mma1);
-                pend[4] = 1;
             }
             // while it runs: S^T *= decay (per key column), back into TMEM before MMA2
             {
@@ -224,23 +233,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
                         sv[j2][x] = lo.x; sv[j2][x + 1] = lo.y; sv[j2][x + 2] = hi.x; sv[j2][x + 3] = hi.y;
                     }
                     ptx::tmem_st32(tlane + 32 * j, sv[j2]);
-                }
-            }
-            // MMA1b (off the critical path): D[buf][:, 64:128] = S^T Q+^T, once the output
-            // warps have read D[buf] of chunk c - NBUF
-            if (tid == 0) {
-                bool ok = true;
-                if (c >= NBUF) ok = ptx::mbar_wait(bar_ofree0 + 8 * buf, use ^ 1u, WAIT_LIMIT_NS);
-                if (!ok) {
-                    *abort_flag = 1;
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t koff = (kk & 3) * 32;
-                        const uint64_t ad = ptx::sdesc_sw128(base + OFF_ST + (kk >> 2) * 16384 + koff);
-                        const uint64_t bq = ptx::sdesc_sw128(stg + REC_Q + (kk >> 2) * 8192 + koff);
-                        ptx::mma_f16(tmem + dcol + 64, ad, bq, IDESC_N64, kk > 0);
-                    }
                 }
             }
             // the abort flag (set by thread 0 above) is checked after this wait and barrier
@@ -275,20 +267,24 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
             if (tid == 0) {
                 ptx::tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
+                for (int kk = 0; kk < 4; ++kk) {   // MMA2: S^T += U^T Kt (the chain)
                     const uint64_t au = ptx::sdesc_sw128(base + OFF_UT + kk * 32);
-                    const uint64_t bk = ptx::sdesc_sw128(stg + REC_KT + kk * 32);
-                    const uint64_t bp = ptx::sdesc_sw128(stg + REC_P + kk * 32);
-                    ptx::mma_f16(tmem, au, bk, IDESC_N128, 1);             // S^T += U^T Kt
-                    ptx::mma_f16(tmem + dcol + 64, au, bp, IDESC_N64, 1);  // O^T += U^T P^T
+                    ptx::mma_f16(tmem, au, ptx::sdesc_sw128(stg + REC_KT + kk * 32), IDESC_N128, 1);
+                }
+                ptx::mma_commit(bar_state);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {   // MMA3: O^T += U^T P^T, finishing under the next S copy
+                    const uint64_t au = ptx::sdesc_sw128(base + OFF_UT + kk * 32);
+                    ptx::mma_f16(tmem + dcol + 64, au, ptx::sdesc_sw128(stg + REC_P + kk * 32), IDESC_N64, 1);
                 }
                 ptx::mma_commit(bar_mma23_0 + 8 * buf);
             }
-            if (!ptx::mbar_wait(bar_mma23_0 + 8 * buf, use, WAIT_LIMIT_NS)) *abort_flag = 1;
+            // the next chunk's U stage rewrites U^T only after its MMA1, which thread 0
+            // issues after this MMA3: that MMA1's commit covers MMA3 too
+            if (!ptx::mbar_wait(bar_state, (uint32_t)(c & 1), WAIT_LIMIT_NS)) *abort_flag = 1;
             bar_sync(1, NSTATE);
             if (*abort_flag) break;
             ptx::tc_fence_after();
-            if (tid == 0) pend[4] = 0;  // every MMA issued so far has completed
         }
         if (!*abort_flag) {
             // final state: S_out[key][value] = S^T[value][key]
@@ -417,6 +413,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
             ptx::mbar_wait(bar_drain, 0, WAIT_LIMIT_NS);
         }
     }
+
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 0) {

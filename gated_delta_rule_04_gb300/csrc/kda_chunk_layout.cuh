@@ -17,8 +17,12 @@ constexpr int CHUNK_T = 64;  // tokens per chunk
 // operand here is bounded (unit-norm keys and queries scaled by decays <= 1,
 // values of order 1-10, the UT-solve products), so the 3 extra mantissa bits
 // cut the operand rounding error 8x at the same tensor-core rate.
-constexpr int REC_W = 0;          // W     [64 tok rows][128 key]  2 panels x 64 rows x 128 B
-constexpr int REC_Q = 16384;      // Q+    [64 tok rows][128 key]  2 panels
+// W and Q+ are interleaved panel by panel (W keys 0-63, Q+ keys 0-63, W keys
+// 64-127, Q+ keys 64-127), so that [W; Q+] is one 128-row operand with the
+// 64-row W and Q+ panels REC_PANEL bytes apart.
+constexpr int REC_W = 0;          // W     [64 tok rows][128 key]  2 panels x 64 rows x 128 B, stride REC_PANEL
+constexpr int REC_Q = 8192;       // Q+    [64 tok rows][128 key]  2 panels, stride REC_PANEL
+constexpr int REC_PANEL = 16384;  // panel stride of W and Q+
 constexpr int REC_KT = 32768;     // Kt^T  [128 key rows][64 tok]  1 panel x 128 rows
 constexpr int REC_UT = 49152;     // U0^T  [128 val rows][64 tok]  1 panel x 128 rows
 constexpr int REC_P = 65536;      // P     [64 r rows][64 s]       1 panel x 64 rows

@@ -356,7 +356,8 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         ptx::fence_async_smem();
         bar_sync_n(2, PT - 128);
         if (tid == PT - 32) {
-            ptx::bulk_s2g(rp + REC_W, base + S_WUSTAGE, 16384);
+            ptx::bulk_s2g(rp + REC_W, base + S_WUSTAGE, 8192);                  // W keys 0-63
+            ptx::bulk_s2g(rp + REC_W + REC_PANEL, base + S_WUSTAGE + 8192, 8192);  // W keys 64-127
             ptx::bulk_s2g(rp + REC_UT, base + S_WUSTAGE + 16384, 16384);
             ptx::bulk_commit();
         }
@@ -519,7 +520,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         // swizzle and every row index is (multiple of 8) + j, so element (row0 + j,
         // c0) sits at  tile + row-block offset + colpart + 128 j + ((lane/4 ^ j) << 4).
         const uint32_t colpart = (uint32_t)(warp & 1) * 16384u + 4u * (lane & 3);   // 128-row tiles
-        const uint32_t colrec = (uint32_t)(warp & 1) * 8192u + 4u * (lane & 3);     // 64-row record tiles
+        const uint32_t colrec = (uint32_t)(warp & 1) * REC_PANEL + 4u * (lane & 3); // Q+ record panels
         const uint32_t chunk = (uint32_t)lane >> 2;
         auto lap_off = [&](int row0) {   // row0: LAP row of token tok0 (a multiple of 8)
             return (uint32_t)(row0 >> 7) * 32768u + (uint32_t)(row0 & 127) * 128u + colpart;
