@@ -17,23 +17,28 @@
 // Everything is computed transposed so that every MMA has M = 128 (the value
 // dimension) and the state lives in TMEM as S^T (lane = value index, column
 // = key index):
-//   MMA1  D[b][:, 0:64]   = S^T W^T          (A = S^T fp16 copy, B = W)
-//         D[b][:, 64:128] = S^T Q+^T         (B = Q+)
-//   SIMT  U^T = U0^T - D[b][:, 0:64]  -> fp16 tile
-//   MMA2  S^T += U^T Kt                    (onto the decayed state, B = Kt^T tile)
-//   MMA3  D[b][:, 64:128] += U^T P^T       (B = P)
-//   SIMT  S^T -> fp16 copy, S^T *= next decay
+//   MMA1  D[b] = S^T [W; Q+]^T              (A = S^T fp16 in TMEM, B = the W and
+//                                            Q+ panels; columns 0-63 S^T W^T,
+//                                            64-127 S^T Q+^T)
+//   SIMT  U^T = U0^T - D[b][:, 0:64]  -> fp16 in TMEM
+//   MMA2  S^T += U^T Kt                    (onto the decayed state, A = U^T in TMEM)
+//   MMA3  D[b][:, 64:128] += U^T P^T       (B = P), committed after MMA2 so that
+//                                           the chain waits for the state only
+//   SIMT  S^T -> fp16 copy in TMEM, S^T *= next decay
+// The fp16 A operands stay in tensor memory (tcgen05.st, then the MMA reads
+// them from there), so the chain has no shared-memory round trip.
 // Warp roles: warps 0-7 run this serial chain (each step split over two warps
 // per TMEM lane quarter); warps 8-15 (two per lane quarter, 32 tokens each)
 // take O^T of the chunk out of TMEM buffer b and apply the output norm while
-// the chain moves on (three D buffers: the chain may run two chunks ahead).
+// the chain moves on (two D buffers: the chain may run a chunk ahead).
 // O passes through a shared-memory tile, 32 tokens at a time, so that each
 // token row is normalised by the 8 threads holding it and the gate logits
-// are read and the output written as whole 16-byte row segments.  Each chunk's record arrives with one bulk
-// copy into a two-stage ring, two chunks ahead of use.  Every wait is
-// bounded; on timeout the kernel records the timeout in the workspace status
-// word, drains its own copies and MMAs and returns after freeing its tensor
-// memory.
+// are read and the output written as whole 16-byte row segments.  Each
+// chunk's record arrives with bulk copies into a two-stage ring, issued by a
+// chain thread as soon as the chunk before has finished its last MMA.  Every
+// wait is bounded; on timeout the kernel records the timeout in the
+// workspace status word, drains its own copies and MMAs and returns after
+// freeing its tensor memory.
 #include "kda_chunk_layout.cuh"
 #include "tc_ptx.cuh"
 
@@ -42,13 +47,14 @@ namespace {
 
 constexpr int NT = 512;                    // 16 warps: 8 state-chain warps + 8 output warps
 constexpr int NSTATE = 256;                // threads of the state chain
-constexpr uint32_t TMEM_COLS = 512;        // [0,128) S^T, then D[0], D[1], D[2] (128 columns each)
-constexpr int NBUF = 3;                    // D buffers: the chain may run two chunks ahead of the output
+constexpr uint32_t TMEM_COLS = 512;        // [0,128) S^T, [128,384) D[0], D[1] (128 columns each),
+                                           // [384,448) S^T fp16, [448,480) U^T fp16 (A operands)
+constexpr int NBUF = 2;                    // D buffers: the chain may run a chunk ahead of the output
+constexpr uint32_t TM_SH = 384;            // S^T as fp16 pairs: lane = value, column = 2 keys
+constexpr uint32_t TM_UH = 448;            // U^T as fp16 pairs: lane = value, column = 2 tokens
 constexpr uint32_t STAGE_STRIDE = 75776;   // REC_BYTES rounded up to 1 KiB
-constexpr uint32_t OFF_ST = 2 * STAGE_STRIDE;      // S^T fp16, 2 panels x 128 rows x 128 B
-constexpr uint32_t OFF_UT = OFF_ST + 32768;        // U^T fp16, 1 panel x 128 rows x 128 B
 constexpr int LDYS = 132;                          // padded row stride of the output tile
-constexpr uint32_t OFF_Y = OFF_UT + 16384;         // fp32 [32 tok][132] output of half a chunk
+constexpr uint32_t OFF_Y = 2 * STAGE_STRIDE;       // fp32 [32 tok][132] output of half a chunk
 constexpr uint32_t OFF_BAR = OFF_Y + 32 * LDYS * 4; // mbarriers + TMEM slot + flags
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 128 + 1024;  // + slack for 1 KiB alignment
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
@@ -62,6 +68,11 @@ __device__ __forceinline__ uint4 pack8_f16(const float* v) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) p[e] = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
     return u;
+}
+
+__device__ __forceinline__ uint32_t pack2_f16(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 __device__ __forceinline__ float tanh_fast(float x) {
@@ -185,18 +196,18 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
             if (*abort_flag) break;
             if (tid == 0) pend[s] = 0;
 
-            // ---- state transition: fp16 copy of S^T, the A operand of MMA1
+            // ---- state transition: fp16 copy of S^T in TMEM, the A operand of MMA1
             float sv[2][32];
 #pragma unroll
             for (int j2 = 0; j2 < 2; ++j2) {
                 const int j = 2 * half + j2;
                 ptx::tmem_ld32(tlane + 32 * j, sv[j2]);
+                uint32_t hp[16];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4*>(sb + OFF_ST + sw128_off(vrow, 32 * j + 8 * q, 128)) =
-                        pack8_f16(sv[j2] + 8 * q);
+                for (int e = 0; e < 16; ++e) hp[e] = pack2_f16(sv[j2][2 * e], sv[j2][2 * e + 1]);
+                ptx::tmem_st16u(tlane + TM_SH + 16 * j, hp);
             }
-            ptx::fence_async_smem();
+            ptx::tmem_wait_st();
             ptx::tc_fence_before();
             bar_sync(1, NSTATE);
             // MMA1: D[buf] = S^T [W; Q+]^T (columns 0-63: S^T W^T, 64-127: S^T Q+^T), once
@@ -211,12 +222,23 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t koff = (kk & 3) * 32;  // 16 fp16 of K inside the 128-byte row
-                        const uint64_t ad = ptx::sdesc_sw128(base + OFF_ST + (kk >> 2) * 16384 + koff);
                         const uint64_t bwq = ptx::sdesc_sw128(stg + REC_W + (kk >> 2) * REC_PANEL + koff);
-                        ptx::mma_f16(tmem + dcol, ad, bwq, IDESC_N128, kk > 0);
+                        ptx::mma_f16_ta(tmem + dcol, tmem + TM_SH + 8 * kk, bwq, IDESC_N128, kk > 0);
                     }
                     ptx::mma_commit(bar_mma1);
                     pend[4] = 1;
+                }
+            }
+            // Stage (c - 1) & 1 is free once the last MMA of chunk c - 1 (its MMA3) has
+            // finished: warp 1 (off the MMA-issuing warp) refills it with chunk c + 1.
+            // Buffer (c - 1) % NBUF completes no later phase before MMA1 of chunk c + 1.
+            if (tid == 32 && c >= 1 && c + 1 < nc) {
+                const int pb = (int)((c - 1) % NBUF);
+                if (!ptx::mbar_wait(bar_mma23_0 + 8 * pb, (uint32_t)(((c - 1) / NBUF) & 1), WAIT_LIMIT_NS))
+                    *abort_flag = 1;
+                else {
+                    ptx::fence_async_smem();
+                    issue_load(c + 1);
                 }
             }
             // while it runs: S^T *= decay (per key column), back into TMEM before MMA2
@@ -242,41 +264,39 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
             if (*abort_flag) break;
             ptx::tc_fence_after();
 
-            // ---- U^T = U0^T - (W S)^T as the fp16 A operand of MMA2 / MMA3 (this warp: 32 tokens)
+            // ---- U^T = U0^T - (W S)^T in TMEM, the fp16 A operand of MMA2 / MMA3 (this
+            // warp: 32 tokens)
             {
                 float v[32];
                 ptx::tmem_ld32(tlane + dcol + 32 * half, v);
+                uint32_t up[16];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const uint32_t off = sw128_off(vrow, 32 * half + 8 * q, 128);
                     const uint4 u0 = *reinterpret_cast<const uint4*>(sp + REC_UT + off);
                     const __half2* p = reinterpret_cast<const __half2*>(&u0);
-                    float u[8];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 f = __half22float2(p[e]);
-                        u[2 * e] = f.x - v[8 * q + 2 * e];
-                        u[2 * e + 1] = f.y - v[8 * q + 2 * e + 1];
+                        up[4 * q + e] = pack2_f16(f.x - v[8 * q + 2 * e], f.y - v[8 * q + 2 * e + 1]);
                     }
-                    *reinterpret_cast<uint4*>(sb + OFF_UT + off) = pack8_f16(u);
                 }
+                ptx::tmem_st16u(tlane + TM_UH + 16 * half, up);
             }
-            ptx::fence_async_smem();
+            ptx::tmem_wait_st();
             ptx::tc_fence_before();
             bar_sync(1, NSTATE);
             if (tid == 0) {
                 ptx::tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {   // MMA2: S^T += U^T Kt (the chain)
-                    const uint64_t au = ptx::sdesc_sw128(base + OFF_UT + kk * 32);
-                    ptx::mma_f16(tmem, au, ptx::sdesc_sw128(stg + REC_KT + kk * 32), IDESC_N128, 1);
-                }
+                for (int kk = 0; kk < 4; ++kk)     // MMA2: S^T += U^T Kt (the chain)
+                    ptx::mma_f16_ta(tmem, tmem + TM_UH + 8 * kk, ptx::sdesc_sw128(stg + REC_KT + kk * 32),
+                                    IDESC_N128, 1);
                 ptx::mma_commit(bar_state);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {   // MMA3: O^T += U^T P^T, finishing under the next S copy
-                    const uint64_t au = ptx::sdesc_sw128(base + OFF_UT + kk * 32);
-                    ptx::mma_f16(tmem + dcol + 64, au, ptx::sdesc_sw128(stg + REC_P + kk * 32), IDESC_N64, 1);
-                }
+                for (int kk = 0; kk < 4; ++kk)     // MMA3: O^T += U^T P^T, finishing under the next S copy
+                    ptx::mma_f16_ta(tmem + dcol + 64, tmem + TM_UH + 8 * kk, ptx::sdesc_sw128(stg + REC_P + kk * 32),
+                                    IDESC_N64, 1);
                 ptx::mma_commit(bar_mma23_0 + 8 * buf);
             }
             // the next chunk's U stage rewrites U^T only after its MMA1, which thread 0
@@ -339,12 +359,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
             const size_t row0 = (size_t)(bos + (int64_t)CHUNK_T * c);
             load_gout(c + 1, gnext);
             if (!ptx::mbar_wait(bar_mma23_0 + 8 * buf, use, WAIT_LIMIT_NS)) *abort_flag = 1;
-            // the chain is done with stage c & 1: fetch chunk c + 2 into it (issuing bulk
-            // copies takes time, so it is kept off the chain's critical path)
-            if (otid == 0 && c + 2 < nc && !*abort_flag) {
-                ptx::fence_async_smem();
-                issue_load(c + 2);
-            }
             bar_sync(2, 256);
             if (*abort_flag) break;
             ptx::tc_fence_after();
