@@ -31,9 +31,9 @@
 // per TMEM lane quarter); warps 8-15 (two per lane quarter, 32 tokens each)
 // take O^T of the chunk out of TMEM buffer b and apply the output norm while
 // the chain moves on (two D buffers: the chain may run a chunk ahead).
-// O passes through a shared-memory tile, 32 tokens at a time, so that each
+// O passes through a shared-memory tile, a whole chunk at a time, so that each
 // token row is normalised by the 8 threads holding it and the gate logits
-// are read and the output written as whole 16-byte row segments.  Each
+// are read and the output written as 64-byte row segments per 8 threads.  Each
 // chunk's record arrives with bulk copies into a two-stage ring, issued by a
 // chain thread as soon as the chunk before has finished its last MMA.  Every
 // wait is bounded; on timeout the kernel records the timeout in the
@@ -54,8 +54,8 @@ constexpr uint32_t TM_SH = 384;            // S^T as fp16 pairs: lane = value, c
 constexpr uint32_t TM_UH = 448;            // U^T as fp16 pairs: lane = value, column = 2 tokens
 constexpr uint32_t STAGE_STRIDE = 75776;   // REC_BYTES rounded up to 1 KiB
 constexpr int LDYS = 132;                          // padded row stride of the output tile
-constexpr uint32_t OFF_Y = 2 * STAGE_STRIDE;       // fp32 [32 tok][132] output of half a chunk
-constexpr uint32_t OFF_BAR = OFF_Y + 32 * LDYS * 4; // mbarriers + TMEM slot + flags
+constexpr uint32_t OFF_Y = 2 * STAGE_STRIDE;       // fp32 [64 tok][132] output of a chunk
+constexpr uint32_t OFF_BAR = OFF_Y + CHUNK_T * LDYS * 4; // mbarriers + TMEM slot + flags
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 128 + 1024;  // + slack for 1 KiB alignment
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 
@@ -220,8 +220,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
                 } else {
                     ptx::tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t koff = (kk & 3) * 32;  // 16 fp16 of K inside the 128-byte row
+                    for (int kk = 0; kk < 8; ++kk) {   // one N = 128 MMA per K step: the issue
+                        const uint32_t koff = (kk & 3) * 32;  // rate, not N, sets the time
                         const uint64_t bwq = ptx::sdesc_sw128(stg + REC_W + (kk >> 2) * REC_PANEL + koff);
                         ptx::mma_f16_ta(tmem + dcol, tmem + TM_SH + 8 * kk, bwq, IDESC_N128, kk > 0);
                     }
@@ -318,37 +318,39 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
         }
     } else {
         // ============================ output warps ===========================
-        // Per chunk: O^T (lane = value) -> fp32 tile [32 tokens][128 values],
-        // one token half at a time; then 8 threads per token row: sum of O^2
-        // (3 shuffles), o = O * rsqrt(mean + eps) * w * sigmoid(gout).
+        // Per chunk: O^T (lane = value) -> fp32 tile [64 tokens][128 values];
+        // then 8 threads per token row, two rows each: sum of O^2 (3 shuffles),
+        // o = O * rsqrt(mean + eps) * w * sigmoid(gout).
         const int ow = warp - 8;                       // 0..7
         const int th = ow >> 2;                        // the token half this warp's TMEM columns hold
         const int otid = tid - NSTATE;                 // 0..255
-        const int rt = otid >> 3, rseg = otid & 7;     // row pass: token rt of the half, values 16 rseg .. +15
-        const TO* gout = static_cast<const TO*>(a.gout);
-        TO* out = static_cast<TO*>(a.o);
+        // row pass: token rt of each half, values 32 q + 4 rseg .. +3 (q = 0..3), so
+        // that the 8 threads of a row read 128 contiguous bytes of the tile at a time
+        const int rt = otid >> 3, rseg = otid & 7;
+        static_assert(sizeof(TO) == 2, "the chunked path has bf16 I/O");
+        const unsigned short* gout = static_cast<const unsigned short*>(a.gout);
+        unsigned short* out = static_cast<unsigned short*>(a.o);
         float* ys = reinterpret_cast<float*>(sb + OFF_Y);
         float wv[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) wv[e] = a.norm_w[16 * rseg + e];
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) wv[4 * q + i] = a.norm_w[32 * q + 4 * rseg + i];
         // gate logits of this thread's two token rows, one chunk ahead of use
-        auto load_gout = [&](int64_t c, uint4 (&g)[2][2]) {
+        auto load_gout = [&](int64_t c, uint2 (&g)[2][4]) {
             const int64_t rem = L - (int64_t)CHUNK_T * c;
             const int Lc = rem < CHUNK_T ? (int)rem : CHUNK_T;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const int t = 32 * hf + rt;
-                if (c < nc && t < Lc) {
-                    const uint4* src = reinterpret_cast<const uint4*>(
-                        gout + (size_t)(bos + (int64_t)CHUNK_T * c + t) * W + (size_t)h * D + 16 * rseg);
-                    g[hf][0] = __ldg(src);
-                    g[hf][1] = __ldg(src + 1);
-                } else {
-                    g[hf][0] = g[hf][1] = make_uint4(0, 0, 0, 0);
-                }
+                const unsigned short* src =
+                    gout + (size_t)(bos + (int64_t)CHUNK_T * c + t) * W + (size_t)h * D + 4 * rseg;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    g[hf][q] = (c < nc && t < Lc) ? __ldg(reinterpret_cast<const uint2*>(src + 32 * q)) : make_uint2(0, 0);
             }
         };
-        uint4 gcur[2][2], gnext[2][2];
+        uint2 gcur[2][4], gnext[2][4];
         load_gout(0, gcur);
 #pragma unroll 1
         for (int64_t c = 0; c < nc; ++c) {
@@ -358,12 +360,31 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
             const int Lc = rem < CHUNK_T ? (int)rem : CHUNK_T;
             const size_t row0 = (size_t)(bos + (int64_t)CHUNK_T * c);
             load_gout(c + 1, gnext);
+            // sigmoid(g) = (1 + tanh(g / 2)) / 2 of this chunk's gate logits while the
+            // chain finishes the chunk; kept as fp16 pairs (the output is rounded to bf16,
+            // far coarser than the tanh's 2^-11)
+            uint32_t sgh[2][8];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(gcur[hf]);   // 8 pairs
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float2 gf = __bfloat1622float2(gh[e]);
+                    const float2 th2 = make_float2(tanh_fast(0.5f * gf.x), tanh_fast(0.5f * gf.y));
+                    const float2 sg = __ffma2_rn(th2, make_float2(0.5f, 0.5f), make_float2(0.5f, 0.5f));
+                    sgh[hf][e] = pack2_f16(sg.x, sg.y);
+                }
+            }
             if (!ptx::mbar_wait(bar_mma23_0 + 8 * buf, use, WAIT_LIMIT_NS)) *abort_flag = 1;
             bar_sync(2, 256);
             if (*abort_flag) break;
             ptx::tc_fence_after();
-            float o[32];
-            ptx::tmem_ld32(tlane + 128 + 128 * buf + 64 + 32 * th, o);
+            {
+                float o[32];
+                ptx::tmem_ld32(tlane + 128 + 128 * buf + 64 + 32 * th, o);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) ys[(32 * th + j) * LDYS + vrow] = o[j];
+            }
             // D[buf] is no longer needed: MMA1 of chunk c + NBUF may overwrite it
             ptx::tc_fence_before();
             bar_sync(2, 256);
@@ -371,14 +392,12 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int t = 32 * half + rt;          // token of this thread's row pass
-                if (th == half) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) ys[j * LDYS + vrow] = o[j];
-                }
-                bar_sync(2, 256);
                 float y[16];
-                lds8(ys + rt * LDYS + 16 * rseg, *reinterpret_cast<float(*)[8]>(y));
-                lds8(ys + rt * LDYS + 16 * rseg + 8, *reinterpret_cast<float(*)[8]>(y + 8));
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 y4 = *reinterpret_cast<const float4*>(ys + t * LDYS + 32 * q + 4 * rseg);
+                    y[4 * q] = y4.x; y[4 * q + 1] = y4.y; y[4 * q + 2] = y4.z; y[4 * q + 3] = y4.w;
+                }
                 float ss = 0.f;
 #pragma unroll
                 for (int e = 0; e < 16; ++e) ss = fmaf(y[e], y[e], ss);
@@ -387,31 +406,32 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
                 ss += __shfl_xor_sync(0xffffffffu, ss, 4);
                 const float rs = rsqrtf(ss * (1.0f / D) + a.eps);
                 if (t < Lc) {
-                    // o * rs * w * sigmoid(g), sigmoid(g) = (1 + tanh(g / 2)) / 2; the result
-                    // is rounded to bf16, far coarser than the tanh's 2^-11
+                    // o * rs * w * sigmoid(g)
                     float r[16];
-                    const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(gcur[half]);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const float2 gf = __bfloat1622float2(gh[e]);
                         const float2 yw = __fmul2_rn(make_float2(y[2 * e], y[2 * e + 1]),
                                                      __fmul2_rn(make_float2(wv[2 * e], wv[2 * e + 1]), make_float2(rs, rs)));
-                        const float2 th2 = make_float2(tanh_fast(0.5f * gf.x), tanh_fast(0.5f * gf.y));
-                        const float2 sg = __ffma2_rn(th2, make_float2(0.5f, 0.5f), make_float2(0.5f, 0.5f));
+                        const float2 sg = __half22float2(*reinterpret_cast<const __half2*>(&sgh[half][e]));
                         const float2 rr = __fmul2_rn(yw, sg);
                         r[2 * e] = rr.x;
                         r[2 * e + 1] = rr.y;
                     }
-                    const size_t roff = (row0 + t) * W + (size_t)h * D + 16 * rseg;
-                    Vec8<TO>::store(out + roff, *reinterpret_cast<float(*)[8]>(r));
-                    Vec8<TO>::store(out + roff + 8, *reinterpret_cast<float(*)[8]>(r + 8));
+                    const size_t roff = (row0 + t) * W + (size_t)h * D + 4 * rseg;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const __nv_bfloat162 b0 = __floats2bfloat162_rn(r[4 * q], r[4 * q + 1]);
+                        const __nv_bfloat162 b1 = __floats2bfloat162_rn(r[4 * q + 2], r[4 * q + 3]);
+                        *reinterpret_cast<uint2*>(out + roff + 32 * q) =
+                            make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
+                    }
                 }
-                bar_sync(2, 256);  // the tile is read before the next half overwrites it
             }
+            // (the next chunk writes the tile only after the barrier behind its MMA wait)
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                gcur[hf][0] = gnext[hf][0];
-                gcur[hf][1] = gnext[hf][1];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) gcur[hf][q] = gnext[hf][q];
             }
         }
     }
