@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
     if (slot < 0 || slot >= a.n_slots) return;  // invalid pool index: the session is skipped
 
     const float* Sg_in = a.S_in + ((size_t)slot * H + h) * D * D;
+    float* Sg_out = a.S_out + ((size_t)slot * H + h) * D * D;
     float4 Sr[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r)
@@ -155,8 +156,10 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
         }
         __syncthreads();
 
-        // ---- S = Diag(e) S + k^ d^T (registers)
+        // ---- S = Diag(e) S + k^ d^T (registers); after the last token each row
+        // streams out as soon as it is final (every read of S_in is behind us)
         const float4 d4 = *reinterpret_cast<const float4*>(&s_d[4 * lane]);
+        const bool last = t + 1 == a.n_tok;
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
             const int rr = 16 * warp + r;
@@ -165,6 +168,7 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
             Sr[r].y = fmaf(er, Sr[r].y, kr * d4.y);
             Sr[r].z = fmaf(er, Sr[r].z, kr * d4.z);
             Sr[r].w = fmaf(er, Sr[r].w, kr * d4.w);
+            if (last) __stcs(reinterpret_cast<float4*>(Sg_out + (size_t)rr * D) + lane, Sr[r]);
         }
 
         // ---- RMSNormGated epilogue
@@ -175,14 +179,10 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
             const float y = oj * r * a.norm_w[tid] / (1.0f + expf(-gt));
             static_cast<TI*>(a.o)[tok] = from_f32<TI>(y);
         }
-        __syncthreads();  // the shared vectors are rewritten by the next token
+        if (!last) __syncthreads();  // the shared vectors are rewritten by the next token
     }
 
-    // ---- state and ring out (written once, after every read of the inputs)
-    float* Sg_out = a.S_out + ((size_t)slot * H + h) * D * D;
-#pragma unroll
-    for (int r = 0; r < 16; ++r)
-        __stcs(reinterpret_cast<float4*>(Sg_out + (size_t)(16 * warp + r) * D) + lane, Sr[r]);
+    // ---- ring out (written once, after every read of the inputs)
     TI* ring_out = static_cast<TI*>(a.ring_out) + (size_t)slot * 3 * RING * W;
 #pragma unroll
     for (int pp = 0; pp < 2; ++pp) {
