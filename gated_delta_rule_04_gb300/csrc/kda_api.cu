@@ -117,6 +117,39 @@ kda_status check_cu(const int64_t* cu, int32_t n, int64_t T) {
 
 kda_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
+struct OverlapPlan {
+    int S = 0, sms = 0;
+    int64_t seg = 0, seg_chunks = 0;
+    size_t meta_stride = 0, off_meta = 0, off_cufull = 0, off_rec[2] = {0, 0}, total = 0;
+};
+constexpr size_t WS_COUNTER = 64;   // two work counters of the chunk preparation, inside the status block
+
+// The windows and their workspace layout for a T-token sequence (false when it
+// is too short for two windows).  No device query: the workspace size uses it.
+bool overlap_layout(const kda_params* p, int64_t T, OverlapPlan* pl) {
+    if (T < 2 * 8192) return false;
+    const int64_t s0 = std::min<int64_t>(4, T / 8192);   // windows of at least 8192 tokens
+    const int64_t seg = ((T + s0 - 1) / s0 + CHUNK - 1) / CHUNK * CHUNK;
+    pl->S = (int)((T + seg - 1) / seg);
+    if (pl->S < 2) return false;
+    pl->seg = seg;
+    pl->seg_chunks = seg / CHUNK;
+    pl->meta_stride = 4 * sizeof(int64_t) + sizeof(ChunkDesc) * (size_t)pl->seg_chunks;
+    size_t off = WS_ALIGN;  // status block
+    pl->off_meta = off;
+    off = align_up(off + pl->meta_stride * pl->S, WS_ALIGN);
+    pl->off_cufull = off;
+    off += WS_ALIGN;
+    const size_t rec_bytes = (size_t)REC_BYTES * (size_t)pl->seg_chunks * (size_t)p->num_heads;
+    for (int r = 0; r < 2; ++r) {
+        pl->off_rec[r] = off;
+        off = align_up(off + rec_bytes, WS_ALIGN);
+    }
+    pl->total = off;
+    return true;
+}
+
+
 }  // namespace
 }  // namespace kda
 
@@ -150,7 +183,10 @@ size_t kda_prefill_workspace_bytes(const kda_params* p, int32_t n_seqs, int64_t 
     if (n_seqs == 0 && total_tokens == 0) return 0;
     // upper bound on the chunk count: every sequence may add one partial chunk
     const int64_t n_chunks = total_tokens / CHUNK + n_seqs;
-    return layout(p, algo, n_seqs, total_tokens, n_chunks).total;
+    size_t need = layout(p, algo, n_seqs, total_tokens, n_chunks).total;
+    OverlapPlan pl;   // one long sequence may run as windows (see prefill_overlapped)
+    if (algo == Algo::Chunked && n_seqs == 1 && overlap_layout(p, total_tokens, &pl)) need = std::max(need, pl.total);
+    return need;
 }
 
 }  // extern "C"
@@ -166,6 +202,103 @@ cudaError_t mark(void* const* ev, int i, cudaStream_t s) {
 }  // namespace
 
 namespace kda {
+namespace {
+
+// ---- overlapped chunked prefill ------------------------------------------------
+// One sequence whose recurrence (one CTA per head) would leave SMs idle: the
+// sequence runs as S windows of whole chunks, and the recurrence of window w
+// overlaps the chunk preparation of window w + 1.  The preparation of a window
+// is two launches sharing one work counter: part 1 on the caller's stream with
+// as many CTAs as the recurrence leaves SMs free, part 2 on the recurrence
+// stream behind the recurrence of the window before, with one CTA per SM it
+// frees.  Windows start on the chunk grid of the sequence and read the conv halo
+// from the inputs, so the result is the same, bit for bit, as the single pass;
+// the state continues in S_out from window to window, and the ring is updated
+// once at the end.
+// Whether this call runs as windows: one long sequence, fewer heads than SMs.
+bool plan_overlap(const kda_params* p, int64_t T, size_t ws_bytes, OverlapPlan* pl) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    if (p->num_heads >= sms || !overlap_layout(p, T, pl)) return false;
+    pl->sms = sms;
+    return pl->total <= ws_bytes;
+}
+
+kda_status prefill_overlapped(const kda_params* p, const void* q, const void* k, const void* v, const void* z,
+                              const void* b, const void* gout, int64_t T, const float* S_in, float* S_out,
+                              const void* ring_in, void* ring_out, void* o, unsigned char* ws, cudaStream_t s,
+                              const OverlapPlan& pl, bool reset_status) {
+    const int H = p->num_heads, W = H * D;
+    // every window's cu, chunk offsets and chunk table, one upload
+    std::vector<unsigned char> meta(pl.meta_stride * pl.S, 0);
+    for (int w = 0; w < pl.S; ++w) {
+        const int64_t t0 = w * pl.seg, t1 = std::min(T, t0 + pl.seg);
+        const int64_t nck = (t1 - t0 + CHUNK - 1) / CHUNK;
+        int64_t* m = reinterpret_cast<int64_t*>(meta.data() + w * pl.meta_stride);
+        m[0] = t0; m[1] = t1; m[2] = 0; m[3] = nck;
+        ChunkDesc* cd = reinterpret_cast<ChunkDesc*>(m + 4);
+        for (int64_t i = 0; i < nck; ++i) {
+            const int64_t t = t0 + CHUNK * i;
+            cd[i] = ChunkDesc{0, (int32_t)t, (int32_t)std::min<int64_t>(CHUNK, t1 - t), (int32_t)t};
+        }
+    }
+    const int64_t cufull[2] = {0, T};
+    int32_t* status = reinterpret_cast<int32_t*>(ws);
+    int32_t* counters = reinterpret_cast<int32_t*>(ws + WS_COUNTER);   // [2], by window parity
+
+    int least = 0, greatest = 0;
+    cudaStream_t sr = nullptr;
+    cudaEvent_t ev[6] = {};   // start, prep part 1 [2], recurrence [2], end
+    kda_status st = KDA_OK;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&sr, cudaStreamNonBlocking, greatest) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    for (auto& e : ev)
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) st = KDA_ERR_CUDA;
+    auto ok = [&](cudaError_t e) { if (e != cudaSuccess) st = KDA_ERR_CUDA; return st == KDA_OK; };
+    if (st == KDA_OK && ok(cudaEventRecord(ev[0], s)) && ok(cudaStreamWaitEvent(sr, ev[0], 0)) &&
+        ok(reset_status ? cudaMemsetAsync(ws, 0, WS_ALIGN, s) : cudaSuccess) &&
+        ok(cudaMemcpyAsync(ws + pl.off_meta, meta.data(), meta.size(), cudaMemcpyHostToDevice, s)) &&
+        ok(cudaMemcpyAsync(ws + pl.off_cufull, cufull, sizeof(cufull), cudaMemcpyHostToDevice, s))) {
+        const float qs = resolved_q_scale(p);
+        for (int w = 0; w < pl.S && st == KDA_OK; ++w) {
+            const int r = w & 1;
+            unsigned char* rec = ws + pl.off_rec[r];
+            const unsigned char* mw = ws + pl.off_meta + w * pl.meta_stride;
+            const int64_t t0 = w * pl.seg, nck = (std::min(T, t0 + pl.seg) - t0 + CHUNK - 1) / CHUNK;
+            int32_t* counter = counters + r;
+            // records and counter of window w - 2 (same parity) are no longer in use
+            if (w >= 2 && !ok(cudaStreamWaitEvent(s, ev[3 + r], 0))) break;
+            if (!ok(cudaMemsetAsync(counter, 0, sizeof(int32_t), s))) break;
+            PrepArgs pr{q, k, v, z, b, ring_in, p->conv_w, p->A_log, p->dt_bias, p->gate_lower_bound, p->l2_eps, qs,
+                        reinterpret_cast<const ChunkDesc*>(mw + 4 * sizeof(int64_t)), (int32_t)nck, H, T, rec, status,
+                        counter, {}, {}};
+            // part 1 alongside the recurrence of window w - 1 (all SMs for window 0)
+            if (!ok(launch_chunk_prep(pr, s, w == 0 ? 0 : pl.sms - H)) || !ok(cudaEventRecord(ev[1 + r], s))) break;
+            // part 2 on the SMs that recurrence frees
+            if (w > 0 && !ok(launch_chunk_prep(pr, sr, H))) break;
+            if (!ok(cudaStreamWaitEvent(sr, ev[1 + r], 0))) break;
+            ChunkRecArgs ca{rec, w == 0 ? S_in : S_out, S_out, gout, p->norm_w, o, p->norm_eps,
+                            reinterpret_cast<const int64_t*>(mw), reinterpret_cast<const int64_t*>(mw) + 2, nullptr,
+                            status, 1, H};
+            if (!ok(launch_chunk_recurrence(ca, sr)) || !ok(cudaEventRecord(ev[3 + r], sr))) break;
+        }
+        if (st == KDA_OK && ring_out) {
+            RingArgs ra{q, k, v, ring_in, ring_out, reinterpret_cast<const int64_t*>(ws + pl.off_cufull), 1, W};
+            ok(launch_ring_update(ra, 1, sr));
+        }
+    }
+    // the caller's stream orders after everything on the recurrence stream
+    if (ev[5] == nullptr || cudaEventRecord(ev[5], sr) != cudaSuccess || cudaStreamWaitEvent(s, ev[5], 0) != cudaSuccess)
+        st = KDA_ERR_CUDA;
+    for (auto& e : ev)
+        if (e) cudaEventDestroy(e);
+    cudaStreamDestroy(sr);
+    return st;
+}
+
+}  // namespace
 
 kda_status prefill_check(const kda_params* p) {
     kda_status st = check_params(p);
@@ -204,6 +337,12 @@ kda_status prefill_run(const kda_params* p, const void* q, const void* k, const 
     const WsLayout L = layout(p, algo, n_seqs, total_tokens, n_chunks);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream_);
+    if (algo == Algo::Chunked && ev == nullptr && n_seqs == 1) {
+        OverlapPlan pl;
+        if (plan_overlap(p, total_tokens, workspace_bytes, &pl))
+            return prefill_overlapped(p, q, k, v, z, b, gout, total_tokens, S_in, S_out, ring_in, ring_out, o,
+                                      static_cast<unsigned char*>(workspace), s, pl, reset_status);
+    }
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     const int H = p->num_heads, W = H * D;
     const int io_bf16 = p->io_dtype == KDA_DTYPE_BF16;
@@ -260,7 +399,7 @@ kda_status prefill_run(const kda_params* p, const void* q, const void* k, const 
         // the chunk preparation runs the pre-stage itself
         if (mark(ev, 1, s) != cudaSuccess) return KDA_ERR_CUDA;
         PrepArgs pr{q, k, v, z, b, ring_in, p->conv_w, p->A_log, p->dt_bias, p->gate_lower_bound, p->l2_eps, qs,
-                    d_chunks, (int32_t)n_chunks, H, total_tokens, ws + L.rec, reinterpret_cast<int32_t*>(ws + L.status), {}, {}};
+                    d_chunks, (int32_t)n_chunks, H, total_tokens, ws + L.rec, reinterpret_cast<int32_t*>(ws + L.status), nullptr, {}, {}};
         e = launch_chunk_prep(pr, s);
         if (e != cudaSuccess || mark(ev, 2, s) != cudaSuccess) return KDA_ERR_CUDA;
         // the recurrence kernel applies the output norm itself
@@ -287,6 +426,15 @@ kda_status prefill_run(const kda_params* p, const void* q, const void* k, const 
 }  // namespace kda
 
 extern "C" {
+
+int32_t kda_prefill_windows(const kda_params* p, int32_t n_seqs, int64_t total_tokens, size_t workspace_bytes) {
+    if (check_params(p) != KDA_OK || n_seqs < 0 || total_tokens < 0) return -1;
+    Algo algo;
+    if (resolve_algo(p, &algo) != KDA_OK) return -1;
+    OverlapPlan pl;
+    if (algo == Algo::Chunked && n_seqs == 1 && plan_overlap(p, total_tokens, workspace_bytes, &pl)) return pl.S;
+    return 1;
+}
 
 kda_status kda_prefill(const kda_params* p, const void* q, const void* k, const void* v,
                        const void* z, const void* b, const void* gout,

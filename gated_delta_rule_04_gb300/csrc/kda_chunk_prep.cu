@@ -305,22 +305,39 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         b_raw = tid < cn.len ? static_cast<const unsigned short*>(a.b)[(size_t)(cn.t0 + tid) * H + hn] : 0;
     };
 
-    // chunk descriptor of the current item, carried from the previous iteration
-    // This CTA's items: a contiguous range in head-major order (item j is chunk
-    // j % n_chunks of head j / n_chunks), so consecutive items share their
-    // head's conv taps and gate constants, which then stay in L1.
+    // This CTA's items, in head-major order (item j is chunk j % n_chunks of head
+    // j / n_chunks, so consecutive items share their head's constants): either one
+    // contiguous range, or batches of PREP_BATCH taken from the work counter one
+    // batch ahead (the next item must be known an item ahead for its loads).
+    // [jt, j_stop) is the current batch and nb_start the first item of the next.
     const int NC = a.n_chunks;
-    const int j_begin = (int)(((int64_t)blockIdx.x * n_items) / gridDim.x);
-    const int j_end = (int)(((int64_t)(blockIdx.x + 1) * n_items) / gridDim.x);
-    ChunkDesc cd = j_begin < j_end ? a.chunks[j_begin % NC] : ChunkDesc{0, 0, 0, 0};
-    if (j_begin < j_end) {
-        if (warp == PT / 32 - 1) issue_raw(a, cd, j_begin / NC, base, bar_raw, lane);
-        load_zb(cd, j_begin / NC);
+    volatile int* s_take = reinterpret_cast<volatile int*>(sb + S_BAR + 32);
+    int jt, j_stop, nb_start;
+    if (a.work_counter != nullptr) {
+        if (tid == 0) {
+            s_take[0] = atomicAdd(a.work_counter, 1);
+            s_take[1] = atomicAdd(a.work_counter, 1);
+        }
+        __syncthreads();
+        jt = min(s_take[0] * PREP_BATCH, n_items);
+        j_stop = min(jt + PREP_BATCH, n_items);
+        nb_start = min(s_take[1] * PREP_BATCH, n_items);
+        __syncthreads();   // read before the loop rewrites s_take
+    } else {
+        jt = (int)(((int64_t)blockIdx.x * n_items) / gridDim.x);
+        j_stop = (int)(((int64_t)(blockIdx.x + 1) * n_items) / gridDim.x);
+        nb_start = n_items;
+    }
+    // chunk descriptor of the current item, carried from the previous iteration
+    ChunkDesc cd = jt < j_stop ? a.chunks[jt % NC] : ChunkDesc{0, 0, 0, 0};
+    if (jt < j_stop) {
+        if (warp == PT / 32 - 1) issue_raw(a, cd, jt / NC, base, bar_raw, lane);
+        load_zb(cd, jt / NC);
     }
     // in-flight bookkeeping for the drain after a timeout: a raw load issued by
     // the last warp and not yet consumed (flag in that warp's lane 0), and the
     // MMAs of thread 0 (1 = bar_mma1, 2 = bar_mma2 in flight)
-    int pend_raw = j_begin < j_end && tid == PT - 32;
+    int pend_raw = jt < j_stop && tid == PT - 32;
     uint32_t raw_par = 0;                           // phase parity of that load
     int mma_pending = 0;
     uint32_t mma_par = 0;                           // phase parity of those MMAs
@@ -364,12 +381,13 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
     };
 
 #pragma unroll 1
-    for (int jt = j_begin; jt < j_end; ++jt, ++k_iter) {
+    while (jt < j_stop) {
         const uint32_t par = k_iter & 1u;
         const int h = jt / NC, len = cd.len;
         // the next item's descriptor, read now so that nothing waits on it later
-        const int next = jt + 1;
-        const bool has_next = next < j_end;
+        const bool last_of_batch = jt + 1 == j_stop;
+        const int next = last_of_batch ? nb_start : jt + 1;
+        const bool has_next = next < n_items;
         const ChunkDesc cn = a.chunks[(has_next ? next : jt) % NC];
         const int hn = next / NC;
         unsigned char* rec = static_cast<unsigned char*>(a.records) + ((size_t)(jt % NC) * H + h) * REC_BYTES;
@@ -767,6 +785,8 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
 #pragma unroll
             for (int r = 0; r < 16; ++r) Xm[(ob + r) * LDS + ob + j] = x[r];
         }
+        // the batch after the next one (read at the end of this item)
+        if (tid == PT - 32 && last_of_batch && a.work_counter != nullptr) s_take[0] = atomicAdd(a.work_counter, 1);
         __syncthreads();
         solve_premultiply(Am, Xm, tid);
         solve_level<1>(Am, Xm, tid);
@@ -807,6 +827,14 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         ptx::tc_fence_before();
         __syncthreads();
         if (*abort_flag) break;
+        ++k_iter;
+        if (!last_of_batch) {
+            ++jt;
+        } else {
+            jt = nb_start;
+            j_stop = min(nb_start + PREP_BATCH, n_items);
+            nb_start = a.work_counter != nullptr ? min(s_take[0] * PREP_BATCH, n_items) : n_items;
+        }
     }
 
     // (the loop leaves right after a barrier, so the flag reads the same everywhere)
@@ -873,7 +901,7 @@ bool encode_rows(CUtensorMap* m, const void* base, int64_t T, int64_t W, uint32_
 
 }  // namespace
 
-cudaError_t launch_chunk_prep(const PrepArgs& args, cudaStream_t s) {
+cudaError_t launch_chunk_prep(const PrepArgs& args, cudaStream_t s, int max_ctas) {
     const int64_t items = (int64_t)args.n_chunks * args.H;
     if (items == 0) return cudaSuccess;
     if (items > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
@@ -891,7 +919,8 @@ cudaError_t launch_chunk_prep(const PrepArgs& args, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const int64_t grid = items < sms ? items : sms;
+    int64_t grid = items < sms ? items : sms;
+    if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
     chunk_prep_kernel<<<(unsigned)grid, PT, SMEM_BYTES, s>>>(a);
     return cudaGetLastError();
 }

@@ -26,8 +26,11 @@
  *
  * Conventions shared by every entry point
  *   - The caller owns every buffer.  The library allocates no device memory,
- *     holds no global state and never synchronises: all work is enqueued on
- *     `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *     holds no global state and never synchronises: all work is ordered on
+ *     `stream` (a cudaStream_t; NULL is the legacy default stream).  A call
+ *     may fan work out to streams it is given or creates, and joins them back
+ *     into `stream` before it returns (kda_prefill's overlapped windows,
+ *     kda_prefill_host's copy streams).
  *   - Every pointer marked "device" must be a device (or managed) address
  *     aligned to 16 bytes, except b which needs only element alignment.
  *   - Token tensors are token-major: element (t, c) at t*(H*128) + c.
@@ -132,6 +135,17 @@ kda_status kda_prefill(const kda_params* p,
                        const void* ring_in, void* ring_out,
                        void* o, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Number of windows kda_prefill runs these arguments as: 1 for the single
+ * pass, S >= 2 when one long sequence's recurrence would leave SMs idle
+ * (chunked path, one sequence, fewer heads than SMs, at least 16384 tokens,
+ * and a workspace that holds two windows' records).  Then the sequence runs
+ * as S windows of whole chunks: window w's chunk preparation overlaps the
+ * recurrence of window w - 1 on a second, high-priority stream that the call
+ * creates, and the result is bit-identical to the single pass.  The query
+ * needs a current CUDA device (it reads the SM count); -1 for arguments
+ * kda_prefill would reject. */
+int32_t kda_prefill_windows(const kda_params* p, int32_t n_seqs, int64_t total_tokens, size_t workspace_bytes);
+
 /* Same as kda_prefill, and records caller-created CUDA events on `stream` at
  * the stage boundaries, for profiling: stage_events[0] before the pre-stage,
  * [1] after the pre-stage (conv, norms, gate, beta), [2] after the chunk
@@ -140,7 +154,8 @@ kda_status kda_prefill(const kda_params* p,
  * [4] after the separate RMSNormGated epilogue (scan path; right after [3]
  * on the chunked path), [5] after the conv-ring update.  stage_events holds
  * KDA_PREFILL_EVENTS cudaEvent_t handles (any may be NULL to skip it) or is
- * NULL. */
+ * NULL.  With events the call always runs the single pass (one window), so
+ * that every stage boundary is a point on `stream`. */
 #define KDA_PREFILL_EVENTS 6
 kda_status kda_prefill_with_events(const kda_params* p,
                                    const void* q, const void* k, const void* v, const void* z,

@@ -273,3 +273,14 @@ def test_host_validation(L):
     assert prefill_host(L, p, [0, 64], scratch=None) == kda.KDA_ERR_WORKSPACE
     assert prefill_host(L, p, [0, 64], scratch=FAKE + 16) == kda.KDA_ERR_WORKSPACE
     assert prefill_host(L, p, [0], T=0) == kda.KDA_OK
+
+
+def test_prefill_windows_query(L):
+    p = params()
+    assert L.kda_prefill_windows(ctypes.byref(params(head_dim=64)), 1, 32768, 1 << 40) == -1
+    assert L.kda_prefill_windows(ctypes.byref(p), -1, 32768, 1 << 40) == -1
+    # several sequences, short ones, or the scan path: always the single pass
+    assert L.kda_prefill_windows(ctypes.byref(p), 2, 32768, 1 << 40) == 1
+    assert L.kda_prefill_windows(ctypes.byref(p), 1, 4096, 1 << 40) == 1
+    assert L.kda_prefill_windows(ctypes.byref(params(algo=kda.KDA_ALGO_SCAN)), 1, 32768, 1 << 40) == 1
+    assert L.kda_prefill_windows(ctypes.byref(p), 1, 32768, 1 << 40) >= 1   # needs a device for more
