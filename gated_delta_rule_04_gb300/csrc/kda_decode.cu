@@ -27,7 +27,8 @@ namespace {
 
 constexpr int DC_THREADS = 256;
 
-template <typename TI>
+// ONE: a.n_tok == 1 (plain decode), compiled without the token loop
+template <typename TI, bool ONE>
 __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
     const int H = a.H, W = H * D;
     const int n = blockIdx.x / H, h = blockIdx.x % H;
@@ -76,9 +77,10 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
     const float eA = expf(a.A_log[h]);
     const float dtb = a.dt_bias[c];
 
+    const int n_tok = ONE ? 1 : a.n_tok;
 #pragma unroll 1
-    for (int t = 0; t < a.n_tok; ++t) {
-        const size_t row = (size_t)n * a.n_tok + t;   // token row of (session, t)
+    for (int t = 0; t < n_tok; ++t) {
+        const size_t row = (size_t)n * n_tok + t;     // token row of (session, t)
         const size_t tok = row * W + c;
         auto conv_plane = [&](int pp) -> float {
             const TI xr = (pp == 0 ? plane0 : plane1)[tok];
@@ -159,7 +161,7 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
         // ---- S = Diag(e) S + k^ d^T (registers); after the last token each row
         // streams out as soon as it is final (every read of S_in is behind us)
         const float4 d4 = *reinterpret_cast<const float4*>(&s_d[4 * lane]);
-        const bool last = t + 1 == a.n_tok;
+        const bool last = t + 1 == n_tok;
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
             const int rr = 16 * warp + r;
@@ -197,8 +199,14 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
 cudaError_t launch_decode(const DecodeArgs& a, int io_bf16, cudaStream_t s) {
     const int64_t blocks = (int64_t)a.n * a.H;
     if (blocks == 0 || a.n_tok == 0) return cudaSuccess;
-    if (io_bf16) decode_kernel<__nv_bfloat16><<<(unsigned)blocks, DC_THREADS, 0, s>>>(a);
-    else decode_kernel<float><<<(unsigned)blocks, DC_THREADS, 0, s>>>(a);
+    const bool one = a.n_tok == 1;
+    if (io_bf16) {
+        if (one) decode_kernel<__nv_bfloat16, true><<<(unsigned)blocks, DC_THREADS, 0, s>>>(a);
+        else decode_kernel<__nv_bfloat16, false><<<(unsigned)blocks, DC_THREADS, 0, s>>>(a);
+    } else {
+        if (one) decode_kernel<float, true><<<(unsigned)blocks, DC_THREADS, 0, s>>>(a);
+        else decode_kernel<float, false><<<(unsigned)blocks, DC_THREADS, 0, s>>>(a);
+    }
     return cudaGetLastError();
 }
 
