@@ -629,6 +629,9 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         constexpr uint32_t IDESC_BF16_N128 = ptx::idesc_bf16_f32(128, 128);
         if (tid == 0) {
             ptx::tc_fence_after();
+            // three independent accumulator chains, interleaved by K step: A and the
+            // off-diagonal P (two M = 128 halves of the left rows) and the diagonal P
+            // ([q hi; q lo] x [R hi; R lo], N = 128; the readout adds hi*hi + hi*lo + lo*hi)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t koff = (kk & 3) * 32, pn = kk >> 2;
@@ -636,13 +639,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                 ptx::mma_f16(tmem + TM_D0, ptx::sdesc_sw128(base + S_LAP + pn * 16384 + koff), bR, IDESC_BF16_N64, kk > 0);
                 ptx::mma_f16(tmem + TM_D1, ptx::sdesc_sw128(base + S_LAP + 32768 + pn * 16384 + koff), bR, IDESC_BF16_N64,
                              kk > 0);
-            }
-            // diagonal P: [q hi; q lo] x [R hi; R lo] (N = 128); the readout adds hi*hi + hi*lo + lo*hi
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t koff = (kk & 3) * 32, pn = kk >> 2;
-                ptx::mma_f16(tmem + TM_D2, ptx::sdesc_sw128(base + S_QD + pn * 16384 + koff),
-                             ptx::sdesc_sw128(base + S_RHL + pn * 16384 + koff), IDESC_BF16_N128, kk > 0);
+                ptx::mma_f16(tmem + TM_D2, ptx::sdesc_sw128(base + S_QD + pn * 16384 + koff), bR, IDESC_BF16_N128, kk > 0);
             }
             ptx::mma_commit(bar_mma1);
             mma_pending = 1;
