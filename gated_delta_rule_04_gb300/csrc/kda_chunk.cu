@@ -62,14 +62,6 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 constexpr uint32_t IDESC_N64 = ptx::idesc_f16_f32(128, 64);
 constexpr uint32_t IDESC_N128 = ptx::idesc_f16_f32(128, 128);
 
-__device__ __forceinline__ uint4 pack8_f16(const float* v) {
-    uint4 u;
-    __half2* p = reinterpret_cast<__half2*>(&u);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) p[e] = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
-    return u;
-}
-
 __device__ __forceinline__ uint32_t pack2_f16(float a, float b) {
     const __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&h);
@@ -85,10 +77,6 @@ __device__ __forceinline__ float tanh_fast(float x) {
 __device__ __forceinline__ void bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");

@@ -47,13 +47,16 @@
 // warp reduce-scatters plus one shared-memory exchange, and the cumulative
 // gate is a per-thread running sum plus a prefix over octets.
 //
-// Schedule.  The grid is persistent (one CTA per SM); the raw rows of a CTA's
-// next item are bulk-copied into shared memory as soon as the current item
-// has read its own, so the load overlaps the rest of the item.
+// Schedule.  The grid is persistent (one CTA per SM, or fewer when the
+// launch shares the GPU).  A CTA walks its items in head-major order, either a
+// fixed contiguous range or batches taken from a work counter.  The next
+// item's raw rows (TMA tensor copies) and its head's conv taps and dt_bias
+// (bulk copies) arrive while the current item is being solved.
 //
 // Output: one record per (chunk, head) in the exact shared-memory image the
-// recurrence kernel consumes (fp16, K-major, 128-byte swizzle), written
-// straight from registers.
+// recurrence kernel consumes (fp16, K-major, 128-byte swizzle).  Q+ and the
+// decay are stored from registers; Kt, P, W and U0^T are assembled in shared
+// memory and leave as contiguous bulk stores.
 #include <type_traits>
 
 #include "kda_chunk_layout.cuh"
