@@ -16,19 +16,56 @@
 // over register-resident state), and keeping the input state untouched gives
 // its snapshot-and-replay rollback (kda_verify_rollback_rows).
 //
-// Memory: warp w owns key rows 16w..16w+15 of S, lane l value columns
-// 4l..4l+3, so every load and store instruction moves 512 contiguous bytes.
-// The state and ring are read from the input pools before anything is
-// written, so input and output may alias (in-place update).
+// Work split.  Everything that does not touch S (conv, SiLU, gate, beta, the
+// L2 norms) runs for a group of up to DG tokens at once, and the output norm
+// for the group runs after it, so a group costs three block barriers however
+// many tokens it holds.  Inside the group the recurrence needs none: warp w
+// owns value columns 16w..16w+15 of S, and lane (cg, rb) = (lane % 2,
+// lane / 2) holds key rows 8rb..8rb+7 of columns 16w + 4cg + (0..3) and
+// 16w + 8 + 4cg + (0..3).  The sums over key rows (u = S'^T k, S'^T q) close
+// inside the warp in a four-level butterfly that halves the columns a lane
+// carries at each level; d comes back the same way.  A lane reads 8 rows of
+// each per-token row vector, which keeps the shared-memory traffic of a token
+// at 32 floats per lane (the shared-memory pipe, not the arithmetic, set the
+// speed of wider row ranges).  Column pairs run as packed fp32 pairs.
+//
+// Memory: each load or store instruction of S moves 16 row pieces of 32 bytes.
+// The raw inputs of a group reach shared memory by cp.async, each piece
+// copied by the warp that reads it.  The state and ring are read from the
+// input pools before anything is written, so input and output may alias
+// (in-place update).
+#include <atomic>
+
 #include "kda_common.cuh"
+#include "tc_ptx.cuh"
 
 namespace kda {
 namespace {
 
 constexpr int DC_THREADS = 256;
+constexpr int DG = 8;    // tokens per group
 
-// ONE: a.n_tok == 1 (plain decode), compiled without the token loop
-template <typename TI, bool ONE>
+template <typename TI>
+struct DecodeSmem {
+    TI x[4][DG][D];   // raw q, k, v, z of the group
+    TI go[2][DG][D];  // raw output-gate logits, double-buffered across groups
+    float qc[DG][D], kc[DG][D];  // conv + SiLU of q and k, before the L2 norm
+    float va[DG][D];             // conv + SiLU of v
+    float so[DG][D];             // o before RMSNormGated
+    float e[DG][D];              // exp(g)
+    float kh[DG][D];             // k^
+    float av[DG][D];             // exp(g) k^  (u = S^T av = S'^T k^)
+    float bv[DG][D];             // exp(g) q^  (S^T bv = S'^T q^)
+    float beta[DG], qk[DG];      // beta, q^.k^
+};
+
+// ---- one token per session (plain decode) ----------------------------------
+// Warp w owns key rows 16w..16w+15 of S and lane l value columns 4l..4l+3, so
+// every load and store instruction of S moves 512 contiguous bytes and every
+// per-row value is one shared-memory broadcast; the sums over key rows meet
+// in shared memory.  With a single token the four block barriers this costs
+// are cheaper than the in-warp butterfly of the round kernel below.
+template <typename TI>
 __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
     const int H = a.H, W = H * D;
     const int n = blockIdx.x / H, h = blockIdx.x % H;
@@ -48,140 +85,392 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
     __shared__ float s_sum[8][4];
     __shared__ float s_scal[2];
 
-    // conv windows in registers: threads 0-127 own channel i of planes q and k,
-    // threads 128-255 channel i of plane v (and the gate); slot 0 is the oldest
+    // conv windows: threads 0-127 own channel i of planes q and k, threads
+    // 128-255 channel i of plane v (and the gate); slot 0 is the oldest
     const int i = tid & (D - 1);
     const int c = h * D + i;
     const int p0 = tid < D ? 0 : 2;            // first plane of this thread
+    const size_t tok = (size_t)n * W + c;
     const TI* ring_in = static_cast<const TI*>(a.ring_in) + (size_t)slot * 3 * RING * W;
-    float win[2][RING];
+    TI win[2][RING];
 #pragma unroll
     for (int pp = 0; pp < 2; ++pp) {
         if (pp == 1 && p0 == 2) break;
 #pragma unroll
-        for (int s = 0; s < RING; ++s) win[pp][s] = to_f32(ring_in[((size_t)(p0 + pp) * RING + s) * W + c]);
+        for (int s = 0; s < RING; ++s) win[pp][s] = ring_in[((size_t)(p0 + pp) * RING + s) * W + c];
     }
-    TI raw_last[2][RING];                      // raw values of the new ring (bit-exact copy)
+    const TI* plane0 = static_cast<const TI*>(p0 == 0 ? a.q : a.v);   // this thread's first plane
+    const TI* plane1 = static_cast<const TI*>(a.k);
+    auto conv_plane = [&](int pp) -> float {
+        const TI xr = (pp == 0 ? plane0 : plane1)[tok];
+        const float4 w = __ldg(reinterpret_cast<const float4*>(a.conv_w + ((size_t)(p0 + pp) * W + c) * CONV_K));
+        float y = w.x * to_f32(win[pp][0]);
+        y = fmaf(w.y, to_f32(win[pp][1]), y);
+        y = fmaf(w.z, to_f32(win[pp][2]), y);
+        y = fmaf(w.w, to_f32(xr), y);
+        win[pp][0] = win[pp][1];
+        win[pp][1] = win[pp][2];
+        win[pp][2] = xr;
+        return y / (1.0f + expf(-y));
+    };
+
+    // ---- conv + SiLU (threads 0-127: planes q, k; 128-255: v + gate)
+    float aq = 0.f, ak = 0.f;
+    if (tid < D) {
+        aq = conv_plane(0);
+        ak = conv_plane(1);
+        const float s0 = warp_sum(aq * aq), s1 = warp_sum(ak * ak), s2 = warp_sum(aq * ak);
+        if (lane == 0) { s_sum[warp][0] = s0; s_sum[warp][1] = s1; s_sum[warp][2] = s2; }
+    } else {
+        s_v[i] = conv_plane(0);
+        const float z = to_f32(static_cast<const TI*>(a.z)[tok]);
+        s_e[i] = expf(decay_gate(a.gate_kind, a.lb, expf(a.A_log[h]), z + a.dt_bias[c]));
+    }
+    __syncthreads();
+    if (tid < D) {
+        const float sq = s_sum[0][0] + s_sum[1][0] + s_sum[2][0] + s_sum[3][0];
+        const float sk = s_sum[0][1] + s_sum[1][1] + s_sum[2][1] + s_sum[3][1];
+        const float sqk = s_sum[0][2] + s_sum[1][2] + s_sum[2][2] + s_sum[3][2];
+        const float rq = rsqrtf(sq + a.l2_eps) * a.q_scale, rk = rsqrtf(sk + a.l2_eps);
+        const float qh = aq * rq, kh = ak * rk;
+        const float e = s_e[i];
+        s_k[i] = kh;
+        s_a[i] = e * kh;
+        s_b[i] = e * qh;
+        if (tid == 0) {
+            s_scal[0] = sqk * rq * rk;  // q^.k^
+            const float bl = to_f32(static_cast<const TI*>(a.b)[(size_t)n * H + h]);
+            s_scal[1] = 1.0f / (1.0f + expf(-bl));
+        }
+    }
+    __syncthreads();
+
+    // ---- u = S'^T k^ and w = S'^T q^ over this warp's 16 rows
+    float u[4] = {0.f, 0.f, 0.f, 0.f}, w[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        const float ar = s_a[16 * warp + r], br = s_b[16 * warp + r];
+        u[0] = fmaf(ar, Sr[r].x, u[0]); u[1] = fmaf(ar, Sr[r].y, u[1]);
+        u[2] = fmaf(ar, Sr[r].z, u[2]); u[3] = fmaf(ar, Sr[r].w, u[3]);
+        w[0] = fmaf(br, Sr[r].x, w[0]); w[1] = fmaf(br, Sr[r].y, w[1]);
+        w[2] = fmaf(br, Sr[r].z, w[2]); w[3] = fmaf(br, Sr[r].w, w[3]);
+    }
+    *reinterpret_cast<float4*>(&s_red[warp][0][4 * lane]) = make_float4(u[0], u[1], u[2], u[3]);
+    *reinterpret_cast<float4*>(&s_red[warp][1][4 * lane]) = make_float4(w[0], w[1], w[2], w[3]);
+    __syncthreads();
+
+    float oj = 0.f;
+    if (tid < D) {
+        float uj = 0.f, wj = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) { uj += s_red[k][0][tid]; wj += s_red[k][1][tid]; }
+        const float dj = s_scal[1] * (s_v[tid] - uj);
+        s_d[tid] = dj;
+        oj = fmaf(s_scal[0], dj, wj);
+        const float so = warp_sum(oj * oj);
+        if (lane == 0) s_sum[warp][3] = so;
+    }
+    __syncthreads();
+
+    // ---- S = Diag(e) S + k^ d^T, each row streamed out as soon as it is final
+    const float4 d4 = *reinterpret_cast<const float4*>(&s_d[4 * lane]);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        const int rr = 16 * warp + r;
+        const float er = s_e[rr], kr = s_k[rr];
+        Sr[r].x = fmaf(er, Sr[r].x, kr * d4.x);
+        Sr[r].y = fmaf(er, Sr[r].y, kr * d4.y);
+        Sr[r].z = fmaf(er, Sr[r].z, kr * d4.z);
+        Sr[r].w = fmaf(er, Sr[r].w, kr * d4.w);
+        __stcs(reinterpret_cast<float4*>(Sg_out + (size_t)rr * D) + lane, Sr[r]);
+    }
+
+    // ---- RMSNormGated
+    if (tid < D) {
+        const float ss = s_sum[0][3] + s_sum[1][3] + s_sum[2][3] + s_sum[3][3];
+        const float r = rsqrtf(ss * (1.0f / D) + a.norm_eps);
+        const float gt = to_f32(static_cast<const TI*>(a.gout)[tok]);
+        static_cast<TI*>(a.o)[tok] = from_f32<TI>(oj * r * a.norm_w[tid] / (1.0f + expf(-gt)));
+    }
+
+    // ---- ring out (after every read of the inputs)
+    TI* ring_out = static_cast<TI*>(a.ring_out) + (size_t)slot * 3 * RING * W;
 #pragma unroll
     for (int pp = 0; pp < 2; ++pp) {
         if (pp == 1 && p0 == 2) break;
 #pragma unroll
-        for (int s = 0; s < RING; ++s) raw_last[pp][s] = ring_in[((size_t)(p0 + pp) * RING + s) * W + c];
+        for (int s = 0; s < RING; ++s) ring_out[((size_t)(p0 + pp) * RING + s) * W + c] = win[pp][s];
+    }
+}
+
+// ---- a round of n_tok >= 2 tokens per session -------------------------------
+template <typename TI>
+__global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs a) {
+    extern __shared__ __align__(16) unsigned char dc_smem[];
+    DecodeSmem<TI>& sm = *reinterpret_cast<DecodeSmem<TI>*>(dc_smem);
+    const int H = a.H, W = H * D;
+    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int slot = a.slots ? a.slots[n] : n;
+    if (slot < 0 || slot >= a.n_slots) return;  // invalid pool index: the session is skipped
+    const int n_tok = a.n_tok;
+    const size_t row0 = (size_t)n * n_tok;      // token row of (session, token 0)
+
+    // ---- raw inputs of the group starting at token g0, into buffer `buf`.
+    // Warps 0-3 copy channels 32(w%4).. of q and k, warps 4-7 of v and z:
+    // exactly what each warp's threads read in the conv step.  Warp t copies
+    // the gate logits of token t, which it reads in the output step; warp 7
+    // lane t prefetches the beta logit of token t into a register.
+    TI b_next = TI(0.f);
+    auto stage = [&](int g0, int buf) {
+        const TI* pl0 = static_cast<const TI*>(warp < 4 ? a.q : a.v);
+        const TI* pl1 = static_cast<const TI*>(warp < 4 ? a.k : a.z);
+        const int pbase = warp < 4 ? 0 : 2, cbase = 32 * (warp & 3);
+        const int ng = min(DG, n_tok - g0);
+        constexpr int EPC = 16 / sizeof(TI);    // elements per 16-byte chunk
+        constexpr int CPR = 32 / EPC;           // chunks per 32 channels
+        for (int c = lane; c < 2 * ng * CPR; c += 32) {
+            const int part = c % CPR, t = (c / CPR) % ng, pp = c / (CPR * ng);
+            const size_t off = (row0 + g0 + t) * W + (size_t)h * D + cbase + part * EPC;
+            ptx::cp_async16(&sm.x[pbase + pp][t][cbase + part * EPC], (pp == 0 ? pl0 : pl1) + off);
+        }
+        if (warp < ng) {
+            const TI* gsrc = static_cast<const TI*>(a.gout) + (row0 + g0 + warp) * W + (size_t)h * D;
+            for (int c = lane; c < D / EPC; c += 32) ptx::cp_async16(&sm.go[buf][warp][c * EPC], gsrc + c * EPC);
+        }
+        ptx::cp_async_commit();
+        if (warp == 7 && lane < ng) b_next = static_cast<const TI*>(a.b)[(row0 + g0 + lane) * H + h];
+    };
+    stage(0, 0);
+
+    // ---- the state block of this lane: rows 8rb + r; Sp[r][p] holds local
+    // columns 2p, 2p + 1, where local column m is 16w + 8(m / 4) + 4cg + m % 4
+    const int cg = lane & 1, rb = lane >> 1;
+    const int H1 = (lane >> 4) & 1, H2 = (lane >> 3) & 1, H3 = (lane >> 2) & 1;  // butterfly levels
+    const int ca = 16 * warp + 4 * cg;
+    const float* Sg_in = a.S_in + ((size_t)slot * H + h) * D * D;
+    float* Sg_out = a.S_out + ((size_t)slot * H + h) * D * D;
+    float2 Sp[8][4];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const float* src = Sg_in + (size_t)(8 * rb + r) * D + ca;
+        const float4 lo = __ldcs(reinterpret_cast<const float4*>(src));
+        const float4 hi = __ldcs(reinterpret_cast<const float4*>(src + 8));
+        Sp[r][0] = make_float2(lo.x, lo.y);
+        Sp[r][1] = make_float2(lo.z, lo.w);
+        Sp[r][2] = make_float2(hi.x, hi.y);
+        Sp[r][3] = make_float2(hi.z, hi.w);
+    }
+
+    // ---- conv windows in registers: threads 0-127 own channel i of planes q
+    // and k, threads 128-255 channel i of plane v (and the gate); slot 0 is
+    // the oldest
+    const int i = tid & (D - 1);
+    const int c = h * D + i;
+    const int p0 = tid < D ? 0 : 2;  // first ring plane of this thread
+    const TI* ring_in = static_cast<const TI*>(a.ring_in) + (size_t)slot * 3 * RING * W;
+    TI win[2][RING];                 // raw values; they become the new ring (bit-exact copy)
+#pragma unroll
+    for (int pp = 0; pp < 2; ++pp) {
+        if (pp == 1 && p0 == 2) break;
+#pragma unroll
+        for (int s = 0; s < RING; ++s) win[pp][s] = ring_in[((size_t)(p0 + pp) * RING + s) * W + c];
     }
     float4 wconv[2];
     wconv[0] = __ldg(reinterpret_cast<const float4*>(a.conv_w + ((size_t)p0 * W + c) * CONV_K));
     wconv[1] = p0 == 0 ? __ldg(reinterpret_cast<const float4*>(a.conv_w + ((size_t)1 * W + c) * CONV_K))
                        : make_float4(0.f, 0.f, 0.f, 0.f);
-    const TI* plane0 = static_cast<const TI*>(p0 == 0 ? a.q : a.v);   // this thread's first plane
-    const TI* plane1 = static_cast<const TI*>(a.k);
     const float eA = expf(a.A_log[h]);
     const float dtb = a.dt_bias[c];
+    auto conv_plane = [&](int pp, TI xr) -> float {
+        const float xv = to_f32(xr);
+        const float4 w = wconv[pp];
+        float y = w.x * to_f32(win[pp][0]);
+        y = fmaf(w.y, to_f32(win[pp][1]), y);
+        y = fmaf(w.z, to_f32(win[pp][2]), y);
+        y = fmaf(w.w, xv, y);
+        win[pp][0] = win[pp][1];
+        win[pp][1] = win[pp][2];
+        win[pp][2] = xr;
+        return y / (1.0f + expf(-y));
+    };
 
-    const int n_tok = ONE ? 1 : a.n_tok;
 #pragma unroll 1
-    for (int t = 0; t < n_tok; ++t) {
-        const size_t row = (size_t)n * n_tok + t;     // token row of (session, t)
-        const size_t tok = row * W + c;
-        auto conv_plane = [&](int pp) -> float {
-            const TI xr = (pp == 0 ? plane0 : plane1)[tok];
-            const float xv = to_f32(xr);
-            const float4 w = wconv[pp];
-            float y = w.x * win[pp][0];
-            y = fmaf(w.y, win[pp][1], y);
-            y = fmaf(w.z, win[pp][2], y);
-            y = fmaf(w.w, xv, y);
-            win[pp][0] = win[pp][1];
-            win[pp][1] = win[pp][2];
-            win[pp][2] = xv;
-            raw_last[pp][0] = raw_last[pp][1];
-            raw_last[pp][1] = raw_last[pp][2];
-            raw_last[pp][2] = xr;
-            return y / (1.0f + expf(-y));
-        };
+    for (int g0 = 0, gi = 0; g0 < n_tok; g0 += DG, ++gi) {
+        const int ng = min(DG, n_tok - g0);
+        const TI bl = b_next;
+        ptx::cp_async_wait_all();
+        __syncwarp();
 
-        // ---- prologue: conv + SiLU (threads 0-127: planes q, k; 128-255: v + gate)
-        float aq = 0.f, ak = 0.f;
-        if (tid < D) {
-            aq = conv_plane(0);
-            ak = conv_plane(1);
-            const float s0 = warp_sum(aq * aq), s1 = warp_sum(ak * ak), s2 = warp_sum(aq * ak);
-            if (lane == 0) { s_sum[warp][0] = s0; s_sum[warp][1] = s1; s_sum[warp][2] = s2; }
-        } else {
-            s_v[i] = conv_plane(0);
-            const float z = to_f32(static_cast<const TI*>(a.z)[tok]);
-            const float g = decay_gate(a.gate_kind, a.lb, eA, z + dtb);
-            s_e[i] = expf(g);
+        // ---- conv + SiLU, gate, beta of the group's tokens
+#pragma unroll 1
+        for (int t = 0; t < ng; ++t) {
+            if (tid < D) {
+                sm.qc[t][i] = conv_plane(0, sm.x[0][t][i]);
+                sm.kc[t][i] = conv_plane(1, sm.x[1][t][i]);
+            } else {
+                sm.va[t][i] = conv_plane(0, sm.x[2][t][i]);
+                const float z = to_f32(sm.x[3][t][i]);
+                sm.e[t][i] = expf(decay_gate(a.gate_kind, a.lb, eA, z + dtb));
+            }
+        }
+        if (warp == 7 && lane < ng) sm.beta[lane] = 1.0f / (1.0f + expf(-to_f32(bl)));
+        __syncthreads();
+        if (g0 + DG < n_tok) stage(g0 + DG, (gi + 1) & 1);  // the staged inputs are consumed
+
+        // ---- L2 norms: warp t normalises token t, lane l channels 4l..4l+3
+        if (warp < ng) {
+            const int t = warp, ro = 4 * lane;
+            const float4 q4 = *reinterpret_cast<const float4*>(&sm.qc[t][4 * lane]);
+            const float4 k4 = *reinterpret_cast<const float4*>(&sm.kc[t][4 * lane]);
+            const float4 e4 = *reinterpret_cast<const float4*>(&sm.e[t][ro]);
+            float sq = q4.x * q4.x, sk = k4.x * k4.x, sqk = q4.x * k4.x;
+            sq = fmaf(q4.y, q4.y, sq); sk = fmaf(k4.y, k4.y, sk); sqk = fmaf(q4.y, k4.y, sqk);
+            sq = fmaf(q4.z, q4.z, sq); sk = fmaf(k4.z, k4.z, sk); sqk = fmaf(q4.z, k4.z, sqk);
+            sq = fmaf(q4.w, q4.w, sq); sk = fmaf(k4.w, k4.w, sk); sqk = fmaf(q4.w, k4.w, sqk);
+            sq = warp_sum(sq);
+            sk = warp_sum(sk);
+            sqk = warp_sum(sqk);
+            const float rq = rsqrtf(sq + a.l2_eps) * a.q_scale, rk = rsqrtf(sk + a.l2_eps);
+            const float4 kh = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
+            const float4 qh = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
+            *reinterpret_cast<float4*>(&sm.kh[t][ro]) = kh;
+            *reinterpret_cast<float4*>(&sm.av[t][ro]) =
+                make_float4(e4.x * kh.x, e4.y * kh.y, e4.z * kh.z, e4.w * kh.w);
+            *reinterpret_cast<float4*>(&sm.bv[t][ro]) =
+                make_float4(e4.x * qh.x, e4.y * qh.y, e4.z * qh.z, e4.w * qh.w);
+            if (lane == 0) sm.qk[t] = sqk * rq * rk;
         }
         __syncthreads();
-        if (tid < D) {
-            const float sq = s_sum[0][0] + s_sum[1][0] + s_sum[2][0] + s_sum[3][0];
-            const float sk = s_sum[0][1] + s_sum[1][1] + s_sum[2][1] + s_sum[3][1];
-            const float sqk = s_sum[0][2] + s_sum[1][2] + s_sum[2][2] + s_sum[3][2];
-            const float rq = rsqrtf(sq + a.l2_eps) * a.q_scale, rk = rsqrtf(sk + a.l2_eps);
-            const float qh = aq * rq, kh = ak * rk;
-            const float e = s_e[i];
-            s_k[i] = kh;
-            s_a[i] = e * kh;
-            s_b[i] = e * qh;
-            if (tid == 0) {
-                s_scal[0] = sqk * rq * rk;  // q^.k^
-                const float bl = to_f32(static_cast<const TI*>(a.b)[row * H + h]);
-                s_scal[1] = 1.0f / (1.0f + expf(-bl));
+
+        // ---- the recurrence over the group, no block barrier
+#pragma unroll 1
+        for (int t = 0; t < ng; ++t) {
+            // partial S^T av and S^T bv over this lane's 8 rows, per local column pair
+            const float* A = &sm.av[t][8 * rb];
+            const float* B = &sm.bv[t][8 * rb];
+            float2 u[4], w[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) u[p] = w[p] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int r4 = 0; r4 < 2; ++r4) {
+                const float4 a4 = *reinterpret_cast<const float4*>(A + 4 * r4);
+                const float4 b4 = *reinterpret_cast<const float4*>(B + 4 * r4);
+                const float ar[4] = {a4.x, a4.y, a4.z, a4.w}, br[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const float2 aa = make_float2(ar[m], ar[m]), bb = make_float2(br[m], br[m]);
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        u[p] = ptx::fma2(aa, Sp[4 * r4 + m][p], u[p]);
+                        w[p] = ptx::fma2(bb, Sp[4 * r4 + m][p], w[p]);
+                    }
+                }
+            }
+            // butterfly over the 16 row blocks: at each level a lane keeps
+            // half of its columns and adds its partner's partial sums of them.
+            // It ends with local column m = 4H1 + 2H2 + H3 (in two lanes, equal
+            // to the last bit: the last addition only swaps operands).
+            float uj, wj;
+            {
+                float2 ku0 = H1 ? u[2] : u[0], ku1 = H1 ? u[3] : u[1];
+                float2 kw0 = H1 ? w[2] : w[0], kw1 = H1 ? w[3] : w[1];
+                const float2 su0 = H1 ? u[0] : u[2], su1 = H1 ? u[1] : u[3];
+                const float2 sw0 = H1 ? w[0] : w[2], sw1 = H1 ? w[1] : w[3];
+                ku0.x += __shfl_xor_sync(0xffffffffu, su0.x, 16);
+                ku0.y += __shfl_xor_sync(0xffffffffu, su0.y, 16);
+                ku1.x += __shfl_xor_sync(0xffffffffu, su1.x, 16);
+                ku1.y += __shfl_xor_sync(0xffffffffu, su1.y, 16);
+                kw0.x += __shfl_xor_sync(0xffffffffu, sw0.x, 16);
+                kw0.y += __shfl_xor_sync(0xffffffffu, sw0.y, 16);
+                kw1.x += __shfl_xor_sync(0xffffffffu, sw1.x, 16);
+                kw1.y += __shfl_xor_sync(0xffffffffu, sw1.y, 16);
+                float2 pu = H2 ? ku1 : ku0, pw = H2 ? kw1 : kw0;
+                const float2 qu = H2 ? ku0 : ku1, qw = H2 ? kw0 : kw1;
+                pu.x += __shfl_xor_sync(0xffffffffu, qu.x, 8);
+                pu.y += __shfl_xor_sync(0xffffffffu, qu.y, 8);
+                pw.x += __shfl_xor_sync(0xffffffffu, qw.x, 8);
+                pw.y += __shfl_xor_sync(0xffffffffu, qw.y, 8);
+                uj = H3 ? pu.y : pu.x;
+                wj = H3 ? pw.y : pw.x;
+                uj += __shfl_xor_sync(0xffffffffu, H3 ? pu.x : pu.y, 4);
+                wj += __shfl_xor_sync(0xffffffffu, H3 ? pw.x : pw.y, 4);
+                uj += __shfl_xor_sync(0xffffffffu, uj, 2);
+                wj += __shfl_xor_sync(0xffffffffu, wj, 2);
+            }
+            const int j = 16 * warp + 8 * H1 + 4 * cg + 2 * H2 + H3;
+            const float dj = sm.beta[t] * (sm.va[t][j] - uj);
+            const float oj = fmaf(sm.qk[t], dj, wj);
+            if (!(rb & 1)) sm.so[t][j] = oj;
+            // d of all eight local columns back to every lane, the butterfly reversed
+            float2 d[4];
+            {
+                const float dx = __shfl_xor_sync(0xffffffffu, dj, 4);
+                const float2 dp = H3 ? make_float2(dx, dj) : make_float2(dj, dx);
+                const float2 dq = make_float2(__shfl_xor_sync(0xffffffffu, dp.x, 8),
+                                              __shfl_xor_sync(0xffffffffu, dp.y, 8));
+                const float2 lo = H2 ? dq : dp, hi = H2 ? dp : dq;  // local columns 4H1 + 0..3
+                const float2 elo = make_float2(__shfl_xor_sync(0xffffffffu, lo.x, 16),
+                                               __shfl_xor_sync(0xffffffffu, lo.y, 16));
+                const float2 ehi = make_float2(__shfl_xor_sync(0xffffffffu, hi.x, 16),
+                                               __shfl_xor_sync(0xffffffffu, hi.y, 16));
+                d[0] = H1 ? elo : lo;
+                d[1] = H1 ? ehi : hi;
+                d[2] = H1 ? lo : elo;
+                d[3] = H1 ? hi : ehi;
+            }
+
+            // S = Diag(e) S + k^ d^T; after the last token each row piece
+            // streams out as soon as it is final (every read of S_in is behind us)
+            const float* E = &sm.e[t][8 * rb];
+            const float* K = &sm.kh[t][8 * rb];
+            const bool last = g0 + t + 1 == n_tok;
+#pragma unroll
+            for (int r4 = 0; r4 < 2; ++r4) {
+                const float4 e4 = *reinterpret_cast<const float4*>(E + 4 * r4);
+                const float4 k4 = *reinterpret_cast<const float4*>(K + 4 * r4);
+                const float er[4] = {e4.x, e4.y, e4.z, e4.w}, kr[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int r = 4 * r4 + m;
+                    const float2 ee = make_float2(er[m], er[m]), kk = make_float2(kr[m], kr[m]);
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) Sp[r][p] = ptx::fma2(ee, Sp[r][p], ptx::mul2(kk, d[p]));
+                    if (last) {
+                        float* dst = Sg_out + (size_t)(8 * rb + r) * D + ca;
+                        __stcs(reinterpret_cast<float4*>(dst),
+                               make_float4(Sp[r][0].x, Sp[r][0].y, Sp[r][1].x, Sp[r][1].y));
+                        __stcs(reinterpret_cast<float4*>(dst + 8),
+                               make_float4(Sp[r][2].x, Sp[r][2].y, Sp[r][3].x, Sp[r][3].y));
+                    }
+                }
             }
         }
         __syncthreads();
 
-        // ---- u = S'^T k^ and w = S'^T q^ over this warp's 16 rows
-        float u[4] = {0.f, 0.f, 0.f, 0.f}, w[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const float ar = s_a[16 * warp + r], br = s_b[16 * warp + r];
-            u[0] = fmaf(ar, Sr[r].x, u[0]); u[1] = fmaf(ar, Sr[r].y, u[1]);
-            u[2] = fmaf(ar, Sr[r].z, u[2]); u[3] = fmaf(ar, Sr[r].w, u[3]);
-            w[0] = fmaf(br, Sr[r].x, w[0]); w[1] = fmaf(br, Sr[r].y, w[1]);
-            w[2] = fmaf(br, Sr[r].z, w[2]); w[3] = fmaf(br, Sr[r].w, w[3]);
-        }
-        *reinterpret_cast<float4*>(&s_red[warp][0][4 * lane]) = make_float4(u[0], u[1], u[2], u[3]);
-        *reinterpret_cast<float4*>(&s_red[warp][1][4 * lane]) = make_float4(w[0], w[1], w[2], w[3]);
-        __syncthreads();
-
-        float oj = 0.f;
-        if (tid < D) {
-            float uj = 0.f, wj = 0.f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) { uj += s_red[k][0][tid]; wj += s_red[k][1][tid]; }
-            const float dj = s_scal[1] * (s_v[tid] - uj);
-            s_d[tid] = dj;
-            oj = fmaf(s_scal[0], dj, wj);
-            const float so = warp_sum(oj * oj);
-            if (lane == 0) s_sum[warp][3] = so;
-        }
-        __syncthreads();
-
-        // ---- S = Diag(e) S + k^ d^T (registers); after the last token each row
-        // streams out as soon as it is final (every read of S_in is behind us)
-        const float4 d4 = *reinterpret_cast<const float4*>(&s_d[4 * lane]);
-        const bool last = t + 1 == n_tok;
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int rr = 16 * warp + r;
-            const float er = s_e[rr], kr = s_k[rr];
-            Sr[r].x = fmaf(er, Sr[r].x, kr * d4.x);
-            Sr[r].y = fmaf(er, Sr[r].y, kr * d4.y);
-            Sr[r].z = fmaf(er, Sr[r].z, kr * d4.z);
-            Sr[r].w = fmaf(er, Sr[r].w, kr * d4.w);
-            if (last) __stcs(reinterpret_cast<float4*>(Sg_out + (size_t)rr * D) + lane, Sr[r]);
-        }
-
-        // ---- RMSNormGated epilogue
-        if (tid < D) {
-            const float ss = s_sum[0][3] + s_sum[1][3] + s_sum[2][3] + s_sum[3][3];
+        // ---- RMSNormGated: warp t finishes token t, lane l channels 4l..4l+3
+        if (warp < ng) {
+            const int t = warp;
+            const float4 o4 = *reinterpret_cast<const float4*>(&sm.so[t][4 * lane]);
+            float ss = o4.x * o4.x;
+            ss = fmaf(o4.y, o4.y, ss);
+            ss = fmaf(o4.z, o4.z, ss);
+            ss = fmaf(o4.w, o4.w, ss);
+            ss = warp_sum(ss);
             const float r = rsqrtf(ss * (1.0f / D) + a.norm_eps);
-            const float gt = to_f32(static_cast<const TI*>(a.gout)[tok]);
-            const float y = oj * r * a.norm_w[tid] / (1.0f + expf(-gt));
-            static_cast<TI*>(a.o)[tok] = from_f32<TI>(y);
+            const float4 nw = __ldg(reinterpret_cast<const float4*>(a.norm_w) + lane);
+            const TI* gg = &sm.go[gi & 1][t][4 * lane];
+            const float ov[4] = {o4.x, o4.y, o4.z, o4.w}, nv[4] = {nw.x, nw.y, nw.z, nw.w};
+            TI y[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) y[m] = from_f32<TI>(ov[m] * r * nv[m] / (1.0f + expf(-to_f32(gg[m]))));
+            TI* dst = static_cast<TI*>(a.o) + (row0 + g0 + t) * W + (size_t)h * D + 4 * lane;
+            if constexpr (sizeof(TI) == 4) {
+                *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(y);
+            } else {
+                *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(y);
+            }
         }
-        if (!last) __syncthreads();  // the shared vectors are rewritten by the next token
     }
 
     // ---- ring out (written once, after every read of the inputs)
@@ -190,8 +479,28 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
     for (int pp = 0; pp < 2; ++pp) {
         if (pp == 1 && p0 == 2) break;
 #pragma unroll
-        for (int s = 0; s < RING; ++s) ring_out[((size_t)(p0 + pp) * RING + s) * W + c] = raw_last[pp][s];
+        for (int s = 0; s < RING; ++s) ring_out[((size_t)(p0 + pp) * RING + s) * W + c] = win[pp][s];
     }
+}
+
+template <typename TI>
+cudaError_t launch_round(const DecodeArgs& a, int64_t blocks, cudaStream_t s) {
+    constexpr size_t smem = sizeof(DecodeSmem<TI>);
+    // above the 48 KiB default the kernel needs the opt-in, once per device
+    static std::atomic<uint64_t> opted{0};
+    if (smem > 48 * 1024) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        const uint64_t bit = dev < 64 ? uint64_t(1) << dev : 0;
+        if (!bit || !(opted.load() & bit)) {
+            e = cudaFuncSetAttribute(decode_round_kernel<TI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            opted.fetch_or(bit);
+        }
+    }
+    decode_round_kernel<TI><<<(unsigned)blocks, DC_THREADS, smem, s>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -199,15 +508,12 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
 cudaError_t launch_decode(const DecodeArgs& a, int io_bf16, cudaStream_t s) {
     const int64_t blocks = (int64_t)a.n * a.H;
     if (blocks == 0 || a.n_tok == 0) return cudaSuccess;
-    const bool one = a.n_tok == 1;
-    if (io_bf16) {
-        if (one) decode_kernel<__nv_bfloat16, true><<<(unsigned)blocks, DC_THREADS, 0, s>>>(a);
-        else decode_kernel<__nv_bfloat16, false><<<(unsigned)blocks, DC_THREADS, 0, s>>>(a);
-    } else {
-        if (one) decode_kernel<float, true><<<(unsigned)blocks, DC_THREADS, 0, s>>>(a);
-        else decode_kernel<float, false><<<(unsigned)blocks, DC_THREADS, 0, s>>>(a);
+    if (a.n_tok == 1) {
+        if (io_bf16) decode_kernel<__nv_bfloat16><<<(unsigned)blocks, DC_THREADS, 0, s>>>(a);
+        else decode_kernel<float><<<(unsigned)blocks, DC_THREADS, 0, s>>>(a);
+        return cudaGetLastError();
     }
-    return cudaGetLastError();
+    return io_bf16 ? launch_round<__nv_bfloat16>(a, blocks, s) : launch_round<float>(a, blocks, s);
 }
 
 }  // namespace kda
