@@ -34,6 +34,7 @@
 // copied by the warp that reads it.  The state and ring are read from the
 // input pools before anything is written, so input and output may alias
 // (in-place update).
+#include <algorithm>
 #include <atomic>
 
 #include "kda_common.cuh"
@@ -59,6 +60,32 @@ struct DecodeSmem {
     float beta[DG], qk[DG];      // beta, q^.k^
 };
 
+// Persistent CTAs walk the (session, head) items with a stride of the grid.
+// While one item computes, its successor's state (64 KiB), token rows and
+// conv ring are fetched into L2, so the HBM traffic of the next item overlaps
+// this item's arithmetic.  Threads 0..(5 + 3 * RING) each issue one prefetch.
+template <typename TI>
+__device__ __forceinline__ void prefetch_item(const DecodeArgs& a, int item, int n_tok, int tid) {
+    const int H = a.H, W = H * D;
+    const int n = item / H, h = item % H;
+    if (tid > 5 + 3 * RING) return;
+    const int slot = a.slots ? a.slots[n] : n;
+    if (slot < 0 || slot >= a.n_slots) return;
+    const size_t rowb = (size_t)D * sizeof(TI);
+    if (tid == 0) {
+        ptx::bulk_prefetch_l2(a.S_in + ((size_t)slot * H + h) * D * D, D * D * sizeof(float));
+    } else if (tid <= 5) {
+        const void* pl = tid == 1 ? a.q : tid == 2 ? a.k : tid == 3 ? a.v : tid == 4 ? a.z : a.gout;
+        const char* base = static_cast<const char*>(pl) + ((size_t)n * n_tok * W + (size_t)h * D) * sizeof(TI);
+        for (int t = 0; t < n_tok; ++t) ptx::bulk_prefetch_l2(base + (size_t)t * W * sizeof(TI), (uint32_t)rowb);
+    } else {
+        const int r = tid - 6;  // ring row (plane r / RING, slot r % RING)
+        ptx::bulk_prefetch_l2(static_cast<const char*>(a.ring_in) +
+                                  (((size_t)slot * 3 * RING + r) * W + (size_t)h * D) * sizeof(TI),
+                              (uint32_t)rowb);
+    }
+}
+
 // ---- one token per session (plain decode) ----------------------------------
 // Warp w owns key rows 16w..16w+15 of S and lane l value columns 4l..4l+3, so
 // every load and store instruction of S moves 512 contiguous bytes and every
@@ -68,10 +95,18 @@ struct DecodeSmem {
 template <typename TI>
 __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
     const int H = a.H, W = H * D;
-    const int n = blockIdx.x / H, h = blockIdx.x % H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n_items = a.n * H;
+    __shared__ float s_e[D], s_k[D], s_a[D], s_b[D], s_v[D], s_d[D];
+    __shared__ float s_red[8][2][D];
+    __shared__ float s_sum[8][4];
+    __shared__ float s_scal[2];
+#pragma unroll 1
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    if (item + (int)gridDim.x < n_items) prefetch_item<TI>(a, item + gridDim.x, 1, tid);
+    const int n = item / H, h = item % H;
     const int slot = a.slots ? a.slots[n] : n;
-    if (slot < 0 || slot >= a.n_slots) return;  // invalid pool index: the session is skipped
+    if (slot < 0 || slot >= a.n_slots) continue;  // invalid pool index: the session is skipped
 
     const float* Sg_in = a.S_in + ((size_t)slot * H + h) * D * D;
     float* Sg_out = a.S_out + ((size_t)slot * H + h) * D * D;
@@ -79,11 +114,6 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
 #pragma unroll
     for (int r = 0; r < 16; ++r)
         Sr[r] = __ldcs(reinterpret_cast<const float4*>(Sg_in + (size_t)(16 * warp + r) * D) + lane);
-
-    __shared__ float s_e[D], s_k[D], s_a[D], s_b[D], s_v[D], s_d[D];
-    __shared__ float s_red[8][2][D];
-    __shared__ float s_sum[8][4];
-    __shared__ float s_scal[2];
 
     // conv windows: threads 0-127 own channel i of planes q and k, threads
     // 128-255 channel i of plane v (and the gate); slot 0 is the oldest
@@ -201,6 +231,8 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
 #pragma unroll
         for (int s = 0; s < RING; ++s) ring_out[((size_t)(p0 + pp) * RING + s) * W + c] = win[pp][s];
     }
+    __syncthreads();  // the shared vectors are rewritten by the next item
+    }
 }
 
 // ---- a round of n_tok >= 2 tokens per session -------------------------------
@@ -209,11 +241,15 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
     extern __shared__ __align__(16) unsigned char dc_smem[];
     DecodeSmem<TI>& sm = *reinterpret_cast<DecodeSmem<TI>*>(dc_smem);
     const int H = a.H, W = H * D;
-    const int n = blockIdx.x / H, h = blockIdx.x % H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int slot = a.slots ? a.slots[n] : n;
-    if (slot < 0 || slot >= a.n_slots) return;  // invalid pool index: the session is skipped
+    const int n_items = a.n * H;
     const int n_tok = a.n_tok;
+#pragma unroll 1
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    if (item + (int)gridDim.x < n_items) prefetch_item<TI>(a, item + gridDim.x, n_tok, tid);
+    const int n = item / H, h = item % H;
+    const int slot = a.slots ? a.slots[n] : n;
+    if (slot < 0 || slot >= a.n_slots) continue;  // invalid pool index: the session is skipped
     const size_t row0 = (size_t)n * n_tok;      // token row of (session, token 0)
 
     // ---- raw inputs of the group starting at token g0, into buffer `buf`.
@@ -481,6 +517,22 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
 #pragma unroll
         for (int s = 0; s < RING; ++s) ring_out[((size_t)(p0 + pp) * RING + s) * W + c] = win[pp][s];
     }
+    __syncthreads();  // the staging buffers are rewritten by the next item
+    }
+}
+
+// Resident CTAs of a decode kernel: two per SM (the register budget of
+// __launch_bounds__), looked up once per device.
+int decode_grid(int64_t items) {
+    static std::atomic<int> sms_cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return (int)std::min<int64_t>(items, 2 * 152);
+    int sms = dev < 64 ? sms_cache[dev].load() : 0;
+    if (sms == 0) {
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
+        if (dev < 64) sms_cache[dev].store(sms);
+    }
+    return (int)std::min<int64_t>(items, 2 * (int64_t)sms);
 }
 
 template <typename TI>
@@ -499,7 +551,7 @@ cudaError_t launch_round(const DecodeArgs& a, int64_t blocks, cudaStream_t s) {
             opted.fetch_or(bit);
         }
     }
-    decode_round_kernel<TI><<<(unsigned)blocks, DC_THREADS, smem, s>>>(a);
+    decode_round_kernel<TI><<<decode_grid(blocks), DC_THREADS, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -509,8 +561,9 @@ cudaError_t launch_decode(const DecodeArgs& a, int io_bf16, cudaStream_t s) {
     const int64_t blocks = (int64_t)a.n * a.H;
     if (blocks == 0 || a.n_tok == 0) return cudaSuccess;
     if (a.n_tok == 1) {
-        if (io_bf16) decode_kernel<__nv_bfloat16><<<(unsigned)blocks, DC_THREADS, 0, s>>>(a);
-        else decode_kernel<float><<<(unsigned)blocks, DC_THREADS, 0, s>>>(a);
+        const int grid = decode_grid(blocks);
+        if (io_bf16) decode_kernel<__nv_bfloat16><<<grid, DC_THREADS, 0, s>>>(a);
+        else decode_kernel<float><<<grid, DC_THREADS, 0, s>>>(a);
         return cudaGetLastError();
     }
     return io_bf16 ? launch_round<__nv_bfloat16>(a, blocks, s) : launch_round<float>(a, blocks, s);
