@@ -398,8 +398,8 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
                     const float2 aa = make_float2(ar[m], ar[m]), bb = make_float2(br[m], br[m]);
 #pragma unroll
                     for (int p = 0; p < 4; ++p) {
-                        u[p] = ptx::fma2(aa, Sp[4 * r4 + m][p], u[p]);
-                        w[p] = ptx::fma2(bb, Sp[4 * r4 + m][p], w[p]);
+                        u[p] = __ffma2_rn(aa, Sp[4 * r4 + m][p], u[p]);
+                        w[p] = __ffma2_rn(bb, Sp[4 * r4 + m][p], w[p]);
                     }
                 }
             }
@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
                     const int r = 4 * r4 + m;
                     const float2 ee = make_float2(er[m], er[m]), kk = make_float2(kr[m], kr[m]);
 #pragma unroll
-                    for (int p = 0; p < 4; ++p) Sp[r][p] = ptx::fma2(ee, Sp[r][p], ptx::mul2(kk, d[p]));
+                    for (int p = 0; p < 4; ++p) Sp[r][p] = __ffma2_rn(ee, Sp[r][p], __fmul2_rn(kk, d[p]));
                     if (last) {
                         float* dst = Sg_out + (size_t)(8 * rb + r) * D + ca;
                         __stcs(reinterpret_cast<float4*>(dst),
@@ -551,7 +551,11 @@ cudaError_t launch_round(const DecodeArgs& a, int64_t blocks, cudaStream_t s) {
             opted.fetch_or(bit);
         }
     }
-    decode_round_kernel<TI><<<decode_grid(blocks), DC_THREADS, smem, s>>>(a);
+    // Short rounds walk the items persistently, prefetching the next one; from
+    // 8 tokens on, the arithmetic of an item covers the latency of the next
+    // load anyway and one CTA per item measured faster.
+    const int grid = a.n_tok <= 4 ? decode_grid(blocks) : (int)blocks;
+    decode_round_kernel<TI><<<grid, DC_THREADS, smem, s>>>(a);
     return cudaGetLastError();
 }
 
