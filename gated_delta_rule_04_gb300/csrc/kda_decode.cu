@@ -36,6 +36,7 @@
 // (in-place update).
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 
 #include "kda_common.cuh"
 #include "tc_ptx.cuh"
@@ -305,12 +306,14 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
     const int c = h * D + i;
     const int p0 = tid < D ? 0 : 2;  // first ring plane of this thread
     const TI* ring_in = static_cast<const TI*>(a.ring_in) + (size_t)slot * 3 * RING * W;
-    TI win[2][RING];                 // raw values; they become the new ring (bit-exact copy)
+    // raw values; they become the new ring (bit-exact copy).  Plane 1 of
+    // threads 128-255 is the gate logit z, which has no ring: it stays zero.
+    TI win[2][RING];
 #pragma unroll
     for (int pp = 0; pp < 2; ++pp) {
-        if (pp == 1 && p0 == 2) break;
 #pragma unroll
-        for (int s = 0; s < RING; ++s) win[pp][s] = ring_in[((size_t)(p0 + pp) * RING + s) * W + c];
+        for (int s = 0; s < RING; ++s)
+            win[pp][s] = (pp == 1 && p0 == 2) ? TI(0.f) : ring_in[((size_t)(p0 + pp) * RING + s) * W + c];
     }
     float4 wconv[2];
     wconv[0] = __ldg(reinterpret_cast<const float4*>(a.conv_w + ((size_t)p0 * W + c) * CONV_K));
@@ -318,18 +321,6 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
                        : make_float4(0.f, 0.f, 0.f, 0.f);
     const float eA = expf(a.A_log[h]);
     const float dtb = a.dt_bias[c];
-    auto conv_plane = [&](int pp, TI xr) -> float {
-        const float xv = to_f32(xr);
-        const float4 w = wconv[pp];
-        float y = w.x * to_f32(win[pp][0]);
-        y = fmaf(w.y, to_f32(win[pp][1]), y);
-        y = fmaf(w.z, to_f32(win[pp][2]), y);
-        y = fmaf(w.w, xv, y);
-        win[pp][0] = win[pp][1];
-        win[pp][1] = win[pp][2];
-        win[pp][2] = xr;
-        return y / (1.0f + expf(-y));
-    };
 
 #pragma unroll 1
     for (int g0 = 0, gi = 0; g0 < n_tok; g0 += DG, ++gi) {
@@ -338,18 +329,61 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
         ptx::cp_async_wait_all();
         __syncwarp();
 
-        // ---- conv + SiLU, gate, beta of the group's tokens
-#pragma unroll 1
-        for (int t = 0; t < ng; ++t) {
-            if (tid < D) {
-                sm.qc[t][i] = conv_plane(0, sm.x[0][t][i]);
-                sm.kc[t][i] = conv_plane(1, sm.x[1][t][i]);
-            } else {
-                sm.va[t][i] = conv_plane(0, sm.x[2][t][i]);
-                const float z = to_f32(sm.x[3][t][i]);
-                sm.e[t][i] = expf(decay_gate(a.gate_kind, a.lb, eA, z + dtb));
+        // ---- conv + SiLU, gate, beta of the group's tokens.  The conv reads a
+        // sequence of the 3 window values and the group's raw inputs, so the
+        // tokens do not depend on one another and their exponentials and
+        // divides overlap.  NT (2, 4 or 8) rows are computed, those past the
+        // group's end dropped.
+        auto conv_group = [&](auto nt_c) {
+            constexpr int NT = decltype(nt_c)::value;
+            TI xs[2][RING + NT];
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp) {
+#pragma unroll
+                for (int s = 0; s < RING; ++s) xs[pp][s] = win[pp][s];
+#pragma unroll
+                for (int t = 0; t < NT; ++t) xs[pp][RING + t] = sm.x[p0 + pp][t][i];
             }
-        }
+            auto conv_at = [&](int pp, int t) -> float {
+                const float4 w = wconv[pp];
+                float y = w.x * to_f32(xs[pp][t]);
+                y = fmaf(w.y, to_f32(xs[pp][t + 1]), y);
+                y = fmaf(w.z, to_f32(xs[pp][t + 2]), y);
+                y = fmaf(w.w, to_f32(xs[pp][t + 3]), y);
+                return y / (1.0f + expf(-y));
+            };
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                if (tid < D) {
+                    const float yq = conv_at(0, t), yk = conv_at(1, t);
+                    if (t < ng) {
+                        sm.qc[t][i] = yq;
+                        sm.kc[t][i] = yk;
+                    }
+                } else {
+                    const float yv = conv_at(0, t);
+                    const float ee = expf(decay_gate(a.gate_kind, a.lb, eA, to_f32(xs[1][RING + t]) + dtb));
+                    if (t < ng) {
+                        sm.va[t][i] = yv;
+                        sm.e[t][i] = ee;
+                    }
+                }
+            }
+            // the window after the group: raw inputs ng .. ng + 2 of the sequence
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp) {
+#pragma unroll
+                for (int s = 0; s < RING; ++s) {
+                    TI v = xs[pp][s];
+#pragma unroll
+                    for (int m = 1; m <= NT; ++m) v = ng == m ? xs[pp][m + s] : v;
+                    win[pp][s] = v;
+                }
+            }
+        };
+        if (ng <= 2) conv_group(std::integral_constant<int, 2>{});
+        else if (ng <= 4) conv_group(std::integral_constant<int, 4>{});
+        else conv_group(std::integral_constant<int, DG>{});
         if (warp == 7 && lane < ng) sm.beta[lane] = 1.0f / (1.0f + expf(-to_f32(bl)));
         __syncthreads();
         if (g0 + DG < n_tok) stage(g0 + DG, (gi + 1) & 1);  // the staged inputs are consumed
