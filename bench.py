@@ -529,8 +529,11 @@ def main():
                 "workload": f"verify round: {VERIFY_TOKENS} tokens per session in one call (kda_decode_multi), "
                             "same sessions and state",
                 "value": dr["sessions"] * VERIFY_TOKENS * world / (allreduce_max(dr["verify_ms"], world) / 1e3),
-                "unit": "session*tokens/s", "ms_per_step": dr["verify_ms"],
+                "unit": "session*tokens/s", "ms_per_step": dr["verify_ms"], "kernel": "decode_round_kernel",
                 "hbm_frac": dr["verify_bytes"] / (dr["verify_ms"] / 1e3) / 1e9 / hbm,
+                "traffic": ncu_traffic("decode_round_kernel",
+                                       os.path.join(ROOT, "gated_delta_rule_04_gb300", "csrc", "kda_decode.cu"),
+                                       dr["sessions"] * dr["H"]),
                 "algorithmic_bytes_per_launch": dr["verify_bytes"]},
         }
     if not args.no_e2e:

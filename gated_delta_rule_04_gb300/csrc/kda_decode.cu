@@ -46,6 +46,12 @@ namespace {
 
 constexpr int DC_THREADS = 256;
 constexpr int DG = 8;    // tokens per group
+constexpr int RP = 144;  // padded row vector: key row r at rix(r)
+
+// Key row r of a padded row vector.  A half warp reads row blocks rb..rb+7
+// (8 floats apart) in one 128-bit load; the 4-float step after every 32 rows
+// puts blocks rb and rb + 4 in different banks.
+__device__ __forceinline__ int rix(int r) { return r + ((r >> 5) << 2); }
 
 template <typename TI>
 struct DecodeSmem {
@@ -54,10 +60,10 @@ struct DecodeSmem {
     float qc[DG][D], kc[DG][D];  // conv + SiLU of q and k, before the L2 norm
     float va[DG][D];             // conv + SiLU of v
     float so[DG][D];             // o before RMSNormGated
-    float e[DG][D];              // exp(g)
-    float kh[DG][D];             // k^
-    float av[DG][D];             // exp(g) k^  (u = S^T av = S'^T k^)
-    float bv[DG][D];             // exp(g) q^  (S^T bv = S'^T q^)
+    float e[DG][RP];             // exp(g)
+    float kh[DG][RP];            // k^
+    float av[DG][RP];            // exp(g) k^  (u = S^T av = S'^T k^)
+    float bv[DG][RP];            // exp(g) q^  (S^T bv = S'^T q^)
     float beta[DG], qk[DG];      // beta, q^.k^
 };
 
@@ -365,7 +371,7 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
                     const float ee = expf(decay_gate(a.gate_kind, a.lb, eA, to_f32(xs[1][RING + t]) + dtb));
                     if (t < ng) {
                         sm.va[t][i] = yv;
-                        sm.e[t][i] = ee;
+                        sm.e[t][rix(i)] = ee;
                     }
                 }
             }
@@ -390,7 +396,7 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
 
         // ---- L2 norms: warp t normalises token t, lane l channels 4l..4l+3
         if (warp < ng) {
-            const int t = warp, ro = 4 * lane;
+            const int t = warp, ro = rix(4 * lane);
             const float4 q4 = *reinterpret_cast<const float4*>(&sm.qc[t][4 * lane]);
             const float4 k4 = *reinterpret_cast<const float4*>(&sm.kc[t][4 * lane]);
             const float4 e4 = *reinterpret_cast<const float4*>(&sm.e[t][ro]);
@@ -417,8 +423,8 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
 #pragma unroll 1
         for (int t = 0; t < ng; ++t) {
             // partial S^T av and S^T bv over this lane's 8 rows, per local column pair
-            const float* A = &sm.av[t][8 * rb];
-            const float* B = &sm.bv[t][8 * rb];
+            const float* A = &sm.av[t][rix(8 * rb)];
+            const float* B = &sm.bv[t][rix(8 * rb)];
             float2 u[4], w[4];
 #pragma unroll
             for (int p = 0; p < 4; ++p) u[p] = w[p] = make_float2(0.f, 0.f);
@@ -492,8 +498,8 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
 
             // S = Diag(e) S + k^ d^T; after the last token each row piece
             // streams out as soon as it is final (every read of S_in is behind us)
-            const float* E = &sm.e[t][8 * rb];
-            const float* K = &sm.kh[t][8 * rb];
+            const float* E = &sm.e[t][rix(8 * rb)];
+            const float* K = &sm.kh[t][rix(8 * rb)];
             const bool last = g0 + t + 1 == n_tok;
 #pragma unroll
             for (int r4 = 0; r4 < 2; ++r4) {
