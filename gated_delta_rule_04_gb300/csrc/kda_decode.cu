@@ -18,22 +18,18 @@
 //
 // Work split.  Everything that does not touch S (conv, SiLU, gate, beta, the
 // L2 norms) runs for a group of up to DG tokens at once, and the output norm
-// for the group runs after it, so a group costs three block barriers however
-// many tokens it holds.  Inside the group the recurrence needs none: warp w
-// owns value columns 16w..16w+15 of S, and lane (cg, rb) = (lane % 2,
-// lane / 2) holds key rows 8rb..8rb+7 of columns 16w + 4cg + (0..3) and
-// 16w + 8 + 4cg + (0..3).  The sums over key rows (u = S'^T k, S'^T q) close
-// inside the warp in a four-level butterfly that halves the columns a lane
-// carries at each level; d comes back the same way.  A lane reads 8 rows of
-// each per-token row vector, which keeps the shared-memory traffic of a token
-// at 32 floats per lane (the shared-memory pipe, not the arithmetic, set the
-// speed of wider row ranges).  Column pairs run as packed fp32 pairs.
+// for the group runs after it.  In both kernels warp w owns key rows
+// 16w..16w+15 of S and lane l value columns 4l..4l+3, so every load and store
+// instruction of S moves 512 contiguous bytes and every per-row value is one
+// shared-memory broadcast; the sums over key rows meet in shared memory.
+// A token costs two block barriers in the round kernel (partial sums in,
+// d out).  A layout that keeps the key-row sums inside a warp (an 8 x 8
+// lane tile and a shuffle butterfly) needs no barrier per token, but its
+// 32-byte row pieces made the state traffic alone 0.044 ms slower on 8192
+// session-heads, more than the barriers cost.
 //
-// Memory: each load or store instruction of S moves 16 row pieces of 32 bytes.
-// The raw inputs of a group reach shared memory by cp.async, each piece
-// copied by the warp that reads it.  The state and ring are read from the
-// input pools before anything is written, so input and output may alias
-// (in-place update).
+// The state and ring are read from the input pools before anything is
+// written, so input and output may alias (in-place update).
 #include <algorithm>
 #include <atomic>
 #include <type_traits>
@@ -48,9 +44,8 @@ constexpr int DC_THREADS = 256;
 constexpr int DG = 8;    // tokens per group
 constexpr int RP = 144;  // padded row vector: key row r at rix(r)
 
-// Key row r of a padded row vector.  A half warp reads row blocks rb..rb+7
-// (8 floats apart) in one 128-bit load; the 4-float step after every 32 rows
-// puts blocks rb and rb + 4 in different banks.
+// Key row r of a padded row vector (a 4-float step after every 32 rows
+// spreads the rows that the L2-norm step writes at once over all banks).
 __device__ __forceinline__ int rix(int r) { return r + ((r >> 5) << 2); }
 
 template <typename TI>
@@ -65,6 +60,8 @@ struct DecodeSmem {
     float av[DG][RP];            // exp(g) k^  (u = S^T av = S'^T k^)
     float bv[DG][RP];            // exp(g) q^  (S^T bv = S'^T q^)
     float beta[DG], qk[DG];      // beta, q^.k^
+    float red[8][2][D];          // per-warp partial sums of S^T av and S^T bv
+    float sd[D];                 // d of the current token
 };
 
 // Persistent CTAs walk the (session, head) items with a stride of the grid.
@@ -94,11 +91,9 @@ __device__ __forceinline__ void prefetch_item(const DecodeArgs& a, int item, int
 }
 
 // ---- one token per session (plain decode) ----------------------------------
-// Warp w owns key rows 16w..16w+15 of S and lane l value columns 4l..4l+3, so
-// every load and store instruction of S moves 512 contiguous bytes and every
-// per-row value is one shared-memory broadcast; the sums over key rows meet
-// in shared memory.  With a single token the four block barriers this costs
-// are cheaper than the in-warp butterfly of the round kernel below.
+// The token's inputs are read straight into registers (no group staging), and
+// its conv, norms and gate run on the threads that own the channels; four
+// block barriers in all.
 template <typename TI>
 __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
     const int H = a.H, W = H * D;
@@ -286,24 +281,13 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
     };
     stage(0, 0);
 
-    // ---- the state block of this lane: rows 8rb + r; Sp[r][p] holds local
-    // columns 2p, 2p + 1, where local column m is 16w + 8(m / 4) + 4cg + m % 4
-    const int cg = lane & 1, rb = lane >> 1;
-    const int H1 = (lane >> 4) & 1, H2 = (lane >> 3) & 1, H3 = (lane >> 2) & 1;  // butterfly levels
-    const int ca = 16 * warp + 4 * cg;
+    // ---- the state: rows 16w + r, columns 4l..4l+3
     const float* Sg_in = a.S_in + ((size_t)slot * H + h) * D * D;
     float* Sg_out = a.S_out + ((size_t)slot * H + h) * D * D;
-    float2 Sp[8][4];
+    float4 Sr[16];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        const float* src = Sg_in + (size_t)(8 * rb + r) * D + ca;
-        const float4 lo = __ldcs(reinterpret_cast<const float4*>(src));
-        const float4 hi = __ldcs(reinterpret_cast<const float4*>(src + 8));
-        Sp[r][0] = make_float2(lo.x, lo.y);
-        Sp[r][1] = make_float2(lo.z, lo.w);
-        Sp[r][2] = make_float2(hi.x, hi.y);
-        Sp[r][3] = make_float2(hi.z, hi.w);
-    }
+    for (int r = 0; r < 16; ++r)
+        Sr[r] = __ldcs(reinterpret_cast<const float4*>(Sg_in + (size_t)(16 * warp + r) * D) + lane);
 
     // ---- conv windows in registers: threads 0-127 own channel i of planes q
     // and k, threads 128-255 channel i of plane v (and the gate); slot 0 is
@@ -419,90 +403,52 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
         }
         __syncthreads();
 
-        // ---- the recurrence over the group, no block barrier
+        // ---- the recurrence over the group: per token, partial S^T av and
+        // S^T bv over this warp's 16 rows, their sums and d per column, and
+        // the rank-1 update; column pairs run as packed fp32 pairs
 #pragma unroll 1
         for (int t = 0; t < ng; ++t) {
-            // partial S^T av and S^T bv over this lane's 8 rows, per local column pair
-            const float* A = &sm.av[t][rix(8 * rb)];
-            const float* B = &sm.bv[t][rix(8 * rb)];
-            float2 u[4], w[4];
+            const float* A = &sm.av[t][rix(16 * warp)];
+            const float* B = &sm.bv[t][rix(16 * warp)];
+            float2 u01[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}, u23[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            float2 w01[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}, w23[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int p = 0; p < 4; ++p) u[p] = w[p] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int r4 = 0; r4 < 2; ++r4) {
+            for (int r4 = 0; r4 < 4; ++r4) {
                 const float4 a4 = *reinterpret_cast<const float4*>(A + 4 * r4);
                 const float4 b4 = *reinterpret_cast<const float4*>(B + 4 * r4);
                 const float ar[4] = {a4.x, a4.y, a4.z, a4.w}, br[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
+                    const int r = 4 * r4 + m, p = m & 1;
                     const float2 aa = make_float2(ar[m], ar[m]), bb = make_float2(br[m], br[m]);
-#pragma unroll
-                    for (int p = 0; p < 4; ++p) {
-                        u[p] = __ffma2_rn(aa, Sp[4 * r4 + m][p], u[p]);
-                        w[p] = __ffma2_rn(bb, Sp[4 * r4 + m][p], w[p]);
-                    }
+                    const float2 s01 = make_float2(Sr[r].x, Sr[r].y), s23 = make_float2(Sr[r].z, Sr[r].w);
+                    u01[p] = __ffma2_rn(aa, s01, u01[p]); u23[p] = __ffma2_rn(aa, s23, u23[p]);
+                    w01[p] = __ffma2_rn(bb, s01, w01[p]); w23[p] = __ffma2_rn(bb, s23, w23[p]);
                 }
             }
-            // butterfly over the 16 row blocks: at each level a lane keeps
-            // half of its columns and adds its partner's partial sums of them.
-            // It ends with local column m = 4H1 + 2H2 + H3 (in two lanes, equal
-            // to the last bit: the last addition only swaps operands).
-            float uj, wj;
-            {
-                float2 ku0 = H1 ? u[2] : u[0], ku1 = H1 ? u[3] : u[1];
-                float2 kw0 = H1 ? w[2] : w[0], kw1 = H1 ? w[3] : w[1];
-                const float2 su0 = H1 ? u[0] : u[2], su1 = H1 ? u[1] : u[3];
-                const float2 sw0 = H1 ? w[0] : w[2], sw1 = H1 ? w[1] : w[3];
-                ku0.x += __shfl_xor_sync(0xffffffffu, su0.x, 16);
-                ku0.y += __shfl_xor_sync(0xffffffffu, su0.y, 16);
-                ku1.x += __shfl_xor_sync(0xffffffffu, su1.x, 16);
-                ku1.y += __shfl_xor_sync(0xffffffffu, su1.y, 16);
-                kw0.x += __shfl_xor_sync(0xffffffffu, sw0.x, 16);
-                kw0.y += __shfl_xor_sync(0xffffffffu, sw0.y, 16);
-                kw1.x += __shfl_xor_sync(0xffffffffu, sw1.x, 16);
-                kw1.y += __shfl_xor_sync(0xffffffffu, sw1.y, 16);
-                float2 pu = H2 ? ku1 : ku0, pw = H2 ? kw1 : kw0;
-                const float2 qu = H2 ? ku0 : ku1, qw = H2 ? kw0 : kw1;
-                pu.x += __shfl_xor_sync(0xffffffffu, qu.x, 8);
-                pu.y += __shfl_xor_sync(0xffffffffu, qu.y, 8);
-                pw.x += __shfl_xor_sync(0xffffffffu, qw.x, 8);
-                pw.y += __shfl_xor_sync(0xffffffffu, qw.y, 8);
-                uj = H3 ? pu.y : pu.x;
-                wj = H3 ? pw.y : pw.x;
-                uj += __shfl_xor_sync(0xffffffffu, H3 ? pu.x : pu.y, 4);
-                wj += __shfl_xor_sync(0xffffffffu, H3 ? pw.x : pw.y, 4);
-                uj += __shfl_xor_sync(0xffffffffu, uj, 2);
-                wj += __shfl_xor_sync(0xffffffffu, wj, 2);
+            const float2 uu01 = __fadd2_rn(u01[0], u01[1]), uu23 = __fadd2_rn(u23[0], u23[1]);
+            const float2 ww01 = __fadd2_rn(w01[0], w01[1]), ww23 = __fadd2_rn(w23[0], w23[1]);
+            *reinterpret_cast<float4*>(&sm.red[warp][0][4 * lane]) = make_float4(uu01.x, uu01.y, uu23.x, uu23.y);
+            *reinterpret_cast<float4*>(&sm.red[warp][1][4 * lane]) = make_float4(ww01.x, ww01.y, ww23.x, ww23.y);
+            __syncthreads();
+            if (tid < D) {
+                float uj = 0.f, wj = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) { uj += sm.red[k][0][tid]; wj += sm.red[k][1][tid]; }
+                const float dj = sm.beta[t] * (sm.va[t][tid] - uj);
+                sm.sd[tid] = dj;
+                sm.so[t][tid] = fmaf(sm.qk[t], dj, wj);
             }
-            const int j = 16 * warp + 8 * H1 + 4 * cg + 2 * H2 + H3;
-            const float dj = sm.beta[t] * (sm.va[t][j] - uj);
-            const float oj = fmaf(sm.qk[t], dj, wj);
-            if (!(rb & 1)) sm.so[t][j] = oj;
-            // d of all eight local columns back to every lane, the butterfly reversed
-            float2 d[4];
-            {
-                const float dx = __shfl_xor_sync(0xffffffffu, dj, 4);
-                const float2 dp = H3 ? make_float2(dx, dj) : make_float2(dj, dx);
-                const float2 dq = make_float2(__shfl_xor_sync(0xffffffffu, dp.x, 8),
-                                              __shfl_xor_sync(0xffffffffu, dp.y, 8));
-                const float2 lo = H2 ? dq : dp, hi = H2 ? dp : dq;  // local columns 4H1 + 0..3
-                const float2 elo = make_float2(__shfl_xor_sync(0xffffffffu, lo.x, 16),
-                                               __shfl_xor_sync(0xffffffffu, lo.y, 16));
-                const float2 ehi = make_float2(__shfl_xor_sync(0xffffffffu, hi.x, 16),
-                                               __shfl_xor_sync(0xffffffffu, hi.y, 16));
-                d[0] = H1 ? elo : lo;
-                d[1] = H1 ? ehi : hi;
-                d[2] = H1 ? lo : elo;
-                d[3] = H1 ? hi : ehi;
-            }
-
-            // S = Diag(e) S + k^ d^T; after the last token each row piece
-            // streams out as soon as it is final (every read of S_in is behind us)
-            const float* E = &sm.e[t][rix(8 * rb)];
-            const float* K = &sm.kh[t][rix(8 * rb)];
+            __syncthreads();
+            const float4 d4 = *reinterpret_cast<const float4*>(&sm.sd[4 * lane]);
+            const float2 d01 = make_float2(d4.x, d4.y), d23 = make_float2(d4.z, d4.w);
+            const float* E = &sm.e[t][rix(16 * warp)];
+            const float* K = &sm.kh[t][rix(16 * warp)];
+            // S = Diag(e) S + k^ d^T; after the last token each row streams out
+            // as soon as it is final (every read of S_in is behind us)
             const bool last = g0 + t + 1 == n_tok;
 #pragma unroll
-            for (int r4 = 0; r4 < 2; ++r4) {
+            for (int r4 = 0; r4 < 4; ++r4) {
                 const float4 e4 = *reinterpret_cast<const float4*>(E + 4 * r4);
                 const float4 k4 = *reinterpret_cast<const float4*>(K + 4 * r4);
                 const float er[4] = {e4.x, e4.y, e4.z, e4.w}, kr[4] = {k4.x, k4.y, k4.z, k4.w};
@@ -510,15 +456,10 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
                 for (int m = 0; m < 4; ++m) {
                     const int r = 4 * r4 + m;
                     const float2 ee = make_float2(er[m], er[m]), kk = make_float2(kr[m], kr[m]);
-#pragma unroll
-                    for (int p = 0; p < 4; ++p) Sp[r][p] = __ffma2_rn(ee, Sp[r][p], __fmul2_rn(kk, d[p]));
-                    if (last) {
-                        float* dst = Sg_out + (size_t)(8 * rb + r) * D + ca;
-                        __stcs(reinterpret_cast<float4*>(dst),
-                               make_float4(Sp[r][0].x, Sp[r][0].y, Sp[r][1].x, Sp[r][1].y));
-                        __stcs(reinterpret_cast<float4*>(dst + 8),
-                               make_float4(Sp[r][2].x, Sp[r][2].y, Sp[r][3].x, Sp[r][3].y));
-                    }
+                    const float2 s01 = __ffma2_rn(ee, make_float2(Sr[r].x, Sr[r].y), __fmul2_rn(kk, d01));
+                    const float2 s23 = __ffma2_rn(ee, make_float2(Sr[r].z, Sr[r].w), __fmul2_rn(kk, d23));
+                    Sr[r] = make_float4(s01.x, s01.y, s23.x, s23.y);
+                    if (last) __stcs(reinterpret_cast<float4*>(Sg_out + (size_t)(16 * warp + r) * D) + lane, Sr[r]);
                 }
             }
         }
