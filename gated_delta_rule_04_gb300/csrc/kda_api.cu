@@ -126,9 +126,16 @@ constexpr size_t WS_COUNTER = 64;   // two work counters of the chunk preparatio
 
 // The windows and their workspace layout for a T-token sequence (false when it
 // is too short for two windows).  No device query: the workspace size uses it.
+// Shortest window.  With up to 64 heads the recurrence leaves most SMs to the
+// chunk preparation, and windows of 16 chunks paid from 2048 tokens on (20-25 %
+// at 8192-16384 tokens and 32 heads, measured on GB300).  With more heads the
+// recurrence takes most SMs and windows shorter than 8192 tokens did not pay.
+int64_t window_min(int H) { return H <= 64 ? 1024 : 8192; }
+
 bool overlap_layout(const kda_params* p, int64_t T, OverlapPlan* pl) {
-    if (T < 2 * 8192) return false;
-    const int64_t s0 = std::min<int64_t>(4, T / 8192);   // windows of at least 8192 tokens
+    const int64_t wmin = window_min(p->num_heads);
+    if (T < 2 * wmin) return false;
+    const int64_t s0 = std::min<int64_t>(4, T / wmin);   // up to 4 windows of at least wmin tokens
     const int64_t seg = ((T + s0 - 1) / s0 + CHUNK - 1) / CHUNK * CHUNK;
     pl->S = (int)((T + seg - 1) / seg);
     if (pl->S < 2) return false;
@@ -225,6 +232,38 @@ bool plan_overlap(const kda_params* p, int64_t T, size_t ws_bytes, OverlapPlan* 
     return pl->total <= ws_bytes;
 }
 
+// The recurrence stream (highest priority) and the events of the window
+// schedule, per host thread and device: created on a thread's first windowed
+// call on a device and kept for the thread's lifetime.  Two host threads never
+// share them, so concurrent calls on different streams cannot wait on each
+// other's events; calls from one thread are ordered by the events themselves.
+struct WindowStreams {
+    cudaStream_t sr = nullptr;
+    cudaEvent_t ev[6] = {};
+};
+WindowStreams* window_streams() {
+    thread_local std::vector<WindowStreams> per_device;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
+    if ((size_t)dev >= per_device.size()) per_device.resize(dev + 1);
+    WindowStreams& w = per_device[dev];
+    if (w.sr == nullptr) {
+        int least = 0, greatest = 0;
+        WindowStreams n;
+        bool good = cudaDeviceGetStreamPriorityRange(&least, &greatest) == cudaSuccess &&
+                    cudaStreamCreateWithPriority(&n.sr, cudaStreamNonBlocking, greatest) == cudaSuccess;
+        for (auto& e : n.ev) good = good && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
+        if (!good) {
+            for (auto& e : n.ev)
+                if (e) cudaEventDestroy(e);
+            if (n.sr) cudaStreamDestroy(n.sr);
+            return nullptr;
+        }
+        w = n;
+    }
+    return &w;
+}
+
 kda_status prefill_overlapped(const kda_params* p, const void* q, const void* k, const void* v, const void* z,
                               const void* b, const void* gout, int64_t T, const float* S_in, float* S_out,
                               const void* ring_in, void* ring_out, void* o, unsigned char* ws, cudaStream_t s,
@@ -247,21 +286,21 @@ kda_status prefill_overlapped(const kda_params* p, const void* q, const void* k,
     int32_t* status = reinterpret_cast<int32_t*>(ws);
     int32_t* counters = reinterpret_cast<int32_t*>(ws + WS_COUNTER);   // [2], by window parity
 
-    int least = 0, greatest = 0;
-    cudaStream_t sr = nullptr;
-    cudaEvent_t ev[6] = {};   // start, prep part 1 [2], recurrence [2], end
+    WindowStreams* res = window_streams();
+    if (res == nullptr) return KDA_ERR_CUDA;
+    cudaStream_t sr = res->sr;
+    cudaEvent_t* ev = res->ev;   // start, prep part 1 [2], recurrence [2], end
     kda_status st = KDA_OK;
-    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
-        cudaStreamCreateWithPriority(&sr, cudaStreamNonBlocking, greatest) != cudaSuccess)
-        return KDA_ERR_CUDA;
-    for (auto& e : ev)
-        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) st = KDA_ERR_CUDA;
     auto ok = [&](cudaError_t e) { if (e != cudaSuccess) st = KDA_ERR_CUDA; return st == KDA_OK; };
     if (st == KDA_OK && ok(cudaEventRecord(ev[0], s)) && ok(cudaStreamWaitEvent(sr, ev[0], 0)) &&
         ok(reset_status ? cudaMemsetAsync(ws, 0, WS_ALIGN, s) : cudaSuccess) &&
         ok(cudaMemcpyAsync(ws + pl.off_meta, meta.data(), meta.size(), cudaMemcpyHostToDevice, s)) &&
         ok(cudaMemcpyAsync(ws + pl.off_cufull, cufull, sizeof(cufull), cudaMemcpyHostToDevice, s))) {
         const float qs = resolved_q_scale(p);
+        // items per take: batches of PREP_BATCH amortise the counter, but a
+        // window with few items per SM balances better one item at a time
+        const int64_t win_items = pl.seg_chunks * H;
+        const int32_t batch = win_items >= (int64_t)8 * PREP_BATCH * pl.sms ? PREP_BATCH : 1;
         for (int w = 0; w < pl.S && st == KDA_OK; ++w) {
             const int r = w & 1;
             unsigned char* rec = ws + pl.off_rec[r];
@@ -273,7 +312,7 @@ kda_status prefill_overlapped(const kda_params* p, const void* q, const void* k,
             if (!ok(cudaMemsetAsync(counter, 0, sizeof(int32_t), s))) break;
             PrepArgs pr{q, k, v, z, b, ring_in, p->conv_w, p->A_log, p->dt_bias, p->gate_lower_bound, p->l2_eps, qs,
                         reinterpret_cast<const ChunkDesc*>(mw + 4 * sizeof(int64_t)), (int32_t)nck, H, T, rec, status,
-                        counter, {}, {}};
+                        counter, batch, {}, {}};
             // part 1 alongside the recurrence of window w - 1 (all SMs for window 0)
             if (!ok(launch_chunk_prep(pr, s, w == 0 ? 0 : pl.sms - H)) || !ok(cudaEventRecord(ev[1 + r], s))) break;
             // part 2 on the SMs that recurrence frees
@@ -290,11 +329,8 @@ kda_status prefill_overlapped(const kda_params* p, const void* q, const void* k,
         }
     }
     // the caller's stream orders after everything on the recurrence stream
-    if (ev[5] == nullptr || cudaEventRecord(ev[5], sr) != cudaSuccess || cudaStreamWaitEvent(s, ev[5], 0) != cudaSuccess)
+    if (cudaEventRecord(ev[5], sr) != cudaSuccess || cudaStreamWaitEvent(s, ev[5], 0) != cudaSuccess)
         st = KDA_ERR_CUDA;
-    for (auto& e : ev)
-        if (e) cudaEventDestroy(e);
-    cudaStreamDestroy(sr);
     return st;
 }
 
@@ -399,7 +435,8 @@ kda_status prefill_run(const kda_params* p, const void* q, const void* k, const 
         // the chunk preparation runs the pre-stage itself
         if (mark(ev, 1, s) != cudaSuccess) return KDA_ERR_CUDA;
         PrepArgs pr{q, k, v, z, b, ring_in, p->conv_w, p->A_log, p->dt_bias, p->gate_lower_bound, p->l2_eps, qs,
-                    d_chunks, (int32_t)n_chunks, H, total_tokens, ws + L.rec, reinterpret_cast<int32_t*>(ws + L.status), nullptr, {}, {}};
+                    d_chunks, (int32_t)n_chunks, H, total_tokens, ws + L.rec, reinterpret_cast<int32_t*>(ws + L.status), nullptr,
+                    PREP_BATCH, {}, {}};
         e = launch_chunk_prep(pr, s);
         if (e != cudaSuccess || mark(ev, 2, s) != cudaSuccess) return KDA_ERR_CUDA;
         // the recurrence kernel applies the output norm itself

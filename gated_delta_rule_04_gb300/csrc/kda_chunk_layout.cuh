@@ -51,14 +51,16 @@ struct PrepArgs {
     void* records;                  // [n_chunks][H][REC_BYTES]
     int32_t* status;                // workspace error word
     // NULL: each CTA takes a fixed contiguous range of items.  Otherwise a
-    // zeroed counter from which CTAs take batches of PREP_BATCH items in turn,
-    // so that CTAs starting late (other kernels hold their SMs) take fewer.
+    // zeroed counter from which CTAs take batches of `batch` items in turn
+    // (1 <= batch <= PREP_BATCH), so that CTAs starting late (other kernels
+    // hold their SMs) take fewer.
     int32_t* work_counter;
+    int32_t batch;
     // set by launch_chunk_prep: TMA descriptors of q, k, v as [T][H*128] bf16
     // with a 67-row box (a chunk and the three rows before it) and a 64-row box
     CUtensorMap map67[3], map64[3];
 };
-constexpr int PREP_BATCH = 4;        // items per take from PrepArgs::work_counter
+constexpr int PREP_BATCH = 4;        // most items per take from PrepArgs::work_counter
 // max_ctas > 0 caps the persistent grid (for a launch that shares the GPU).
 cudaError_t launch_chunk_prep(const PrepArgs& a, cudaStream_t s, int max_ctas = 0);
 size_t chunk_prep_smem_bytes();

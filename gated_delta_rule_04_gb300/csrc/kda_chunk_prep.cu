@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
 
     // This CTA's items, in head-major order (item j is chunk j % n_chunks of head
     // j / n_chunks, so consecutive items share their head's constants): either one
-    // contiguous range, or batches of PREP_BATCH taken from the work counter one
+    // contiguous range, or batches of a.batch taken from the work counter one
     // batch ahead (the next item must be known an item ahead for its loads).
     // [jt, j_stop) is the current batch and nb_start the first item of the next.
     const int NC = a.n_chunks;
@@ -322,9 +322,9 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
             s_take[1] = atomicAdd(a.work_counter, 1);
         }
         __syncthreads();
-        jt = min(s_take[0] * PREP_BATCH, n_items);
-        j_stop = min(jt + PREP_BATCH, n_items);
-        nb_start = min(s_take[1] * PREP_BATCH, n_items);
+        jt = min(s_take[0] * a.batch, n_items);
+        j_stop = min(jt + a.batch, n_items);
+        nb_start = min(s_take[1] * a.batch, n_items);
         __syncthreads();   // read before the loop rewrites s_take
     } else {
         jt = (int)(((int64_t)blockIdx.x * n_items) / gridDim.x);
@@ -832,8 +832,8 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
             ++jt;
         } else {
             jt = nb_start;
-            j_stop = min(nb_start + PREP_BATCH, n_items);
-            nb_start = a.work_counter != nullptr ? min(s_take[0] * PREP_BATCH, n_items) : n_items;
+            j_stop = min(nb_start + a.batch, n_items);
+            nb_start = a.work_counter != nullptr ? min(s_take[0] * a.batch, n_items) : n_items;
         }
     }
 

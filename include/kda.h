@@ -137,11 +137,13 @@ kda_status kda_prefill(const kda_params* p,
 
 /* Number of windows kda_prefill runs these arguments as: 1 for the single
  * pass, S >= 2 when one long sequence's recurrence would leave SMs idle
- * (chunked path, one sequence, fewer heads than SMs, at least 16384 tokens,
- * and a workspace that holds two windows' records).  Then the sequence runs
- * as S windows of whole chunks: window w's chunk preparation overlaps the
- * recurrence of window w - 1 on a second, high-priority stream that the call
- * creates, and the result is bit-identical to the single pass.  The query
+ * (chunked path, one sequence, fewer heads than SMs, at least 2048 tokens
+ * with up to 64 heads or 16384 with more, and a workspace that holds two
+ * windows' records).  Then the sequence runs as S <= 4 windows of whole
+ * chunks of at least 1024 tokens (up to 64 heads) or 8192 tokens each, the
+ * last shorter by the rounding to chunks.  Window w's chunk preparation
+ * overlaps the recurrence of window w - 1 on a second, high-priority stream
+ * that the call creates, and the result is bit-identical to the single pass.  The query
  * needs a current CUDA device (it reads the SM count); -1 for arguments
  * kda_prefill would reject. */
 int32_t kda_prefill_windows(const kda_params* p, int32_t n_seqs, int64_t total_tokens, size_t workspace_bytes);

@@ -281,20 +281,23 @@ def test_prefill_windows_query(L):
     assert L.kda_prefill_windows(ctypes.byref(p), -1, 32768, 1 << 40) == -1
     # several sequences, short ones, or the scan path: always the single pass
     assert L.kda_prefill_windows(ctypes.byref(p), 2, 32768, 1 << 40) == 1
-    assert L.kda_prefill_windows(ctypes.byref(p), 1, 4096, 1 << 40) == 1
+    assert L.kda_prefill_windows(ctypes.byref(p), 1, 2047, 1 << 40) == 1
     assert L.kda_prefill_windows(ctypes.byref(params(algo=kda.KDA_ALGO_SCAN)), 1, 32768, 1 << 40) == 1
     assert L.kda_prefill_windows(ctypes.byref(p), 1, 32768, 1 << 40) >= 1   # needs a device for more
 
 
-@pytest.mark.parametrize("T", [16384, 20384, 32768, 32768 + 64 * 7 + 5])
-def test_workspace_covers_overlapped_windows(L, T):
-    """A long single sequence may run as windows; the workspace query covers
+@pytest.mark.parametrize("H", [8, 96])
+@pytest.mark.parametrize("T", [2048, 4096 + 37, 16384, 20384, 32768, 32768 + 64 * 7 + 5])
+def test_workspace_covers_overlapped_windows(L, T, H):
+    """A single sequence may run as up to 4 windows of at least 1024 tokens
+    (up to 64 heads) or 8192 tokens (more heads); the workspace query covers
     two windows' records (window sizes round up to whole 64-token chunks)."""
-    H, rec = 8, 74240
+    rec = 74240
     p = params(num_heads=H)
     need = L.kda_prefill_workspace_bytes(ctypes.byref(p), 1, T)
-    windows = min(4, T // 8192)
-    seg_chunks = -(-(-(-T // windows)) // 64)
-    assert need >= 2 * seg_chunks * H * rec
+    windows = min(4, T // (1024 if H <= 64 else 8192))
+    if windows >= 2:
+        seg_chunks = -(-(-(-T // windows)) // 64)
+        assert need >= 2 * seg_chunks * H * rec
     # and never less than the single pass needs for several sequences' worth of chunks
     assert need >= (T // 64 + 1) * H * rec

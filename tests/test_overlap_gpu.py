@@ -20,7 +20,7 @@ def _built():
     kda.lib()
 
 
-@pytest.mark.parametrize("T, in_place", [(16384, False), (16384 + 4000, True)])
+@pytest.mark.parametrize("T, in_place", [(2048, False), (4096 + 100, True), (16384, False), (16384 + 4000, True)])
 def test_windows_equal_single_pass(T, in_place):
     H, io = 8, "bf16"
     p = kda_synth.draw_params(H, 101)
