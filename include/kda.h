@@ -142,8 +142,11 @@ kda_status kda_prefill(const kda_params* p,
  * windows' records).  Then the sequence runs as S <= 4 windows of whole
  * chunks of at least 1024 tokens (up to 64 heads) or 8192 tokens each, the
  * last shorter by the rounding to chunks.  Window w's chunk preparation
- * overlaps the recurrence of window w - 1 on a second, high-priority stream
- * that the call creates, and the result is bit-identical to the single pass.  The query
+ * overlaps the recurrence of window w - 1 on a second, high-priority stream,
+ * and the result is bit-identical to the single pass.  That stream and six
+ * events are created on a host thread's first windowed call on a device and
+ * kept for the thread's lifetime (one set per thread and device, never
+ * shared between threads).  The query
  * needs a current CUDA device (it reads the SM count); -1 for arguments
  * kda_prefill would reject. */
 int32_t kda_prefill_windows(const kda_params* p, int32_t n_seqs, int64_t total_tokens, size_t workspace_bytes);
