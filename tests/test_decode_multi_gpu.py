@@ -172,3 +172,22 @@ def test_longest_round_f32():
     assert_close("o", o, ref["o"], tol)
     assert_close("S", S, ref["S"], tol)
     np.testing.assert_array_equal(ring.double().cpu().numpy(), ref["ring"])
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("n_tok", [1, 9, 17])
+@pytest.mark.parametrize("gate_kind", [0, 1])
+def test_round_lengths_across_groups_and_gates(io, n_tok, gate_kind):
+    """Round lengths around the 8-token groups of the round kernel (9: a full
+    group and a group of one; 17: two full groups and one) and one token (the
+    one-token kernel), with the bounded and the softplus gate, against the
+    oracle."""
+    n = 2
+    p, tk, S0, ring0 = round_inputs(io, n, n_tok, seed=71 + n_tok)
+    p.gate_kind = gate_kind
+    o, S, ring, _, _ = run_round(p, tk, n, n_tok, io, S0, ring0)
+    ref = oracle_run(p, tk, list(range(0, n * n_tok + 1, n_tok)), S_in=S0, ring_in=ring0)
+    tol = tol_for(io)
+    assert_close("o", o, ref["o"], tol)
+    assert_close("S", S, ref["S"], tol)
+    np.testing.assert_array_equal(ring.double().cpu().numpy(), ref["ring"])
