@@ -8,7 +8,7 @@ import torch
 
 import gated_delta_rule_04_gb300 as kda
 import kda_synth
-from kda_testlib import assert_close, kda_params, oracle_run, tol_for
+from kda_testlib import assert_close, head_cols, kda_params, oracle_run, tol_for
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -102,3 +102,25 @@ def test_host_prefill_status_word_is_clear():
     scratch = torch.empty(kda.kda_prefill_host_scratch_bytes(kp, cu, 128), dtype=torch.uint8, device=DEV)
     kda.kda_prefill_host(kp, *[t.pin_memory() for t in tk.fields()], cu, segment_tokens=128, scratch=scratch)
     assert kda.kda_workspace_status(scratch) == kda.KDA_OK
+
+
+def test_host_prefill_segments_that_run_as_windows():
+    """Segments long enough to run as overlapped windows (2560 tokens, 8
+    heads), on the chunk grid: bit-identical to one kda_prefill of the whole
+    sequence, and the oracle on one head."""
+    io, cu, H = "bf16", [0, 5120], 8
+    p, tk, S0, ring0 = inputs(io, cu, H=H, seed=97)
+    kp = kda_params(p, io)
+    assert kda.kda_prefill_windows(kp, 1, 2560, 1 << 40) >= 2
+    o, S, ring = run_host(p, tk, cu, io, 2560, S0, ring0)
+    o_d, S_d, ring_d = kda.kda_prefill(kp, *[t.to(DEV) for t in tk.fields()], cu, S_in=S0.to(DEV),
+                                       ring_in=ring0.to(DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_d.cpu())
+    assert torch.equal(S.cpu(), S_d.cpu())
+    assert torch.equal(ring.cpu(), ring_d.cpu())
+    ref = oracle_run(p, tk, cu, S_in=S0, ring_in=ring0, heads=[3])
+    cols = head_cols([3])
+    tol = tol_for(io)
+    assert_close("o", o[:, cols], ref["o"], tol)
+    assert_close("S", S[:, [3]], ref["S"], tol)
