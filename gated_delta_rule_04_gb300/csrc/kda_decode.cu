@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
             win[pp][0] = win[pp][1];
             win[pp][1] = win[pp][2];
             win[pp][2] = xr;
-            return y / (1.0f + expf(-y));
+            return silu_fast(y);
         };
 
         // ---- conv + SiLU (threads 0-127: planes q, k; 128-255: v + gate)
@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
         } else {
             s_v[i] = conv_plane(0);
             const float z = to_f32(static_cast<const TI*>(a.z)[tok]);
-            s_e[i] = expf(decay_gate(a.gate_kind, a.lb, expf(a.A_log[h]), z + a.dt_bias[c]));
+            s_e[i] = __expf(decay_gate(a.gate_kind, a.lb, expf(a.A_log[h]), z + a.dt_bias[c]));
         }
         __syncthreads();
         if (tid < D) {
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
             if (tid == 0) {
                 s_scal[0] = sqk * rq * rk;  // q^.k^
                 const float bl = to_f32(static_cast<const TI*>(a.b)[(size_t)n * H + h]);
-                s_scal[1] = 1.0f / (1.0f + expf(-bl));
+                s_scal[1] = sigmoid_fast(bl);
             }
         }
         __syncthreads();
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_kernel(DecodeArgs a) {
             const float ss = s_sum[0][3] + s_sum[1][3] + s_sum[2][3] + s_sum[3][3];
             const float r = rsqrtf(ss * (1.0f / D) + a.norm_eps);
             const float gt = to_f32(static_cast<const TI*>(a.gout)[tok]);
-            static_cast<TI*>(a.o)[tok] = from_f32<TI>(oj * r * a.norm_w[tid] / (1.0f + expf(-gt)));
+            static_cast<TI*>(a.o)[tok] = from_f32<TI>(oj * r * a.norm_w[tid] * sigmoid_fast(gt));
         }
 
         // ---- ring out (after every read of the inputs)
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
                     y = fmaf(w.y, to_f32(xs[pp][t + 1]), y);
                     y = fmaf(w.z, to_f32(xs[pp][t + 2]), y);
                     y = fmaf(w.w, to_f32(xs[pp][t + 3]), y);
-                    return y / (1.0f + expf(-y));
+                    return silu_fast(y);
                 };
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
                         }
                     } else {
                         const float yv = conv_at(0, t);
-                        const float ee = expf(decay_gate(a.gate_kind, a.lb, eA, to_f32(xs[1][RING + t]) + dtb));
+                        const float ee = __expf(decay_gate(a.gate_kind, a.lb, eA, to_f32(xs[1][RING + t]) + dtb));
                         if (t < ng) {
                             sm.va[t][i] = yv;
                             sm.e[t][rix(i)] = ee;
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
             if (ng <= 2) conv_group(std::integral_constant<int, 2>{});
             else if (ng <= 4) conv_group(std::integral_constant<int, 4>{});
             else conv_group(std::integral_constant<int, DG>{});
-            if (warp == 7 && lane < ng) sm.beta[lane] = 1.0f / (1.0f + expf(-to_f32(bl)));
+            if (warp == 7 && lane < ng) sm.beta[lane] = sigmoid_fast(to_f32(bl));
             __syncthreads();
             if (g0 + DG < n_tok) stage(g0 + DG, (gi + 1) & 1);  // the staged inputs are consumed
 
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(DC_THREADS, 2) decode_round_kernel(DecodeArgs 
                 const float ov[4] = {o4.x, o4.y, o4.z, o4.w}, nv[4] = {nw.x, nw.y, nw.z, nw.w};
                 TI y[4];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) y[m] = from_f32<TI>(ov[m] * r * nv[m] / (1.0f + expf(-to_f32(gg[m]))));
+                for (int m = 0; m < 4; ++m) y[m] = from_f32<TI>(ov[m] * r * nv[m] * sigmoid_fast(to_f32(gg[m])));
                 TI* dst = static_cast<TI*>(a.o) + (row0 + g0 + t) * W + (size_t)h * D + 4 * lane;
                 if constexpr (sizeof(TI) == 4) {
                     *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(y);
