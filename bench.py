@@ -10,7 +10,10 @@ inputs resident in HBM.  Alongside it:
   e2e        the same prefill from pinned HOST buffers (kda_prefill_host: token
              segments whose host->device copies and device->host read of o overlap
              the kernels), all copies inside the timed region
-  roofline   the dominant kernel's achieved HBM bandwidth vs the measured peak
+  roofline   the dominant kernel against the method's own bytes (fused single pass)
+  step       the whole step's HBM fraction and tensor-core fraction
+  kernels    each kernel's own bytes over its time
+  other_prefill  the same for the single-sequence T=4096 H=32 and the varlen H=64 workloads
   cpu_baseline  the fp64 oracle on a bounded sample of the same workload
 
 --impl reference times the oracle (the only other implementation) as the
@@ -87,7 +90,7 @@ class Clocks:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
-    PERIOD_MS = 100
+    PERIOD_MS = 20
 
     def __init__(self, device_index):
         self.proc = None
@@ -198,6 +201,15 @@ def scan_bytes_per_token_head():
 
 REC_BYTES = 74240  # one chunk-head record of operand tiles (kda_chunk_layout.cuh)
 
+# The method's own per-token-head figures for prefill at bf16 I/O, independent of
+# how the work is split into kernels:
+#  - bytes: a single fused pass must read the raw q, k, v, z, gout rows (d each) and
+#    the beta logit and write o (d): 5*256 + 2 + 256 = 1538 B;
+#  - flops (64-token chunks): 6 d^2 for Q+S, WS and Kt^T U, plus 5 d C for the five
+#    triangular C x C x d products (the useful half): 98304 + 40960 = 139264.
+METHOD_BYTES_PER_TOKEN_HEAD = 5 * D * 2 + 2 + D * 2
+METHOD_FLOP_PER_TOKEN_HEAD = 6 * D * D + 5 * D * 64
+
 
 def prep_bytes_per_token_head(io_bytes):
     # reads raw q,k,v (+ the three rows before each 64-token chunk), z and b; writes the record
@@ -231,9 +243,11 @@ def verify_bytes_per_session_head(io_bytes, n_tok):
 PREFILL_WORKLOADS = {"long": 3, "prefill": 2, "varlen": 4}
 
 
-def prefill_arm(args, dev, world, rank):
+def prefill_arm(args, dev, world, rank, idx=None, heads=None, steps=None):
     import gated_delta_rule_04_gb300 as kda
-    w = kda_synth.workload(PREFILL_WORKLOADS[args.workload], device=dev, H=args.heads)
+    idx = PREFILL_WORKLOADS[args.workload] if idx is None else idx
+    steps = steps or args.steps
+    w = kda_synth.workload(idx, device=dev, H=heads if heads is not None else args.heads)
     H, T, W = w.H, w.total_tokens, w.H * D
     kp = kda.make_params(w.params.conv_w, w.params.A_log, w.params.dt_bias, w.params.norm_w,
                          io_dtype=w.io, algo=args.algo)
@@ -259,7 +273,7 @@ def prefill_arm(args, dev, world, rank):
         step()
     torch.cuda.synchronize()
     evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(kda.KDA_PREFILL_EVENTS)]
-              for _ in range(args.steps)]
+              for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for evs in evsets:  # create the handles outside the timed region
         for e in evs:
@@ -271,12 +285,12 @@ def prefill_arm(args, dev, world, rank):
     # pass, or overlapped windows for one long sequence)
     with Clocks(dev.index or 0) as clk:
         start.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             step()
         end.record(stream)
         torch.cuda.synchronize()
     barrier(world)
-    ms = start.elapsed_time(end) / args.steps
+    ms = start.elapsed_time(end) / steps
     # each kernel alone: the single pass with events at the stage boundaries
     for _ in range(2):
         step(evsets[0])
@@ -295,7 +309,7 @@ def prefill_arm(args, dev, world, rank):
     # second on), a recurrence per window and the ring; scan: pre-stage, scan, epilogue, ring
     per_step = (3 if windows == 1 else 3 * windows) if algo == "chunked" else 4
     return dict(w=w, ms=ms, ms_max=ms_max, stage_ms=stage_ms, single_ms=single_ms, windows=windows,
-                clocks=clk.summary(), kp=kp, launches=per_step * args.steps, ws_status=ws_status,
+                clocks=clk.summary(), kp=kp, launches=per_step * steps, ws_status=ws_status,
                 algo_resolved=algo)
 
 
@@ -379,13 +393,12 @@ def cpu_baseline(args, sample_heads=None, sample_tokens=32768):
     of it: `sample_heads` heads (default all) x the first `sample_tokens`
     tokens.  The whole workload is about 10 s on 16 host cores."""
     import oracle
-    from tests.kda_testlib import oracle_run  # marshalling helper only
     w = kda_synth.workload(3, device="cuda" if torch.cuda.is_available() else "cpu")
     sample_heads = sample_heads or w.H
     heads = list(range(sample_heads))
     sub = kda_synth.Tokens(*[t[:sample_tokens] for t in w.tokens.fields()])
     t0 = time.perf_counter()
-    oracle_run(w.params.to("cpu"), sub, [0, sample_tokens], heads=heads)
+    oracle.run_synth(w.params.to("cpu"), sub, [0, sample_tokens], heads=heads)
     dt = time.perf_counter() - t0
     token_heads = sample_heads * sample_tokens
     value = token_heads / w.H / dt  # full-layer tokens/s
@@ -402,14 +415,13 @@ def reference_main(args, world, rank):
     if rank != 0:
         return
     import oracle
-    from tests.kda_testlib import oracle_run
     n_tok, n_heads = REFERENCE_STEP["tokens"], REFERENCE_STEP["heads"]
     w = kda_synth.workload(3, device="cpu", lens=[n_tok])
     heads = list(range(n_heads))
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        oracle_run(w.params, w.tokens, w.cu_seqlens, heads=heads)
+        oracle.run_synth(w.params, w.tokens, w.cu_seqlens, heads=heads)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     dt = statistics.mean(times)
@@ -429,6 +441,84 @@ def reference_main(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def prefill_report(r, hbm, tc, tc_sus, peak_kind):
+    """Roofline figures of one prefill measurement.
+
+    roofline: the dominant kernel (largest share of the single pass) against the
+      method's own bytes per token-head (a fused single pass: raw q, k, v, z, gout,
+      beta in and o out) -- the bytes any implementation must move, whatever its
+      kernels -- divided by that kernel's CUDA-event time.
+    step: the same bytes and the method's algorithmic flops over the whole step as
+      a user runs it: the HBM fraction and the tensor-core fraction (of the
+      sustained bf16 peak: the step runs back to back).
+    kernels: each kernel's own bytes (what it reads and writes, its intermediates
+      included) over its time, as a fraction of the copy bandwidth.
+    """
+    w = r["w"]
+    H, T = w.H, w.total_tokens
+    chunked = r["algo_resolved"] == "chunked"
+    stage_names = ["prestage", "chunk_prep", "recurrence", "epilogue", "ring"]
+    kernels = ["prestage_kernel", "chunk_prep_kernel", "chunk_recurrence_kernel" if chunked else "scan_kernel",
+               "epilogue_kernel", "ring_update_kernel"]
+    srcs = ["kda_prestage.cu", "kda_chunk_prep.cu", "kda_chunk.cu" if chunked else "kda_scan.cu",
+            "kda_epilogue.cu", "kda_prestage.cu"]
+    state_bytes = 2 * D * D * 4 * w.n_seqs * H  # S read + written once per (sequence, head)
+    own = [0 if chunked else prestage_bytes_per_token_head(2, 4) * T * H,
+           prep_bytes_per_token_head(2) * T * H if chunked else 0,
+           (chunk_recurrence_bytes_per_token_head(2) if chunked else scan_bytes_per_token_head()) * T * H
+           + state_bytes,
+           0 if chunked else epilogue_bytes_per_token_head(2) * T * H, 0]
+    stage_ms = r["stage_ms"]
+    dom = max(range(4), key=lambda i: stage_ms[i])
+    method_bytes = METHOD_BYTES_PER_TOKEN_HEAD * T * H + (state_bytes if w.warmup_tokens is not None else 0)
+    method_flop = METHOD_FLOP_PER_TOKEN_HEAD * T * H
+    achieved = method_bytes / (stage_ms[dom] / 1e3) / 1e9
+    src_path = os.path.join(ROOT, "gated_delta_rule_04_gb300", "csrc", srcs[dom])
+    roofline = {"bound": "hbm", "kernel": kernels[dom], "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_kind": f"{peak_kind} copy bandwidth",
+                "traffic": ncu_traffic(kernels[dom], src_path, T * H),
+                "bytes_basis": "method bytes: raw q,k,v,z,gout + beta in, o out (bf16)"
+                               + (", S in and out (fp32)" if w.warmup_tokens is not None else ""),
+                "algorithmic_bytes_per_launch": method_bytes,
+                "bytes_per_token_head": method_bytes / (T * H), "ms_per_launch": stage_ms[dom],
+                "timing": "each kernel alone: a second timed pass of the single-pass schedule with CUDA "
+                          "events at the stage boundaries on the launching stream",
+                "single_pass_ms_per_step": r["single_ms"]}
+    step_s = r["ms_max"] / 1e3
+    step = {"ms": r["ms_max"],
+            "hbm_achieved_gbs": method_bytes / step_s / 1e9, "hbm_frac": method_bytes / step_s / 1e9 / hbm,
+            "tflops_algorithmic": method_flop / step_s / 1e12,
+            "tensor_frac": method_flop / step_s / 1e12 / tc_sus,
+            "tensor_peak_tflops": tc_sus, "tensor_peak_kind": f"{peak_kind} bf16 dense, sustained",
+            "flop_per_token_head": METHOD_FLOP_PER_TOKEN_HEAD,
+            "bytes_per_token_head": method_bytes / (T * H),
+            "tensor_cap_at_hbm_peak": (METHOD_FLOP_PER_TOKEN_HEAD / (method_bytes / (T * H))) * hbm / 1e3 / tc_sus}
+    kern = {}
+    for i, nm in enumerate(stage_names):
+        if stage_ms[i] <= 0 or (i < 4 and own[i] == 0 and i != dom):
+            continue
+        k = {"ms": stage_ms[i], "share": stage_ms[i] / max(r["single_ms"], 1e-9)}
+        if own[i]:
+            k.update({"own_bytes_per_token_head": own[i] / (T * H),
+                      "own_bytes_frac_of_hbm": own[i] / (stage_ms[i] / 1e3) / 1e9 / hbm})
+        kern[kernels[i]] = k
+    return {"roofline": roofline, "step": step, "kernels": kern}
+
+
+def other_workload(args, dev, world, rank, idx, hbm, tc, tc_sus, peak_kind):
+    """A sub-line for another prefill workload: its own value, step and roofline."""
+    r = prefill_arm(args, dev, world, rank, idx=idx, heads=kda_synth.WORKLOADS[idx]["H"],
+                    steps=max(args.steps, 20))
+    w = r["w"]
+    rep = prefill_report(r, hbm, tc, tc_sus, peak_kind)
+    return {"workload": kda_synth.describe(w.idx, w.H) + ", fp32 state", "metric": "KDA tokens/s/layer",
+            "value": whole_job_value(w.total_tokens, r["ms_max"], world), "unit": "tokens/s/layer",
+            "ms_per_step": r["ms_max"], "steps": max(args.steps, 20), "algo": r["algo_resolved"],
+            "schedule": ("single pass" if r["windows"] == 1 else f"{r['windows']} overlapped windows"),
+            "step": rep["step"], "roofline": rep["roofline"], "kernels": rep["kernels"],
+            "clocks": r["clocks"], "workspace_status": r["ws_status"]}, r["launches"]
+
+
 # ------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -446,6 +536,8 @@ def main():
     ap.add_argument("--segment", type=int, default=2048,
                     help="tokens per segment of the host-buffer (e2e) prefill")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-other", action="store_true",
+                    help="skip the sub-lines of the other prefill workloads (T=4096 H=32; varlen H=64)")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
     world, rank, local = dist_info()
@@ -468,36 +560,8 @@ def main():
     w = r["w"]
     H, T = w.H, w.total_tokens
     value = whole_job_value(T, r["ms_max"], world)
-
-    # roofline of the dominant kernel (largest share of the step)
-    chunked = r["algo_resolved"] == "chunked"
-    stage_names = ["prestage", "chunk_prep", "recurrence", "epilogue", "ring"]
-    kernels = ["prestage_kernel", "chunk_prep_kernel", "chunk_recurrence_kernel" if chunked else "scan_kernel",
-               "epilogue_kernel", "ring_update_kernel"]
-    srcs = ["kda_prestage.cu", "kda_chunk_prep.cu", "kda_chunk.cu" if chunked else "kda_scan.cu",
-            "kda_epilogue.cu", "kda_prestage.cu"]
-    state_bytes = 2 * D * D * 4 * w.n_seqs * H  # S read + written once per (sequence, head)
-    per_launch = [0 if chunked else prestage_bytes_per_token_head(2, 4) * T * H,
-                  prep_bytes_per_token_head(2) * T * H if chunked else 0,
-                  (chunk_recurrence_bytes_per_token_head(2) if chunked else scan_bytes_per_token_head()) * T * H
-                  + state_bytes,
-                  0 if chunked else epilogue_bytes_per_token_head(2) * T * H, 0]
-    stage_ms = r["stage_ms"]
-    dom = max(range(4), key=lambda i: stage_ms[i])
-    alg_bytes = per_launch[dom]
-    achieved = alg_bytes / (stage_ms[dom] / 1e3) / 1e9
-    src_path = os.path.join(ROOT, "gated_delta_rule_04_gb300", "csrc", srcs[dom])
-    roofline = {"bound": "hbm", "kernel": kernels[dom], "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "peak_kind": f"{peak_kind} copy bandwidth",
-                "traffic": ncu_traffic(kernels[dom], src_path, T * H),
-                "algorithmic_bytes_per_launch": alg_bytes,
-                "bytes_per_token_head": alg_bytes / (T * H), "ms_per_launch": stage_ms[dom],
-                "stage_ms": dict(zip(stage_names, stage_ms)),
-                "stage_frac_of_hbm": {n: (b / (ms / 1e3) / 1e9 / hbm if ms > 0 and b else None)
-                                      for n, b, ms in zip(stage_names, per_launch, stage_ms)},
-                "timing": "each kernel alone: a second timed pass of the single-pass schedule with CUDA "
-                          "events at the stage boundaries on the launching stream",
-                "single_pass_ms_per_step": r["single_ms"]}
+    rep = prefill_report(r, hbm, tc, tc_sus, peak_kind)
+    roofline = rep["roofline"]
 
     line = {
         "metric": "KDA tokens/s/layer (chunked prefill)", "value": value, "unit": "tokens/s/layer",
@@ -511,10 +575,18 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": f"inputs ({sum(t.numel() * t.element_size() for t in w.tokens.fields()) / 1e9:.2f} GB) larger than L2 (129 MB); no flush"},
         "roofline": roofline,
+        "step": rep["step"],
+        "kernels": rep["kernels"],
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
         "workspace_status": r["ws_status"],
     }
+    if not args.no_other and args.heads is None and args.workload == "long":
+        # the other prefill workloads, each with its own value and fractions
+        line["other_prefill"] = {}
+        for name, idx in (("prefill", 2), ("varlen", 4)):
+            sub, launches = other_workload(args, dev, world, rank, idx, hbm, tc, tc_sus, peak_kind)
+            line["other_prefill"][name] = sub
     if not args.no_decode:
         dr = decode_arm(args, dev)
         gbs = dr["bytes"] / (dr["ms"] / 1e3) / 1e9

@@ -239,7 +239,7 @@ bool plan_overlap(const kda_params* p, int64_t T, size_t ws_bytes, OverlapPlan* 
 // other's events; calls from one thread are ordered by the events themselves.
 struct WindowStreams {
     cudaStream_t sr = nullptr;
-    cudaEvent_t ev[6] = {};
+    cudaEvent_t ev[7] = {};
 };
 WindowStreams* window_streams() {
     thread_local std::vector<WindowStreams> per_device;
@@ -289,7 +289,7 @@ kda_status prefill_overlapped(const kda_params* p, const void* q, const void* k,
     WindowStreams* res = window_streams();
     if (res == nullptr) return KDA_ERR_CUDA;
     cudaStream_t sr = res->sr;
-    cudaEvent_t* ev = res->ev;   // start, prep part 1 [2], recurrence [2], end
+    cudaEvent_t* ev = res->ev;   // start, prep part 1 [2], recurrence [2], end, counter reset
     kda_status st = KDA_OK;
     auto ok = [&](cudaError_t e) { if (e != cudaSuccess) st = KDA_ERR_CUDA; return st == KDA_OK; };
     if (st == KDA_OK && ok(cudaEventRecord(ev[0], s)) && ok(cudaStreamWaitEvent(sr, ev[0], 0)) &&
@@ -310,6 +310,8 @@ kda_status prefill_overlapped(const kda_params* p, const void* q, const void* k,
             // records and counter of window w - 2 (same parity) are no longer in use
             if (w >= 2 && !ok(cudaStreamWaitEvent(s, ev[3 + r], 0))) break;
             if (!ok(cudaMemsetAsync(counter, 0, sizeof(int32_t), s))) break;
+            // part 2 (on sr) takes items from this counter: it starts after the reset
+            if (w > 0 && (!ok(cudaEventRecord(ev[6], s)) || !ok(cudaStreamWaitEvent(sr, ev[6], 0)))) break;
             PrepArgs pr{q, k, v, z, b, ring_in, p->conv_w, p->A_log, p->dt_bias, p->gate_lower_bound, p->l2_eps, qs,
                         reinterpret_cast<const ChunkDesc*>(mw + 4 * sizeof(int64_t)), (int32_t)nck, H, T, rec, status,
                         counter, batch, {}, {}};

@@ -143,7 +143,7 @@ kda_status kda_prefill(const kda_params* p,
  * chunks of at least 1024 tokens (up to 64 heads) or 8192 tokens each, the
  * last shorter by the rounding to chunks.  Window w's chunk preparation
  * overlaps the recurrence of window w - 1 on a second, high-priority stream,
- * and the result is bit-identical to the single pass.  That stream and six
+ * and the result is bit-identical to the single pass.  That stream and seven
  * events are created on a host thread's first windowed call on a device and
  * kept for the thread's lifetime (one set per thread and device, never
  * shared between threads).  The query

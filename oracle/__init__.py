@@ -209,3 +209,29 @@ def rmsnorm_gated(x, gate, w, num_heads, eps=1e-5):
     o = np.zeros_like(x)
     _load().kdao_rmsnorm_gated(rows, num_heads, D, eps, _ptr(x), _ptr(gate), _ptr(w), _ptr(o))
     return o
+
+
+def run_synth(p, tokens, cu, S_in=None, ring_in=None, heads=None, intermediates=False, nthreads=None):
+    """``mixer`` on the seeded inputs of ``kda_synth`` (a ``kda_synth.Params``
+    and ``kda_synth.Tokens``, torch tensors on any device), on all heads or on
+    the subset ``heads`` (heads are independent).  S_in / ring_in are the
+    full-width tensors or None.  Marshalling only: every step of the
+    arithmetic is in ``mixer``."""
+    import torch
+
+    def arr(t):
+        return None if t is None else t.detach().to("cpu").double().numpy()
+
+    if heads is not None:
+        p = p.head_slice(heads)
+        tokens = tokens.head_slice(heads)
+        idx = torch.tensor(heads, dtype=torch.long)
+        if S_in is not None:
+            S_in = S_in[:, idx.to(S_in.device)]
+        if ring_in is not None:
+            ch = (idx[:, None] * p.head_dim + torch.arange(p.head_dim)[None, :]).reshape(-1).to(ring_in.device)
+            ring_in = ring_in[..., ch]
+    op = Params(p.num_heads, p.head_dim, arr(p.conv_w), arr(p.A_log), arr(p.dt_bias), arr(p.norm_w),
+                p.gate_lower_bound, p.l2_eps, p.norm_eps, p.q_scale, p.gate_kind)
+    return mixer(op, cu, *[arr(t) for t in tokens.fields()], S_in=arr(S_in), ring_in=arr(ring_in),
+                 intermediates=intermediates, nthreads=nthreads)

@@ -34,13 +34,6 @@ def assert_close(name, got, want, tol):
     return r
 
 
-def oracle_params(p: kda_synth.Params) -> oracle.Params:
-    return oracle.Params(p.num_heads, p.head_dim, p.conv_w.double().cpu().numpy(),
-                         p.A_log.double().cpu().numpy(), p.dt_bias.double().cpu().numpy(),
-                         p.norm_w.double().cpu().numpy(), p.gate_lower_bound, p.l2_eps, p.norm_eps,
-                         p.q_scale, p.gate_kind)
-
-
 def kda_params(p: kda_synth.Params, io: str, algo: str = "auto", device="cuda"):
     import gated_delta_rule_04_gb300 as kda
     return kda.make_params(p.conv_w.to(device), p.A_log.to(device), p.dt_bias.to(device),
@@ -50,25 +43,12 @@ def kda_params(p: kda_synth.Params, io: str, algo: str = "auto", device="cuda"):
                            gate=("bounded", "softplus")[p.gate_kind])
 
 
-def to_np(t):
-    return None if t is None else t.double().cpu().numpy()
-
-
 def oracle_run(p: kda_synth.Params, tokens: kda_synth.Tokens, cu, S_in=None, ring_in=None,
                heads=None, intermediates=False):
     """Oracle on all heads, or on the subset ``heads`` (heads are independent).
     S_in / ring_in are full-width tensors (or None)."""
-    if heads is not None:
-        p = p.head_slice(heads)
-        tokens = tokens.head_slice(heads)
-        idx = torch.tensor(heads, dtype=torch.long)
-        if S_in is not None:
-            S_in = S_in[:, idx.to(S_in.device)]
-        if ring_in is not None:
-            ch = (idx[:, None] * 128 + torch.arange(128)[None, :]).reshape(-1).to(ring_in.device)
-            ring_in = ring_in[..., ch]
-    return oracle.mixer(oracle_params(p), cu, *[to_np(t) for t in tokens.fields()],
-                        S_in=to_np(S_in), ring_in=to_np(ring_in), intermediates=intermediates)
+    return oracle.run_synth(p, tokens, cu, S_in=S_in, ring_in=ring_in, heads=heads,
+                            intermediates=intermediates)
 
 
 def head_cols(heads):
