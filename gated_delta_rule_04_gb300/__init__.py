@@ -56,6 +56,7 @@ class kda_params(ctypes.Structure):
         ("dt_bias", _vp),
         ("norm_w", _vp),
         ("gate_kind", ctypes.c_int32),
+        ("wait_limit_us", ctypes.c_uint32),
     ]
 
 
@@ -140,15 +141,16 @@ _GATES = {"bounded": KDA_GATE_BOUNDED, "softplus": KDA_GATE_SOFTPLUS}
 
 def make_params(conv_w, A_log, dt_bias, norm_w, *, io_dtype: str = "bf16", algo: str = "auto",
                 gate_lower_bound: float = -5.0, l2_eps: float = 1e-6, norm_eps: float = 1e-5,
-                q_scale: float = 0.0, gate: str = "bounded") -> Params:
+                q_scale: float = 0.0, gate: str = "bounded", wait_limit_us: int = 0) -> Params:
     """conv_w [3][H*128][4], A_log [H], dt_bias [H*128], norm_w [128]: fp32 CUDA tensors.
     gate: "bounded" (g = lb sigmoid(e^A (z + dt_bias))) or "softplus"
-    (g = -e^A softplus(z + dt_bias), unbounded below)."""
+    (g = -e^A softplus(z + dt_bias), unbounded below).  wait_limit_us: the
+    test hook of kda_params (0 in normal use)."""
     H = int(A_log.shape[0])
     dt = {"f32": KDA_DTYPE_F32, "bf16": KDA_DTYPE_BF16}[io_dtype]
     tensors = tuple(t.contiguous() for t in (conv_w, A_log, dt_bias, norm_w))
     st = kda_params(H, 128, 4, dt, _ALGOS[algo], gate_lower_bound, l2_eps, norm_eps, q_scale,
-                    *[t.data_ptr() for t in tensors], _GATES[gate])
+                    *[t.data_ptr() for t in tensors], _GATES[gate], int(wait_limit_us))
     return Params(st, tensors, H, dt)
 
 

@@ -314,7 +314,7 @@ kda_status prefill_overlapped(const kda_params* p, const void* q, const void* k,
             if (w > 0 && (!ok(cudaEventRecord(ev[6], s)) || !ok(cudaStreamWaitEvent(sr, ev[6], 0)))) break;
             PrepArgs pr{q, k, v, z, b, ring_in, p->conv_w, p->A_log, p->dt_bias, p->gate_lower_bound, p->l2_eps, qs,
                         reinterpret_cast<const ChunkDesc*>(mw + 4 * sizeof(int64_t)), (int32_t)nck, H, T, rec, status,
-                        counter, batch, {}, {}};
+                        counter, batch, prep_wait_limit_ns(p), {}, {}};
             // part 1 alongside the recurrence of window w - 1 (all SMs for window 0)
             if (!ok(launch_chunk_prep(pr, s, w == 0 ? 0 : pl.sms - H)) || !ok(cudaEventRecord(ev[1 + r], s))) break;
             // part 2 on the SMs that recurrence frees
@@ -438,7 +438,7 @@ kda_status prefill_run(const kda_params* p, const void* q, const void* k, const 
         if (mark(ev, 1, s) != cudaSuccess) return KDA_ERR_CUDA;
         PrepArgs pr{q, k, v, z, b, ring_in, p->conv_w, p->A_log, p->dt_bias, p->gate_lower_bound, p->l2_eps, qs,
                     d_chunks, (int32_t)n_chunks, H, total_tokens, ws + L.rec, reinterpret_cast<int32_t*>(ws + L.status), nullptr,
-                    PREP_BATCH, {}, {}};
+                    PREP_BATCH, prep_wait_limit_ns(p), {}, {}};
         e = launch_chunk_prep(pr, s);
         if (e != cudaSuccess || mark(ev, 2, s) != cudaSuccess) return KDA_ERR_CUDA;
         // the recurrence kernel applies the output norm itself

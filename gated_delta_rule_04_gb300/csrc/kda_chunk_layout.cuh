@@ -56,11 +56,16 @@ struct PrepArgs {
     // hold their SMs) take fewer.
     int32_t* work_counter;
     int32_t batch;
+    // Limit of the waits between the kernel's two warp groups, in ns (0: the
+    // default 2 s).  The drain after a timeout always uses the default.
+    uint64_t wait_limit_ns;
     // set by launch_chunk_prep: TMA descriptors of q, k, v as [T][H*128] bf16
     // with a 67-row box (a chunk and the three rows before it) and a 64-row box
     CUtensorMap map67[3], map64[3];
 };
 constexpr int PREP_BATCH = 4;        // most items per take from PrepArgs::work_counter
+// PrepArgs::wait_limit_ns from the parameters' test hook (0: the default)
+inline uint64_t prep_wait_limit_ns(const kda_params* p) { return (uint64_t)p->wait_limit_us * 1000ull; }
 // max_ctas > 0 caps the persistent grid (for a launch that shares the GPU).
 cudaError_t launch_chunk_prep(const PrepArgs& a, cudaStream_t s, int max_ctas = 0);
 size_t chunk_prep_smem_bytes();

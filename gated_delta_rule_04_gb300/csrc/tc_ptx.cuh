@@ -38,6 +38,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// The same test, but a thread whose phase is not yet complete is suspended
+// until it completes or about `hint_ns` pass, instead of returning at once: a
+// waiting thread then takes no issue slots from the warps doing work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for phase `parity` of the barrier for at most `limit_ns`; returns
 // false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -64,6 +79,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
         ::"r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+// Prefetch of one 2-D tensor box (as tma_load_2d would fetch it) into L2; no
+// completion tracking.
+__device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
+                 : "memory");
 }
 
 // Bulk copy shared -> global, tracked as a bulk async-group of the issuing thread.
@@ -95,6 +117,19 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
 // async-proxy (tensor core, bulk copy) accesses.
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Named barrier over `count` threads that also ORs a predicate across them:
+// every participant gets the same result.
+__device__ __forceinline__ bool bar_sync_or(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+        " bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
 }
 
 // ---- TMEM allocation ---------------------------------------------------------

@@ -95,6 +95,14 @@ typedef struct {
     const float* dt_bias;   /* device [H*128] fp32 */
     const float* norm_w;    /* device [128] fp32, shared by all heads */
     int32_t gate_kind;      /* kda_gate */
+    /* Test hook, 0 in normal use.  Every in-kernel wait gives up after 2 s
+     * (the call then reports KDA_ERR_TIMEOUT through kda_workspace_status).
+     * A nonzero value shortens the waits between the chunk preparation's two
+     * warp groups to that many microseconds, so that a test can make a
+     * bounded wait run out on demand; the waits that let the kernel's own
+     * copies and tensor-core work finish before it frees its resources keep
+     * the 2 s limit. */
+    uint32_t wait_limit_us;
 } kda_params;
 
 /* The prefill algorithm (KDA_ALGO_SCAN or KDA_ALGO_CHUNKED) that kda_prefill
