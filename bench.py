@@ -305,9 +305,10 @@ def prefill_arm(args, dev, world, rank, idx=None, heads=None, steps=None):
     ws_status = kda.kda_workspace_status(ws, stream)
     algo = kda.kda_prefill_algo(kp)
     windows = kda.kda_prefill_windows(kp, n, T, ws_bytes)
-    # chunked single pass: prep, recurrence, ring; windows: a prep part per window (two from the
-    # second on), a recurrence per window and the ring; scan: pre-stage, scan, epilogue, ring
-    per_step = (3 if windows == 1 else 3 * windows) if algo == "chunked" else 4
+    # chunked single pass: metadata, prep, recurrence, ring; windows: the windows' metadata, a prep
+    # part per window (two from the second on), a recurrence per window and the ring; scan:
+    # metadata, pre-stage, scan, epilogue, ring
+    per_step = (4 if windows == 1 else 3 * windows + 1) if algo == "chunked" else 5
     return dict(w=w, ms=ms, ms_max=ms_max, stage_ms=stage_ms, single_ms=single_ms, windows=windows,
                 clocks=clk.summary(), kp=kp, launches=per_step * steps, ws_status=ws_status,
                 algo_resolved=algo)

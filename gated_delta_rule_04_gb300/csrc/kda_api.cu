@@ -241,8 +241,26 @@ struct WindowStreams {
     cudaStream_t sr = nullptr;
     cudaEvent_t ev[7] = {};
 };
+// A thread's window streams and events, released when the thread exits (while
+// the runtime is still usable: at process exit it may already be unloading).
+struct ThreadWindowStreams {
+    std::vector<WindowStreams> per_device;
+    ~ThreadWindowStreams() {
+        int prev = -1;
+        if (cudaGetDevice(&prev) != cudaSuccess) return;
+        for (size_t d = 0; d < per_device.size(); ++d) {
+            WindowStreams& w = per_device[d];
+            if (w.sr == nullptr || cudaSetDevice((int)d) != cudaSuccess) continue;
+            for (auto& e : w.ev)
+                if (e) cudaEventDestroy(e);
+            cudaStreamDestroy(w.sr);
+        }
+        cudaSetDevice(prev);
+    }
+};
 WindowStreams* window_streams() {
-    thread_local std::vector<WindowStreams> per_device;
+    thread_local ThreadWindowStreams tws;
+    std::vector<WindowStreams>& per_device = tws.per_device;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
     if ((size_t)dev >= per_device.size()) per_device.resize(dev + 1);
@@ -269,20 +287,6 @@ kda_status prefill_overlapped(const kda_params* p, const void* q, const void* k,
                               const void* ring_in, void* ring_out, void* o, unsigned char* ws, cudaStream_t s,
                               const OverlapPlan& pl, bool reset_status) {
     const int H = p->num_heads, W = H * D;
-    // every window's cu, chunk offsets and chunk table, one upload
-    std::vector<unsigned char> meta(pl.meta_stride * pl.S, 0);
-    for (int w = 0; w < pl.S; ++w) {
-        const int64_t t0 = w * pl.seg, t1 = std::min(T, t0 + pl.seg);
-        const int64_t nck = (t1 - t0 + CHUNK - 1) / CHUNK;
-        int64_t* m = reinterpret_cast<int64_t*>(meta.data() + w * pl.meta_stride);
-        m[0] = t0; m[1] = t1; m[2] = 0; m[3] = nck;
-        ChunkDesc* cd = reinterpret_cast<ChunkDesc*>(m + 4);
-        for (int64_t i = 0; i < nck; ++i) {
-            const int64_t t = t0 + CHUNK * i;
-            cd[i] = ChunkDesc{0, (int32_t)t, (int32_t)std::min<int64_t>(CHUNK, t1 - t), (int32_t)t};
-        }
-    }
-    const int64_t cufull[2] = {0, T};
     int32_t* status = reinterpret_cast<int32_t*>(ws);
     int32_t* counters = reinterpret_cast<int32_t*>(ws + WS_COUNTER);   // [2], by window parity
 
@@ -294,8 +298,9 @@ kda_status prefill_overlapped(const kda_params* p, const void* q, const void* k,
     auto ok = [&](cudaError_t e) { if (e != cudaSuccess) st = KDA_ERR_CUDA; return st == KDA_OK; };
     if (st == KDA_OK && ok(cudaEventRecord(ev[0], s)) && ok(cudaStreamWaitEvent(sr, ev[0], 0)) &&
         ok(reset_status ? cudaMemsetAsync(ws, 0, WS_ALIGN, s) : cudaSuccess) &&
-        ok(cudaMemcpyAsync(ws + pl.off_meta, meta.data(), meta.size(), cudaMemcpyHostToDevice, s)) &&
-        ok(cudaMemcpyAsync(ws + pl.off_cufull, cufull, sizeof(cufull), cudaMemcpyHostToDevice, s))) {
+        // every window's cu, chunk offsets and chunk table, built on the device
+        ok(launch_build_window_meta(T, pl.seg, pl.S, (int64_t)pl.meta_stride, ws + pl.off_meta,
+                                    reinterpret_cast<int64_t*>(ws + pl.off_cufull), s))) {
         const float qs = resolved_q_scale(p);
         // items per take: batches of PREP_BATCH amortise the counter, but a
         // window with few items per SM balances better one item at a time
@@ -385,24 +390,10 @@ kda_status prefill_run(const kda_params* p, const void* q, const void* k, const 
     const int H = p->num_heads, W = H * D;
     const int io_bf16 = p->io_dtype == KDA_DTYPE_BF16;
 
-    // host-built metadata, one upload
-    std::vector<unsigned char> meta(L.meta_bytes, 0);
-    memcpy(meta.data(), cu_seqlens_host, sizeof(int64_t) * (size_t)(n_seqs + 1));
-    int64_t* coff = reinterpret_cast<int64_t*>(meta.data() + L.off_chunk_off);
-    int32_t* order = reinterpret_cast<int32_t*>(meta.data() + L.off_order);
-    ChunkDesc* cds = reinterpret_cast<ChunkDesc*>(meta.data() + L.off_chunks);
-    int64_t ci = 0;
-    for (int32_t n = 0; n < n_seqs; ++n) {
-        coff[n] = ci;
-        for (int64_t t = cu_seqlens_host[n]; t < cu_seqlens_host[n + 1]; t += CHUNK) {
-            const int64_t len = cu_seqlens_host[n + 1] - t < CHUNK ? cu_seqlens_host[n + 1] - t : CHUNK;
-            cds[ci++] = ChunkDesc{n, (int32_t)t, (int32_t)len, (int32_t)(t - cu_seqlens_host[n])};
-        }
-    }
-    coff[n_seqs] = ci;
     // longest sequences first, so the sequential chunk walks start early
-    std::iota(order, order + n_seqs, 0);
-    std::stable_sort(order, order + n_seqs, [&](int32_t x, int32_t y) {
+    std::vector<int32_t> order(n_seqs);
+    std::iota(order.begin(), order.end(), 0);
+    std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) {
         return cu_seqlens_host[x + 1] - cu_seqlens_host[x] > cu_seqlens_host[y + 1] - cu_seqlens_host[y];
     });
     const int64_t* d_cu = reinterpret_cast<const int64_t*>(ws + L.meta);
@@ -413,7 +404,10 @@ kda_status prefill_run(const kda_params* p, const void* q, const void* k, const 
     // the whole segmented call when the caller clears it once)
     cudaError_t e = reset_status ? cudaMemsetAsync(ws + L.status, 0, WS_ALIGN, s) : cudaSuccess;
     if (e != cudaSuccess) return KDA_ERR_CUDA;
-    e = cudaMemcpyAsync(ws + L.meta, meta.data(), L.meta_bytes, cudaMemcpyHostToDevice, s);
+    // cu_seqlens, chunk offsets, order and chunk table, built on the device from
+    // kernel arguments (no copy from pageable host memory)
+    e = build_meta(cu_seqlens_host, order.data(), n_seqs, 0, const_cast<int64_t*>(d_cu), const_cast<int64_t*>(d_coff),
+                   const_cast<int32_t*>(d_order), const_cast<ChunkDesc*>(d_chunks), s);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
 
     if (mark(ev, 0, s) != cudaSuccess) return KDA_ERR_CUDA;
@@ -529,9 +523,7 @@ kda_status kda_workspace_status(void* workspace, void* stream_) {
         return KDA_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
     if (word == ERR_NONE) return KDA_OK;
-    const int32_t zero = 0;
-    if (cudaMemcpyAsync(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaStreamSynchronize(s) != cudaSuccess)
+    if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
         return KDA_ERR_CUDA;
     return word == ERR_TIMEOUT ? KDA_ERR_TIMEOUT : KDA_ERR_CUDA;
 }

@@ -1041,6 +1041,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         if (*raw_issued > *raw_seen) ptx::mbar_wait(bar_raw, (uint32_t)*raw_seen & 1u, WAIT_LIMIT_NS);
     }
     if (warp == 0) {
+        __syncwarp();   // (thread 0 may have waited above; the dealloc is warp-collective)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
     }

@@ -210,6 +210,35 @@ struct DecodeArgs {
 };
 cudaError_t launch_decode(const DecodeArgs& a, int io_bf16, cudaStream_t s);
 
+// Prefill metadata built on the device from values passed as kernel
+// arguments (no host-to-device copy): for a slice of up to META_SEQS sequences
+// seq0 .. seq0 + n - 1, their token offsets, first chunk index, order entry and
+// the ChunkDesc of each 64-token chunk.  pos_base is added to every chunk's
+// position in its sequence (the start of a window inside one sequence).  Any
+// output pointer may be null to skip it; `tail` also writes the entries of
+// index seq0 + n of cu and chunk_off.
+constexpr int META_SEQS = 1024;
+struct MetaSlice {
+    int64_t cu[META_SEQS + 1];
+    int32_t order[META_SEQS];
+    int32_t n, seq0, tail;
+    int64_t chunk0, pos_base;
+    int64_t* d_cu;
+    int64_t* d_coff;
+    int32_t* d_order;
+    ChunkDesc* d_chunks;
+};
+cudaError_t launch_build_meta(const MetaSlice& m, cudaStream_t s);
+// The whole table for n sequences with host offsets cu[0..n] (cu[0] may be
+// nonzero) and an optional host order[n], in slices of META_SEQS.
+cudaError_t build_meta(const int64_t* cu, const int32_t* order, int32_t n, int64_t pos_base, int64_t* d_cu,
+                       int64_t* d_coff, int32_t* d_order, ChunkDesc* d_chunks, cudaStream_t s);
+
+// The metadata of the overlapped windows of one T-token sequence (S windows of
+// `seg` tokens, blocks of `stride` bytes at `meta`) and the sequence's cu {0, T}.
+cudaError_t launch_build_window_meta(int64_t T, int64_t seg, int32_t S, int64_t stride, unsigned char* meta,
+                                     int64_t* cufull, cudaStream_t s);
+
 // The parameter checks of kda_prefill: KDA_OK or the status it would return.
 kda_status prefill_check(const kda_params* p);
 

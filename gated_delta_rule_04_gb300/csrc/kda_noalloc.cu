@@ -10,9 +10,10 @@
 // GPU which loads this library holds until the process exits.  It calls no
 // memory-allocating routine, on the device or on the host.
 //
-// Set-up: the first call on each device looks up the array's device address
-// with cudaGetSymbolAddress (with that device current) and caches it; make
-// that first call before any stream capture.
+// Set-up: the first call in each CUDA context (one per device for runtime-API
+// callers) looks up the array's device address with cudaGetSymbolAddress,
+// with that device current, and caches it with the context it belongs to;
+// make that first call before any stream capture.
 // Sharing: every call uses the same array and leaves its contents behind.
 // The only part that must start at zero (the error word) is cleared by each
 // call; every other byte is written before it is read.  Calls whose work can
@@ -20,7 +21,7 @@
 // race on the array: order them on one stream.
 #include <string.h>
 
-#include <atomic>
+#include <mutex>
 
 #include "kda_chunk_layout.cuh"
 
@@ -30,14 +31,33 @@ namespace {
 constexpr size_t NA_ALIGN = 256;
 constexpr int NA_CHUNK = CHUNK_T;
 constexpr int NA_MAX_DEVICES = 64;
-constexpr int NA_MAX_SEQS = 512;           // sequences per call
-constexpr size_t NA_META_MAX = 32768;      // host-side metadata built on the stack
+constexpr int NA_MAX_SEQS = 512;           // sequences per call (their order is sorted on the stack)
 
 // The scratch array.  In host code this name is only a handle for
 // cudaGetSymbolAddress, never an address to pass to a kernel.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
 
-std::atomic<void*> g_scratch_addr[NA_MAX_DEVICES];
+// The cached address per device, with the context it was looked up in: a
+// cudaDeviceReset (or another context on the device) invalidates it.
+struct ScratchSlot {
+    void* ctx;
+    void* addr;
+};
+ScratchSlot g_scratch[NA_MAX_DEVICES];
+std::mutex g_scratch_mu;
+
+typedef int (*CtxGetCurrentFn)(void**);   // CUresult cuCtxGetCurrent(CUcontext*)
+CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<CtxGetCurrentFn>(nullptr);
+        return reinterpret_cast<CtxGetCurrentFn>(f);
+    }();
+    return fn;
+}
 
 size_t up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -73,19 +93,35 @@ NaLayout na_layout(int H, bool chunked, int32_t n, int64_t T, int64_t nc) {
     return L;
 }
 
-// Device address of the scratch array on the current device (set up once).
+// Device address of the scratch array in the current context (looked up once
+// per context).
 cudaError_t scratch_address(unsigned char** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= NA_MAX_DEVICES) return cudaErrorInvalidDevice;
-    void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (p == nullptr) {
+    CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+    if (get_ctx == nullptr) return cudaErrorDeviceUninitialized;
+    void* ctx = nullptr;
+    if (get_ctx(&ctx) != 0) return cudaErrorDeviceUninitialized;
+    if (ctx == nullptr) {
+        // no context current yet: the runtime's symbol lookup makes the device's
+        // primary context current
+        void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return e;
-        g_scratch_addr[dev].store(p, std::memory_order_release);
+        if (get_ctx(&ctx) != 0 || ctx == nullptr) return cudaErrorDeviceUninitialized;
     }
-    *out = static_cast<unsigned char*>(p);
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    ScratchSlot& sl = g_scratch[dev];
+    if (sl.ctx != ctx || sl.addr == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        sl.ctx = ctx;
+        sl.addr = p;
+    }
+    *out = static_cast<unsigned char*>(sl.addr);
     return cudaSuccess;
 }
 
@@ -99,14 +135,10 @@ extern "C" kda_status kda_prefill_noalloc(const kda_params* p, const void* q, co
                                           const int64_t* cu, int32_t n_seqs, int64_t total_tokens,
                                           const float* S_in, float* S_out, const void* ring_in, void* ring_out,
                                           void* o, void* stream_) {
-    // the parameter checks and the algorithm choice of kda_prefill
-    const int32_t algo = kda_prefill_algo(p);
-    if (algo < 0) {
-        if (p && (p->head_dim != D || p->conv_kernel != CONV_K)) return KDA_ERR_UNSUPPORTED;
-        if (p && p->algo == KDA_ALGO_CHUNKED) return KDA_ERR_UNSUPPORTED;
-        return KDA_ERR_INVALID_ARG;
-    }
-    const bool chunked = algo == KDA_ALGO_CHUNKED;
+    // the parameter checks and the algorithm choice of kda_prefill, with its statuses
+    const kda_status pst = prefill_check(p);
+    if (pst != KDA_OK) return pst;
+    const bool chunked = kda_prefill_algo(p) == KDA_ALGO_CHUNKED;
     if (n_seqs < 0 || total_tokens < 0 || cu == nullptr) return KDA_ERR_INVALID_ARG;
     if (cu[0] != 0 || cu[n_seqs] != total_tokens) return KDA_ERR_INVALID_ARG;
     for (int32_t i = 0; i < n_seqs; ++i)
@@ -121,36 +153,22 @@ extern "C" kda_status kda_prefill_noalloc(const kda_params* p, const void* q, co
     if (S_out == nullptr || !al16(S_out) || (S_in && !al16(S_in))) return KDA_ERR_INVALID_ARG;
     if ((ring_in && !al16(ring_in)) || (ring_out && !al16(ring_out))) return KDA_ERR_INVALID_ARG;
 
-    // size limits of the fixed scratch and of the on-stack metadata
+    // size limits of the fixed scratch and of the on-stack sequence order
     int64_t nc = 0;
     for (int32_t i = 0; i < n_seqs; ++i) nc += (cu[i + 1] - cu[i] + NA_CHUNK - 1) / NA_CHUNK;
     const int H = p->num_heads, W = H * D;
     if (n_seqs > NA_MAX_SEQS) return KDA_ERR_UNSUPPORTED;
+    if (total_tokens > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;   // (as kda_prefill)
     const NaLayout L = na_layout(H, chunked, n_seqs, total_tokens, nc);
-    if (L.meta_bytes > NA_META_MAX) return KDA_ERR_UNSUPPORTED;
     if (L.total > KDA_NOALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
 
     unsigned char* ws = nullptr;
     if (scratch_address(&ws) != cudaSuccess) return KDA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream_);
 
-    // metadata on the stack: cu_seqlens, first chunk per sequence, order, chunks
-    alignas(16) unsigned char meta[NA_META_MAX];
-    memcpy(meta, cu, sizeof(int64_t) * (size_t)(n_seqs + 1));
-    int64_t* coff = reinterpret_cast<int64_t*>(meta + L.off_coff);
-    int32_t* order = reinterpret_cast<int32_t*>(meta + L.off_order);
-    ChunkDesc* cds = reinterpret_cast<ChunkDesc*>(meta + L.off_chunks);
-    int64_t ci = 0;
-    for (int32_t n = 0; n < n_seqs; ++n) {
-        coff[n] = ci;
-        order[n] = n;
-        for (int64_t t = cu[n]; t < cu[n + 1]; t += NA_CHUNK) {
-            const int64_t len = cu[n + 1] - t < NA_CHUNK ? cu[n + 1] - t : NA_CHUNK;
-            cds[ci++] = ChunkDesc{n, (int32_t)t, (int32_t)len, (int32_t)(t - cu[n])};
-        }
-    }
-    coff[n_seqs] = ci;
-    // longest sequences first (insertion sort: stable, no allocation)
+    // longest sequences first (insertion sort on the stack: stable, no allocation)
+    int32_t order[NA_MAX_SEQS];
+    for (int32_t i = 0; i < n_seqs; ++i) order[i] = i;
     for (int32_t i = 1; i < n_seqs; ++i) {
         const int32_t x = order[i];
         const int64_t lx = cu[x + 1] - cu[x];
@@ -164,7 +182,10 @@ extern "C" kda_status kda_prefill_noalloc(const kda_params* p, const void* q, co
     const ChunkDesc* d_chunks = reinterpret_cast<const ChunkDesc*>(ws + L.meta + L.off_chunks);
     cudaError_t e = cudaMemsetAsync(ws + L.status, 0, NA_ALIGN, s);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
-    e = cudaMemcpyAsync(ws + L.meta, meta, L.meta_bytes, cudaMemcpyHostToDevice, s);
+    // cu_seqlens, chunk offsets, order and chunk table, built on the device from
+    // kernel arguments
+    e = build_meta(cu, order, n_seqs, 0, const_cast<int64_t*>(d_cu), const_cast<int64_t*>(d_coff),
+                   const_cast<int32_t*>(d_order), const_cast<ChunkDesc*>(d_chunks), s);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
 
     const int io_bf16 = p->io_dtype == KDA_DTYPE_BF16;
@@ -199,4 +220,12 @@ extern "C" kda_status kda_prefill_noalloc(const kda_params* p, const void* q, co
         if (launch_ring_update(ra, io_bf16, s) != cudaSuccess) return KDA_ERR_CUDA;
     }
     return KDA_OK;
+}
+
+// Reads (and clears) the error word of the scratch array, as kda_workspace_status
+// does for a caller's workspace.
+extern "C" kda_status kda_noalloc_status(void* stream_) {
+    unsigned char* ws = nullptr;
+    if (scratch_address(&ws) != cudaSuccess) return KDA_ERR_CUDA;
+    return kda_workspace_status(ws, stream_);
 }

@@ -25,12 +25,22 @@
  *      sigmoid gate; "ferrox-models 0.8.0, module kda", fact 2).
  *
  * Conventions shared by every entry point
- *   - The caller owns every buffer.  The library allocates no device memory,
- *     holds no global state and never synchronises: all work is ordered on
- *     `stream` (a cudaStream_t; NULL is the legacy default stream).  A call
- *     may fan work out to streams it is given or creates, and joins them back
- *     into `stream` before it returns (kda_prefill's overlapped windows,
- *     kda_prefill_host's copy streams).
+ *   - The caller owns every buffer.  The library allocates no device memory
+ *     (kda_prefill_noalloc's fixed scratch array aside) and the prefill and
+ *     decode calls never synchronise: all work is ordered on `stream` (a
+ *     cudaStream_t; NULL is the legacy default stream), and the small tables
+ *     a call needs (cu_seqlens, the chunk table) are built on the device from
+ *     kernel arguments, never copied from host memory.  A call may fan work
+ *     out to streams it is given or creates, and joins them back into
+ *     `stream` before it returns (kda_prefill's overlapped windows,
+ *     kda_prefill_host's copy streams).  kda_workspace_status and
+ *     kda_noalloc_status synchronise `stream` by design.
+ *   - The library keeps a few caches, and no other state:
+ *       per device: the SM count and kernel attributes it has set;
+ *       per host thread and device: the overlapped windows' high-priority
+ *       stream and seven events, created on the thread's first windowed call
+ *       and released when the thread exits;
+ *       per CUDA context: the address of kda_prefill_noalloc's scratch array.
  *   - Every pointer marked "device" must be a device (or managed) address
  *     aligned to 16 bytes, except b which needs only element alignment.
  *   - Token tensors are token-major: element (t, c) at t*(H*128) + c.
@@ -241,17 +251,20 @@ kda_status kda_decode_multi(const kda_params* p, int32_t n_sessions, int32_t n_t
  * device memory, or a serving loop that must not call cudaMalloc/cudaFree
  * because they can synchronise the whole device.  The sources describe no
  * counterpart; this is an interface addition of this library.
- * Same arguments and results as kda_prefill, minus the workspace.  The
+ * Same arguments, checks and results as kda_prefill, minus the workspace.  The
  * scratch is a fixed device array of KDA_NOALLOC_SCRATCH_BYTES, held by every
- * GPU that loads the library until the process exits.  The first call on a
- * device looks up that array's address (cudaGetSymbolAddress) and caches it:
- * make it before any stream capture.  Every call shares the array, so calls
- * that can overlap on the GPU race: issue them in order on one stream.
+ * GPU that loads the library until the process exits.  The first call in a
+ * CUDA context (one per device for runtime-API callers) looks up that
+ * array's address (cudaGetSymbolAddress) and caches it with the context:
+ * make that first call before any stream capture.  Every call shares the
+ * array and leaves its contents behind (each call clears the error word and
+ * writes every other byte it reads), so calls that can overlap on the GPU
+ * race: issue them in order on one stream.
  * Returns KDA_ERR_WORKSPACE when the problem needs more scratch than the
  * array holds (kda_prefill_workspace_bytes reports the need), and
- * KDA_ERR_UNSUPPORTED for more than 512 sequences in one call.  Bounded-wait
- * timeouts inside this call are not reported (the error word is private).
- * Calls no memory-allocating routine.
+ * KDA_ERR_UNSUPPORTED for more than 512 sequences in one call (their order is
+ * sorted on the host stack).  Calls no memory-allocating routine.  A
+ * bounded-wait timeout inside a call is read with kda_noalloc_status.
  */
 #define KDA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 kda_status kda_prefill_noalloc(const kda_params* p,
@@ -260,6 +273,13 @@ kda_status kda_prefill_noalloc(const kda_params* p,
                                const int64_t* cu_seqlens_host, int32_t n_seqs, int64_t total_tokens,
                                const float* S_in, float* S_out,
                                const void* ring_in, void* ring_out, void* o, void* stream);
+
+/* Synchronises `stream` and reads the error word in kda_prefill_noalloc's
+ * scratch array on the current device: KDA_OK, or KDA_ERR_TIMEOUT when a
+ * bounded in-kernel wait gave up in an earlier call (the word is then
+ * cleared).  Like kda_prefill_noalloc, allocates nothing.  No counterpart in
+ * the sources. */
+kda_status kda_noalloc_status(void* stream);
 
 /*
  * Prefill of a packed batch held in HOST memory, with the host<->device

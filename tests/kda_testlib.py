@@ -34,13 +34,13 @@ def assert_close(name, got, want, tol):
     return r
 
 
-def kda_params(p: kda_synth.Params, io: str, algo: str = "auto", device="cuda"):
+def kda_params(p: kda_synth.Params, io: str, algo: str = "auto", device="cuda", wait_limit_us: int = 0):
     import gated_delta_rule_04_gb300 as kda
     return kda.make_params(p.conv_w.to(device), p.A_log.to(device), p.dt_bias.to(device),
                            p.norm_w.to(device), io_dtype=io, algo=algo,
                            gate_lower_bound=p.gate_lower_bound, l2_eps=p.l2_eps,
                            norm_eps=p.norm_eps, q_scale=p.q_scale,
-                           gate=("bounded", "softplus")[p.gate_kind])
+                           gate=("bounded", "softplus")[p.gate_kind], wait_limit_us=wait_limit_us)
 
 
 def oracle_run(p: kda_synth.Params, tokens: kda_synth.Tokens, cu, S_in=None, ring_in=None,

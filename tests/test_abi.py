@@ -301,3 +301,43 @@ def test_workspace_covers_overlapped_windows(L, T, H):
         assert need >= 2 * seg_chunks * H * rec
     # and never less than the single pass needs for several sequences' worth of chunks
     assert need >= (T // 64 + 1) * H * rec
+
+
+def noalloc(L, p, cu, T=None, **ptrs):
+    f = L.kda_prefill_noalloc
+    arr = (ctypes.c_int64 * len(cu))(*cu)
+    n = len(cu) - 1
+    T = cu[-1] if T is None else T
+    a = dict(q=FAKE, k=FAKE, v=FAKE, z=FAKE, b=FAKE, gout=FAKE, S_in=None, S_out=FAKE,
+             ring_in=None, ring_out=FAKE, o=FAKE)
+    a.update(ptrs)
+    f.restype = ctypes.c_int
+    return f(ctypes.byref(p), *[ctypes.c_void_p(a[x]) if a[x] else None for x in ("q", "k", "v", "z", "b", "gout")],
+             arr, ctypes.c_int32(n), ctypes.c_int64(T),
+             *[ctypes.c_void_p(a[x]) if a[x] else None for x in ("S_in", "S_out", "ring_in", "ring_out", "o")],
+             None)
+
+
+@pytest.mark.parametrize("kw, cu", [
+    (dict(head_dim=64), [0, 64]),
+    (dict(conv_w=0, algo=kda.KDA_ALGO_CHUNKED), [0, 64]),
+    (dict(num_heads=0, head_dim=96), [0, 64]),
+    (dict(gate_kind=1, algo=kda.KDA_ALGO_CHUNKED), [0, 64]),
+    (dict(l2_eps=-1.0), [0, 64]),
+    (dict(), [0, 70, 60]),
+    (dict(), [1, 64]),
+])
+def test_noalloc_rejects_exactly_as_kda_prefill(L, kw, cu):
+    """The no-allocation entry point runs kda_prefill's checks and returns the
+    same status for every rejected argument set (no kernel runs)."""
+    p = params(**kw)
+    want = prefill(L, p, cu)
+    assert want != kda.KDA_OK
+    assert noalloc(L, p, cu) == want
+
+
+def test_noalloc_rejects_more_than_512_sequences(L):
+    """The sequence order is sorted on the host stack, so one call takes at
+    most 512 sequences; the check runs before anything is enqueued."""
+    cu = list(range(0, 514))   # 513 one-token sequences
+    assert noalloc(L, params(), cu) == kda.KDA_ERR_UNSUPPORTED

@@ -5,7 +5,9 @@ because they can synchronise the whole device).
 
 The entry point is called through the C ABI and must give the same results
 as kda_prefill, within the tolerances of the other parity tests, on two calls
-in a row (the second sees the scratch the first one left behind).
+in a row (the second sees the scratch the first one left behind), and match
+the fp64 oracle by itself.  A bounded-wait timeout inside it is read back with
+kda_noalloc_status.
 
 This file is collected last, so a run that stops at the first failure has
 already run every other test; it also passes on its own in a fresh process.
@@ -18,7 +20,7 @@ import torch
 
 import gated_delta_rule_04_gb300 as kda
 import kda_synth
-from kda_testlib import assert_close, kda_params, tol_for
+from kda_testlib import assert_close, kda_params, oracle_run, tol_for
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -74,6 +76,12 @@ def test_noalloc_matches_kda_prefill_twice(io, algo):
         assert_close(f"call {call} o", o, o_ref.double().cpu().numpy(), tol)
         assert_close(f"call {call} S", S, S_ref.double().cpu().numpy(), tol)
         assert torch.equal(ring, ring_ref)
+        # and against the oracle, independently of kda_prefill
+        ref = oracle_run(p, kda_synth.Tokens(*[t.cpu() for t in tk]), cu,
+                         S_in=None if S_in is None else S_in.cpu(), ring_in=None if ring_in is None else ring_in.cpu())
+        assert_close(f"call {call} o vs oracle", o, ref["o"], tol)
+        assert_close(f"call {call} S vs oracle", S, ref["S"], tol)
+        np.testing.assert_array_equal(ring.double().cpu().numpy(), ref["ring"])
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
@@ -89,3 +97,27 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     st, *_ = call_noalloc(f, kp, [x, x, x, x, bb, x], [0, T])
     assert st == kda.KDA_ERR_WORKSPACE
     np.testing.assert_equal(st, kda.KDA_ERR_WORKSPACE)
+
+
+def test_noalloc_status_reports_a_timeout_then_ok():
+    """With the test hook that shortens the chunk preparation's pipeline waits
+    to 1 us, a call through the no-allocation entry point times out;
+    kda_noalloc_status reports it and clears the word; a normal call then
+    succeeds."""
+    f = noalloc_fn()
+    L = kda.lib()
+    L.kda_noalloc_status.argtypes = [_vp]
+    L.kda_noalloc_status.restype = ctypes.c_int
+    H = 1
+    p = kda_synth.draw_params(H, 25)
+    cu = [0, 128]
+    tk = [t.to(DEV) for t in kda_synth.draw_tokens(128, H, 26, torch.bfloat16).fields()]
+    stream = torch.cuda.current_stream().cuda_stream
+    st, *_ = call_noalloc(f, kda_params(p, "bf16", wait_limit_us=1), tk, cu)
+    assert st == kda.KDA_OK
+    assert L.kda_noalloc_status(stream) == kda.KDA_ERR_TIMEOUT
+    st, o, S, ring = call_noalloc(f, kda_params(p, "bf16"), tk, cu)
+    assert st == kda.KDA_OK
+    assert L.kda_noalloc_status(stream) == kda.KDA_OK
+    ref = oracle_run(p, kda_synth.Tokens(*[t.cpu() for t in tk]), cu)
+    assert_close("o", o, ref["o"], tol_for("bf16"))
