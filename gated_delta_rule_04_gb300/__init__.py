@@ -24,8 +24,9 @@ LIB_PATH = os.path.join(_PKG, "libkda.so")
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = range(6)
 KDA_DTYPE_F32, KDA_DTYPE_BF16 = 0, 1
-KDA_ALGO_AUTO, KDA_ALGO_SCAN, KDA_ALGO_CHUNKED = 0, 1, 2
-_ALGOS = {"auto": KDA_ALGO_AUTO, "scan": KDA_ALGO_SCAN, "chunked": KDA_ALGO_CHUNKED}
+KDA_ALGO_AUTO, KDA_ALGO_SCAN, KDA_ALGO_CHUNKED, KDA_ALGO_CHUNKED_SEGMENTS = 0, 1, 2, 3
+_ALGOS = {"auto": KDA_ALGO_AUTO, "scan": KDA_ALGO_SCAN, "chunked": KDA_ALGO_CHUNKED,
+          "chunked_segments": KDA_ALGO_CHUNKED_SEGMENTS}
 
 _vp = ctypes.c_void_p
 

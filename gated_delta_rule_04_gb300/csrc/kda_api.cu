@@ -39,6 +39,7 @@ kda_status resolve_algo(const kda_params* p, Algo* out) {
     switch (p->algo) {
         case KDA_ALGO_SCAN: *out = Algo::Scan; return KDA_OK;
         case KDA_ALGO_CHUNKED:
+        case KDA_ALGO_CHUNKED_SEGMENTS:
             if (!bf16 || !bound_ok || !chunked_available()) return KDA_ERR_UNSUPPORTED;
             *out = Algo::Chunked;
             return KDA_OK;
@@ -157,6 +158,60 @@ bool overlap_layout(const kda_params* p, int64_t T, OverlapPlan* pl) {
 }
 
 
+// ---- segmented recurrence of one sequence -------------------------------------
+// The sequence's chunks split into P segments; the recurrence of each segment
+// runs in parallel from a zero state (and its linear part from the identity),
+// an affine scan composes the segment maps, and a second pass runs every
+// segment after the first from its true starting state (see kda_segments.cu).
+struct SegPlan {
+    int P = 0;
+    int64_t c_first[MAX_SEGS + 1] = {};   // first chunk of each segment; c_first[P] = chunks
+    size_t slot_bytes = 0, off_slots = 0, total = 0;
+};
+constexpr int64_t SEG_MIN_CHUNKS = 8;   // shortest segment
+constexpr int SMS_GB300 = 152;
+
+// The fewest segments a call runs as: KDA_ALGO_CHUNKED_SEGMENTS takes any
+// P >= 3; KDA_ALGO_AUTO takes P >= 4 (with P = 3, two thirds of the chain
+// remain serial and the overlapped windows are faster on GB300: 1.49 against
+// 1.67 ms for T = 32768, H = 32); KDA_ALGO_CHUNKED never segments.
+int segment_min(const kda_params* p) {
+    if (p->algo == KDA_ALGO_CHUNKED_SEGMENTS) return 3;
+    if (p->algo == KDA_ALGO_AUTO) return 4;
+    return 1 << 30;
+}
+
+// The number of segments for H heads on `sms` SMs (0: not segmented): the
+// first pass runs 2P - 3 CTAs per head, and every segment holds at least
+// SEG_MIN_CHUNKS chunks.
+int segment_count(int H, int sms, int64_t chunks) {
+    int P = 0;
+    for (int c = 3; c <= (MAX_SEGS + 3) / 2; ++c)
+        if ((int64_t)H * (2 * c - 3) <= sms && chunks >= (int64_t)c * SEG_MIN_CHUNKS) P = c;
+    return P;
+}
+
+// Workspace of the segmented schedule: the single pass's, then 3P - 5 state
+// slots of H x 128 x 128 fp32 (the offsets B_0 .. B_{P-2}, the maps M_1 ..
+// M_{P-2}, the composed states X_2 .. X_{P-1}).
+// P is the most segments `sms` SMs take, reduced until the layout fits
+// `ws_bytes` (0: no limit).
+bool segment_layout(const kda_params* p, int64_t T, int sms, size_t single_bytes, size_t ws_bytes, SegPlan* sp) {
+    const int64_t chunks = (T + CHUNK - 1) / CHUNK;
+    const size_t slot = (size_t)p->num_heads * D * D * sizeof(float);
+    const size_t base = align_up(single_bytes, WS_ALIGN);
+    const int P_min = segment_min(p);
+    int P = segment_count(p->num_heads, sms, chunks);
+    while (P >= P_min && ws_bytes != 0 && base + (size_t)(3 * P - 5) * slot > ws_bytes) --P;
+    if (P < P_min || P < 3) return false;
+    sp->P = P;
+    for (int i = 0; i <= P; ++i) sp->c_first[i] = chunks * i / P;
+    sp->slot_bytes = (size_t)p->num_heads * D * D * sizeof(float);
+    sp->off_slots = align_up(single_bytes, WS_ALIGN);
+    sp->total = sp->off_slots + (size_t)(3 * P - 5) * sp->slot_bytes;
+    return true;
+}
+
 }  // namespace
 }  // namespace kda
 
@@ -193,6 +248,12 @@ size_t kda_prefill_workspace_bytes(const kda_params* p, int32_t n_seqs, int64_t 
     size_t need = layout(p, algo, n_seqs, total_tokens, n_chunks).total;
     OverlapPlan pl;   // one long sequence may run as windows (see prefill_overlapped)
     if (algo == Algo::Chunked && n_seqs == 1 && overlap_layout(p, total_tokens, &pl)) need = std::max(need, pl.total);
+    // one sequence may run as segments (prefill_segmented); the reserve assumes
+    // GB300's 152 SMs, and a call with less workspace takes fewer segments
+    SegPlan sp;
+    if (algo == Algo::Chunked && n_seqs == 1 &&
+        segment_layout(p, total_tokens, SMS_GB300, layout(p, algo, 1, total_tokens, n_chunks).total, 0, &sp))
+        need = std::max(need, sp.total);
     return need;
 }
 
@@ -341,6 +402,61 @@ kda_status prefill_overlapped(const kda_params* p, const void* q, const void* k,
     return st;
 }
 
+// Whether this call runs its recurrence as segments: one sequence whose heads
+// leave most SMs idle (2P - 3 CTAs per head for P >= 3 segments of at least
+// SEG_MIN_CHUNKS chunks) and a workspace that holds the state slots.
+bool plan_segments(const kda_params* p, int64_t T, size_t single_bytes, size_t ws_bytes, SegPlan* sp) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    return segment_layout(p, T, sms, single_bytes, ws_bytes, sp);
+}
+
+// The recurrence of one sequence (chunk preparation done, records in `rec`)
+// as P segments: pass 1 runs segments 0 .. P-2 from their starting states
+// (the caller's for segment 0, which writes its outputs there; zero for the
+// others) and the linear parts of segments 1 .. P-2 from the identity; the
+// scan composes X_{p+1} = M_p X_p + B_p; pass 2 runs segments 1 .. P-1 from
+// their true starting states, writing their outputs and, for the last, S_out.
+kda_status recurrence_segmented(const kda_params* p, const void* gout, int64_t T, const float* S_in, float* S_out,
+                                void* o, const void* rec, int32_t* status, unsigned char* ws, const SegPlan& sp,
+                                cudaStream_t s) {
+    const int H = p->num_heads, P = sp.P;
+    auto slot = [&](int i) { return reinterpret_cast<float*>(ws + sp.off_slots + (size_t)i * sp.slot_bytes); };
+    // slots: B_0 .. B_{P-2} at 0 .. P-2, M_p (p = 1 .. P-2) at P-1 .. 2P-4, X_p (p = 2 .. P-1) at 2P-3 .. 3P-6
+    auto B = [&](int q) { return slot(q); };
+    auto M = [&](int q) { return slot(P - 2 + q); };
+    auto X = [&](int q) { return slot(2 * P - 5 + q); };
+    auto seg_t0 = [&](int q) { return (int64_t)CHUNK * sp.c_first[q]; };
+    auto seg_t1 = [&](int q) { return std::min<int64_t>(T, (int64_t)CHUNK * sp.c_first[q + 1]); };
+    ChunkRecArgs a{};
+    a.records = rec; a.gout = gout; a.norm_w = p->norm_w; a.o = o; a.eps = p->norm_eps; a.status = status; a.H = H;
+    int n = 0;
+    auto add = [&](int q, const float* in, float* out, int32_t mode) {
+        a.seg_t0[n] = seg_t0(q); a.seg_t1[n] = seg_t1(q); a.seg_c0[n] = sp.c_first[q];
+        a.seg_S_in[n] = in; a.seg_S_out[n] = out; a.seg_mode[n] = mode;
+        ++n;
+    };
+    add(0, S_in, B(0), 0);
+    for (int q = 1; q + 1 < P; ++q) add(q, nullptr, B(q), SEG_NO_OUTPUT);
+    for (int q = 1; q + 1 < P; ++q) add(q, nullptr, M(q), SEG_IDENTITY | SEG_LINEAR | SEG_NO_OUTPUT);
+    a.n_segs = n;
+    if (launch_chunk_recurrence(a, s) != cudaSuccess) return KDA_ERR_CUDA;
+    {
+        ScanArgs2 sa{};
+        sa.P = P; sa.H = H;
+        for (int q = 0; q + 1 < P; ++q) sa.B[q] = B(q);
+        for (int q = 1; q + 1 < P; ++q) sa.M[q] = M(q);
+        for (int q = 2; q < P; ++q) sa.X[q] = X(q);
+        if (launch_affine_scan(sa, s) != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    n = 0;
+    for (int q = 1; q < P; ++q) add(q, q == 1 ? B(0) : X(q), q == P - 1 ? S_out : nullptr, 0);
+    a.n_segs = n;
+    if (launch_chunk_recurrence(a, s) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
 }  // namespace
 
 kda_status prefill_check(const kda_params* p) {
@@ -380,7 +496,10 @@ kda_status prefill_run(const kda_params* p, const void* q, const void* k, const 
     const WsLayout L = layout(p, algo, n_seqs, total_tokens, n_chunks);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream_);
-    if (algo == Algo::Chunked && ev == nullptr && n_seqs == 1) {
+    SegPlan sp;
+    const bool segmented = algo == Algo::Chunked && n_seqs == 1 &&
+                           plan_segments(p, total_tokens, L.total, workspace_bytes, &sp);
+    if (algo == Algo::Chunked && ev == nullptr && n_seqs == 1 && !segmented) {
         OverlapPlan pl;
         if (plan_overlap(p, total_tokens, workspace_bytes, &pl))
             return prefill_overlapped(p, q, k, v, z, b, gout, total_tokens, S_in, S_out, ring_in, ring_out, o,
@@ -435,11 +554,19 @@ kda_status prefill_run(const kda_params* p, const void* q, const void* k, const 
                     PREP_BATCH, prep_wait_limit_ns(p), {}, {}};
         e = launch_chunk_prep(pr, s);
         if (e != cudaSuccess || mark(ev, 2, s) != cudaSuccess) return KDA_ERR_CUDA;
-        // the recurrence kernel applies the output norm itself
-        ChunkRecArgs ca{ws + L.rec, S_in, S_out, gout, p->norm_w, o, p->norm_eps, d_cu, d_coff, d_order,
-                        reinterpret_cast<int32_t*>(ws + L.status), n_seqs, H};
-        e = launch_chunk_recurrence(ca, s);
-        if (e != cudaSuccess || mark(ev, 3, s) != cudaSuccess) return KDA_ERR_CUDA;
+        // the recurrence kernel applies the output norm itself; one sequence with
+        // few heads runs it as segments
+        if (segmented) {
+            const kda_status st2 = recurrence_segmented(p, gout, total_tokens, S_in, S_out, o, ws + L.rec,
+                                                        reinterpret_cast<int32_t*>(ws + L.status), ws, sp, s);
+            if (st2 != KDA_OK) return st2;
+        } else {
+            ChunkRecArgs ca{ws + L.rec, S_in, S_out, gout, p->norm_w, o, p->norm_eps, d_cu, d_coff, d_order,
+                            reinterpret_cast<int32_t*>(ws + L.status), n_seqs, H};
+            e = launch_chunk_recurrence(ca, s);
+            if (e != cudaSuccess) return KDA_ERR_CUDA;
+        }
+        if (mark(ev, 3, s) != cudaSuccess) return KDA_ERR_CUDA;
     }
     if (algo == Algo::Scan) {
         EpilogueArgs ea{ocore, gout, p->norm_w, o, total_tokens, H, p->norm_eps};
@@ -464,8 +591,13 @@ int32_t kda_prefill_windows(const kda_params* p, int32_t n_seqs, int64_t total_t
     if (check_params(p) != KDA_OK || n_seqs < 0 || total_tokens < 0) return -1;
     Algo algo;
     if (resolve_algo(p, &algo) != KDA_OK) return -1;
+    if (algo != Algo::Chunked || n_seqs != 1) return 1;
+    SegPlan sp;
+    int64_t n_chunks = (total_tokens + CHUNK - 1) / CHUNK;
+    if (plan_segments(p, total_tokens, layout(p, algo, 1, total_tokens, n_chunks).total, workspace_bytes, &sp))
+        return 1;
     OverlapPlan pl;
-    if (algo == Algo::Chunked && n_seqs == 1 && plan_overlap(p, total_tokens, workspace_bytes, &pl)) return pl.S;
+    if (plan_overlap(p, total_tokens, workspace_bytes, &pl)) return pl.S;
     return 1;
 }
 

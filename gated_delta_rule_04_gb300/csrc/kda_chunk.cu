@@ -106,11 +106,16 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, W = H * D;
-    const int n = a.seq_order ? a.seq_order[blockIdx.x / H] : (int)(blockIdx.x / H);
+    const bool segs = a.n_segs > 0;
+    const int n = segs ? (int)(blockIdx.x / H) : a.seq_order ? a.seq_order[blockIdx.x / H] : (int)(blockIdx.x / H);
     const int h = blockIdx.x % H;
-    const int64_t c0 = a.chunk_off[n];
-    const int64_t nc = a.chunk_off[n + 1] - c0;
-    const int64_t bos = a.cu[n], L = a.cu[n + 1] - bos;
+    const int64_t bos = segs ? a.seg_t0[n] : a.cu[n], L = (segs ? a.seg_t1[n] : a.cu[n + 1]) - bos;
+    const int64_t c0 = segs ? a.seg_c0[n] : a.chunk_off[n];
+    const int64_t nc = segs ? (L + CHUNK_T - 1) / CHUNK_T : a.chunk_off[n + 1] - c0;
+    const int32_t mode = segs ? a.seg_mode[n] : 0;
+    // state in and out of this CTA's (sequence or segment, head)
+    const float* S_in = segs ? a.seg_S_in[n] : a.S_in;
+    float* S_out = segs ? a.seg_S_out[n] : a.S_out;
 
     if (warp == 0) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
@@ -153,7 +158,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
         if (c + 2 < nc)  // the record after next goes to L2 already
             ptx::bulk_prefetch_l2(recs + ((size_t)(c0 + c + 2) * H + h) * REC_BYTES, REC_BYTES);
     };
-    const size_t soff = ((size_t)n * H + h) * D * D;
+    const size_t soff = ((size_t)(segs ? 0 : n) * H + h) * D * D;
 
     if (warp < 8) {
         // ============================ state chain ============================
@@ -166,7 +171,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
         for (int j = 2 * half; j < 2 * half + 2; ++j) {
             float v[32];
 #pragma unroll
-            for (int x = 0; x < 32; ++x) v[x] = a.S_in ? a.S_in[soff + (size_t)(32 * j + x) * D + vrow] : 0.f;
+            for (int x = 0; x < 32; ++x)
+                v[x] = (mode & SEG_IDENTITY) ? (32 * j + x == vrow ? 1.f : 0.f)
+                       : S_in ? S_in[soff + (size_t)(32 * j + x) * D + vrow] : 0.f;
             ptx::tmem_st32(tlane + 32 * j, v);
         }
 #pragma unroll 1
@@ -261,7 +268,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const uint32_t off = sw128_off(vrow, 32 * half + 8 * q, 128);
-                    const uint4 u0 = *reinterpret_cast<const uint4*>(sp + REC_UT + off);
+                    // (the linear part of the step alone: U0 read as zero)
+                    const uint4 u0 = (mode & SEG_LINEAR) ? make_uint4(0, 0, 0, 0)
+                                                         : *reinterpret_cast<const uint4*>(sp + REC_UT + off);
                     const __half2* p = reinterpret_cast<const __half2*>(&u0);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -294,14 +303,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
             if (*abort_flag) break;
             ptx::tc_fence_after();
         }
-        if (!*abort_flag) {
+        if (!*abort_flag && S_out != nullptr) {
             // final state: S_out[key][value] = S^T[value][key]
 #pragma unroll 1
             for (int j = 2 * half; j < 2 * half + 2; ++j) {
                 float v[32];
                 ptx::tmem_ld32(tlane + 32 * j, v);
 #pragma unroll
-                for (int x = 0; x < 32; ++x) a.S_out[soff + (size_t)(32 * j + x) * D + vrow] = v[x];
+                for (int x = 0; x < 32; ++x) S_out[soff + (size_t)(32 * j + x) * D + vrow] = v[x];
             }
         }
     } else {
@@ -393,7 +402,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
                 ss += __shfl_xor_sync(0xffffffffu, ss, 2);
                 ss += __shfl_xor_sync(0xffffffffu, ss, 4);
                 const float rs = rsqrtf(ss * (1.0f / D) + a.eps);
-                if (t < Lc) {
+                if (t < Lc && !(mode & SEG_NO_OUTPUT)) {
                     // o * rs * w * sigmoid(g)
                     float r[16];
 #pragma unroll
@@ -452,7 +461,7 @@ cudaError_t launch_chunk_recurrence(const ChunkRecArgs& a, cudaStream_t s) {
     auto k = chunk_recurrence_kernel<__nv_bfloat16>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int64_t blocks = (int64_t)a.n_seqs * a.H;
+    const int64_t blocks = (int64_t)(a.n_segs > 0 ? a.n_segs : a.n_seqs) * a.H;
     if (blocks == 0) return cudaSuccess;
     k<<<(unsigned)blocks, NT, SMEM_BYTES, s>>>(a);
     return cudaGetLastError();

@@ -11,6 +11,8 @@
 namespace kda {
 
 constexpr int CHUNK_T = 64;  // tokens per chunk
+constexpr int MAX_SEGS = 16;  // pseudo-sequences of one segmented recurrence launch
+constexpr int32_t SEG_IDENTITY = 1, SEG_LINEAR = 2, SEG_NO_OUTPUT = 4;
 
 // Record layout (bytes).  Every tile is fp16, K-major with the 128-byte
 // swizzle, and starts on a 1024-byte boundary.  fp16 rather than bf16: every
@@ -83,7 +85,30 @@ struct ChunkRecArgs {
     const int32_t* seq_order;  // [n] sequences by decreasing length (CTA order), or NULL
     int32_t* status;
     int32_t n_seqs, H;
+    // Segments of one sequence (n_segs > 0; then cu, chunk_off, seq_order and
+    // S_in / S_out are not used): CTA (n, h) runs tokens [seg_t0[n], seg_t1[n])
+    // whose first chunk is seg_c0[n], from the state seg_S_in[n] (NULL: zero),
+    // writing its final state to seg_S_out[n] (NULL: not written); states are
+    // [H][128][128].  seg_mode[n] bits: SEG_IDENTITY starts from the identity
+    // instead, SEG_LINEAR runs the linear part of the chunk step only (U0 read
+    // as zero), SEG_NO_OUTPUT writes no output rows.
+    int32_t n_segs;
+    int64_t seg_t0[MAX_SEGS], seg_t1[MAX_SEGS], seg_c0[MAX_SEGS];
+    const float* seg_S_in[MAX_SEGS];
+    float* seg_S_out[MAX_SEGS];
+    int32_t seg_mode[MAX_SEGS];
 };
 cudaError_t launch_chunk_recurrence(const ChunkRecArgs& a, cudaStream_t s);
+
+// Affine composition of segment maps, column block by column block:
+// X_{p+1} = M_p X_p + B_p for p = 1 .. P - 2, with X_1 = B_0 (all [H][128][128]
+// fp32, key-major rows; M_p maps keys to keys).  X[p] receives X_p.
+struct ScanArgs2 {
+    const float* B[MAX_SEGS];
+    const float* M[MAX_SEGS];
+    float* X[MAX_SEGS];
+    int32_t P, H;
+};
+cudaError_t launch_affine_scan(const ScanArgs2& a, cudaStream_t s);
 
 }  // namespace kda

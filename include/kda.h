@@ -75,8 +75,19 @@ typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
 /* Prefill algorithm.  AUTO picks CHUNKED for bf16 I/O with the bounded gate
  * and a bound >= -5.5 (the tensor-core form needs every 16-token rescaling
  * factor below e^88) and SCAN otherwise.  SCAN is the fp32 sequential
- * recurrence. */
-typedef enum { KDA_ALGO_AUTO = 0, KDA_ALGO_SCAN = 1, KDA_ALGO_CHUNKED = 2 } kda_algo;
+ * recurrence.
+ * Segments: the recurrence of a single sequence whose heads leave SMs idle
+ * can run as P segments in parallel: each segment's map S -> M S + B (the
+ * state exchange a context-parallel split of one sequence needs), composed by
+ * a scan, then every segment again from its true starting state.  This
+ * computes the same function up to rounding and takes the single-pass
+ * workspace plus 3P - 5 states of H x 128 x 128 fp32 (included in
+ * kda_prefill_workspace_bytes).  AUTO segments when P >= 4 segments of at
+ * least 8 chunks fit (2P - 3 CTAs per head on the device's SMs); otherwise a
+ * single sequence runs as the overlapped windows of kda_prefill_windows.
+ * CHUNKED_SEGMENTS segments from P = 3; CHUNKED never segments.
+ * kda_prefill_algo reports CHUNKED for all three. */
+typedef enum { KDA_ALGO_AUTO = 0, KDA_ALGO_SCAN = 1, KDA_ALGO_CHUNKED = 2, KDA_ALGO_CHUNKED_SEGMENTS = 3 } kda_algo;
 
 /* Decay gate.
  *   BOUNDED: g = gate_lower_bound * sigmoid(exp(A_log) (z + dt_bias)), in
@@ -164,9 +175,9 @@ kda_status kda_prefill(const kda_params* p,
  * and the result is bit-identical to the single pass.  That stream and seven
  * events are created on a host thread's first windowed call on a device and
  * kept for the thread's lifetime (one set per thread and device, never
- * shared between threads).  The query
- * needs a current CUDA device (it reads the SM count); -1 for arguments
- * kda_prefill would reject. */
+ * shared between threads).  A call that runs as segments (see kda_algo)
+ * reports 1.  The query needs a current CUDA device (it reads the SM count);
+ * -1 for arguments kda_prefill would reject. */
 int32_t kda_prefill_windows(const kda_params* p, int32_t n_seqs, int64_t total_tokens, size_t workspace_bytes);
 
 /* Same as kda_prefill, and records caller-created CUDA events on `stream` at

@@ -28,7 +28,7 @@ def test_windows_equal_single_pass(T, in_place):
     g = torch.Generator().manual_seed(103)
     S0 = torch.randn(1, H, 128, 128, generator=g) * 0.05
     R0 = torch.randn(1, 3, 3, H * 128, generator=g).to(torch.bfloat16)
-    kp = kda_params(p, io)
+    kp = kda_params(p, io, "chunked")   # (auto would run 8 heads as segments)
     cu = [0, T]
     ws = torch.empty(kda.kda_prefill_workspace_bytes(kp, 1, T), dtype=torch.uint8, device=DEV)
     assert kda.kda_prefill_windows(kp, 1, T, ws.numel()) >= 2

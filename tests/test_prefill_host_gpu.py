@@ -110,9 +110,9 @@ def test_host_prefill_segments_that_run_as_windows():
     sequence, and the oracle on one head."""
     io, cu, H = "bf16", [0, 5120], 8
     p, tk, S0, ring0 = inputs(io, cu, H=H, seed=97)
-    kp = kda_params(p, io)
+    kp = kda_params(p, io, "chunked")   # (auto would run 8 heads as segments)
     assert kda.kda_prefill_windows(kp, 1, 2560, 1 << 40) >= 2
-    o, S, ring = run_host(p, tk, cu, io, 2560, S0, ring0)
+    o, S, ring = run_host(p, tk, cu, io, 2560, S0, ring0, algo="chunked")
     o_d, S_d, ring_d = kda.kda_prefill(kp, *[t.to(DEV) for t in tk.fields()], cu, S_in=S0.to(DEV),
                                        ring_in=ring0.to(DEV))
     torch.cuda.synchronize()
