@@ -34,8 +34,10 @@ bool chunked_available() { return chunked_kernel_built(); }
 
 kda_status resolve_algo(const kda_params* p, Algo* out) {
     const bool bf16 = p->io_dtype == KDA_DTYPE_BF16;
-    // 16 * 5.5 = 88 < ln(FLT_MAX); the unbounded gate has no such bound
-    const bool bound_ok = p->gate_kind == KDA_GATE_BOUNDED && p->gate_lower_bound >= -5.5f;
+    // bounded gate: 16 * 5.5 = 88 < ln(FLT_MAX) keeps every sub-tile factor in
+    // range; the unbounded gate takes the diagonal blocks by position pairs
+    const bool bound_ok = (p->gate_kind == KDA_GATE_BOUNDED && p->gate_lower_bound >= -5.5f) ||
+                          p->gate_kind == KDA_GATE_SOFTPLUS;
     switch (p->algo) {
         case KDA_ALGO_SCAN: *out = Algo::Scan; return KDA_OK;
         case KDA_ALGO_CHUNKED:
@@ -380,7 +382,7 @@ kda_status prefill_overlapped(const kda_params* p, const void* q, const void* k,
             if (w > 0 && (!ok(cudaEventRecord(ev[6], s)) || !ok(cudaStreamWaitEvent(sr, ev[6], 0)))) break;
             PrepArgs pr{q, k, v, z, b, ring_in, p->conv_w, p->A_log, p->dt_bias, p->gate_lower_bound, p->l2_eps, qs,
                         reinterpret_cast<const ChunkDesc*>(mw + 4 * sizeof(int64_t)), (int32_t)nck, H, T, rec, status,
-                        counter, batch, prep_wait_limit_ns(p), {}, {}};
+                        counter, batch, prep_wait_limit_ns(p), {}, {}, p->gate_kind};
             // part 1 alongside the recurrence of window w - 1 (all SMs for window 0)
             if (!ok(launch_chunk_prep(pr, s, w == 0 ? 0 : pl.sms - H)) || !ok(cudaEventRecord(ev[1 + r], s))) break;
             // part 2 on the SMs that recurrence frees
@@ -551,7 +553,7 @@ kda_status prefill_run(const kda_params* p, const void* q, const void* k, const 
         if (mark(ev, 1, s) != cudaSuccess) return KDA_ERR_CUDA;
         PrepArgs pr{q, k, v, z, b, ring_in, p->conv_w, p->A_log, p->dt_bias, p->gate_lower_bound, p->l2_eps, qs,
                     d_chunks, (int32_t)n_chunks, H, total_tokens, ws + L.rec, reinterpret_cast<int32_t*>(ws + L.status), nullptr,
-                    PREP_BATCH, prep_wait_limit_ns(p), {}, {}};
+                    PREP_BATCH, prep_wait_limit_ns(p), {}, {}, p->gate_kind};
         e = launch_chunk_prep(pr, s);
         if (e != cudaSuccess || mark(ev, 2, s) != cudaSuccess) return KDA_ERR_CUDA;
         // the recurrence kernel applies the output norm itself; one sequence with

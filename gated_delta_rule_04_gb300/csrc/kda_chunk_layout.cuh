@@ -64,6 +64,7 @@ struct PrepArgs {
     // set by launch_chunk_prep: TMA descriptors of q, k, v as [T][H*128] bf16
     // with a 67-row box (a chunk and the three rows before it) and a 64-row box
     CUtensorMap map67[3], map64[3];
+    int32_t gate_kind;              // KDA_GATE_BOUNDED or KDA_GATE_SOFTPLUS
 };
 constexpr int PREP_BATCH = 4;        // most items per take from PrepArgs::work_counter
 // PrepArgs::wait_limit_ns from the parameters' test hook (0: the default)

@@ -89,11 +89,15 @@ constexpr int NF = 256;                    // front threads (warps 0-7)
 constexpr int NB = 256;                    // back threads (warps 8-15)
 constexpr int BAR_FRONT = 1, BAR_BACK = 2; // named barrier ids
 constexpr int REG_LAUNCH = 65536 / PT;     // registers per thread at launch (__launch_bounds__(PT, 1))
-constexpr int REG_FRONT = 152, REG_BACK = 104;
-static_assert(REG_LAUNCH == 128 && NF * REG_FRONT + NB * REG_BACK <= PT * REG_LAUNCH,
+// register split (front, back); the unbounded gate's position pairs need more in front
+template <bool SP> constexpr int REG_FRONT = SP ? 160 : 152;
+template <bool SP> constexpr int REG_BACK = SP ? 96 : 104;
+template <bool SP> constexpr bool split_ok() {
+    return NF * REG_FRONT<SP> + NB * REG_BACK<SP> <= PT * REG_LAUNCH && REG_FRONT<SP> % 8 == 0 &&
+           REG_BACK<SP> % 8 == 0 && REG_BACK<SP> >= 24 && REG_FRONT<SP> <= 256;
+}
+static_assert(REG_LAUNCH == 128 && split_ok<false>() && split_ok<true>(),
               "the register split must fit the launch's registers, or setmaxnreg.inc waits forever");
-static_assert(REG_FRONT % 8 == 0 && REG_BACK % 8 == 0 && REG_BACK >= 24 && REG_FRONT <= 256,
-              "setmaxnreg counts");
 constexpr int C = CHUNK_T;                 // 64 tokens
 constexpr int XR = 16 + RING;              // raw rows a front thread reads per plane
 constexpr int LDS = 68;                    // fp32 row stride of the 64 x 64 matrices (16-byte rows)
@@ -112,6 +116,8 @@ constexpr uint32_t S_RAW = 0;                      // bf16 [3 planes][67 rows][1
                                                    //   is read before this item's tiles are written
 constexpr uint32_t S_LAP = 0;                      // bf16 2 x [128 rows][128 keys]: A / off-diagonal P left rows
 constexpr uint32_t S_QD = S_LAP + 65536;           // bf16 [128][128]: rows 0-63 q hi, 64-127 q lo
+constexpr uint32_t S_DG = S_QD;                    //   softplus gate: fp32 [2 slots][4 sub-tiles][2 halves][256]
+                                                   //   position-pair sums of the diagonal blocks (no split P)
 constexpr uint32_t S_RHL = S_QD + 32768;           // bf16 [128][128 keys] R: rows 0-63 hi, 64-127 lo
 constexpr uint32_t S_TT = S_RHL + 32768;           // fp16 [64 r][64 s] T; the W product reads it as 128 A
                                                    //   rows, rows 64-127 being the first 8 KiB of (k e^G)^T
@@ -135,6 +141,7 @@ static_assert(S_RAW + 3 * RAW_PLANE <= S_QD, "raw rows inside the left-row tiles
 static_assert(S_KPT == S_TT + 8192, "the W product's junk A rows are the first 8 KiB of (k e^G)^T");
 static_assert(S_WUST + 32768 <= S_NRM, "W / U0^T staging inside the solve tiles");
 static_assert(S_XM + 64 * 16 * 4 <= S_NRM, "lo*hi exchange inside X");
+static_assert(2 * 4 * 2 * 256 * 4 <= 32768, "diagonal pair sums inside the diagonal-P operand tile");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 static_assert(S_LAP % 1024 == 0 && S_QD % 1024 == 0 && S_RHL % 1024 == 0 && S_TT % 1024 == 0 &&
                   S_KPT % 1024 == 0 && S_VT % 1024 == 0,
@@ -156,6 +163,11 @@ __device__ __forceinline__ int group_of(int row) {
 __device__ __forceinline__ float ex2f(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2f(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 __device__ __forceinline__ float rcpf(float x) {
@@ -267,6 +279,39 @@ __device__ __forceinline__ void solve_level(const float* Am, float* Xm, int bt) 
     bar_sync_n(BAR_BACK, NB);
 }
 
+// ---- diagonal blocks under the unbounded (softplus) gate ----------------------
+// Without a lower bound on g, the factors e^{G_r - G_en(a)} of a diagonal
+// sub-tile overflow, so its pairs (r, s) are summed position by position on
+// the CUDA cores ("Kimi K3 - Retention gate", section "Why": the old gate
+// needed an explicit position-pair computation on the diagonal tiles).  Each
+// pair takes its factor from a recursive halving of the 16-token sub-tile:
+// at level t (halves of h = 2^t tokens) the pairs with r in the upper and s in
+// the lower half of a 2h-block use the last token m of the lower half,
+// e^{G_r - G_s} = e^{G_r - G_m} e^{G_m - G_s}, both factors <= 1.  Pair values
+// are numbered level by level (t = 3, 2, 1, 0), block by block, row by row,
+// A before P within a row; the 16 values P[r][r] come last (indices 240 + r).
+__device__ __forceinline__ int dg_index(int jr, int js, int isP) {
+    if (jr == js) return 240 + jr;
+    const int t = 31 - __clz(jr ^ js), h = 1 << t, b0 = (jr >> (t + 1)) << (t + 1);
+    const int lvl = t == 3 ? 0 : t == 2 ? 128 : t == 1 ? 192 : 224;
+    return lvl + (b0 >> (t + 1)) * 2 * h * h + (jr - b0 - h) * 2 * h + isP * h + (js - b0);
+}
+
+// Sum of v[i] over the warp's 32 lanes, lanes 2i and 2i + 1 keeping the sum
+// of v[i] (recursive halving: 16 shuffles for 16 values).
+__device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
+#pragma unroll
+    for (int o = 16; o >= 2; o >>= 1) {
+        const bool up = lane & o;
+#pragma unroll
+        for (int i = 0; i < o / 2; ++i) {
+            const float send = up ? v[i] : v[i + o / 2], keep = up ? v[i + o / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
 // Read-only 4-byte load that does not allocate in L1: the rows are read once,
 // and the L1 left beside the shared-memory tiles is too small to stage them.
 __device__ __forceinline__ uint32_t ldg_na(const uint32_t* p) {
@@ -342,6 +387,9 @@ __device__ __forceinline__ void prefetch_item(const PrepArgs& a, const ChunkDesc
     }
 }
 
+// SP: the unbounded gate g = -e^A softplus(z + dt_bias) (diagonal blocks by
+// position pairs); otherwise the lower-bounded gate.
+template <bool SP>
 __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant__ PrepArgs a) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -387,7 +435,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         // ================================ front ================================
         // registers move from the back group to this one: 256 x REG_FRONT +
         // 256 x REG_BACK is exactly the 512 x 128 the CTA was launched with
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REG_FRONT));
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REG_FRONT<SP>));
         const int ft = tid;
         const int H = a.H, W = H * D, NC = a.n_chunks;
         const int n_items = NC * H;
@@ -479,8 +527,13 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                 bar_sync_n(BAR_FRONT, NF);
                 const float eA = __expf(__ldg(a.A_log + h));
                 const float2 dtb = __ldg(reinterpret_cast<const float2*>(a.dt_bias + h * D + c0));
-                gsc = f2(-eA * LOG2E);     // argument of 2^x: -(z + dt_bias) e^A log2 e
-                gof = __fmul2_rn(dtb, gsc);
+                if (SP) {
+                    gsc = f2(-eA);             // g = -e^A softplus(z + dt_bias)
+                    gof = dtb;
+                } else {
+                    gsc = f2(-eA * LOG2E);     // argument of 2^x: -(z + dt_bias) e^A log2 e
+                    gof = __fmul2_rn(dtb, gsc);
+                }
             }
             const bool full = tok0 + 16 <= len;
 
@@ -494,16 +547,28 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                 if (ptx::bar_sync_or(BAR_FRONT, NF, late)) break;
             }
 
-            // ---- gate g = lb sigmoid(e^A (z + dt_bias)) and its running sum over the
-            // thread's 16 tokens (tokens past the chunk's end add nothing)
+            // ---- gate g = lb sigmoid(e^A (z + dt_bias)) (or -e^A softplus(z + dt_bias))
+            // and its running sum over the thread's 16 tokens (tokens past the chunk's
+            // end add nothing)
             float2 gc[16];
             {
                 const float2 lb2 = f2(a.lb);
                 float2 run = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float2 sarg = __ffma2_rn(bf2f(zr[j]), gsc, gof);
-                    const float2 g = __fmul2_rn(lb2, make_float2(rcpf(1.f + ex2f(sarg.x)), rcpf(1.f + ex2f(sarg.y))));
+                    float2 g;
+                    if (SP) {
+                        // softplus(x) = max(x, 0) + ln 2 log2(1 + 2^{-|x| log2 e})
+                        const float2 x = __fadd2_rn(bf2f(zr[j]), gof);
+                        const float2 l = make_float2(lg2f(1.f + ex2f(-fabsf(x.x) * LOG2E)),
+                                                     lg2f(1.f + ex2f(-fabsf(x.y) * LOG2E)));
+                        const float2 sp = __ffma2_rn(l, f2(0.6931471805599453f),
+                                                     make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)));
+                        g = __fmul2_rn(gsc, sp);
+                    } else {
+                        const float2 sarg = __ffma2_rn(bf2f(zr[j]), gsc, gof);
+                        g = __fmul2_rn(lb2, make_float2(rcpf(1.f + ex2f(sarg.x)), rcpf(1.f + ex2f(sarg.y))));
+                    }
                     if (full || tok0 + j < len) run = __fadd2_rn(run, g);
                     gc[j] = run;
                 }
@@ -604,6 +669,116 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                 nvq = rsqrtf(mine.x + other.x + a.l2_eps) * a.q_scale;
                 nvk = rsqrtf(mine.y + other.y + a.l2_eps);
             }
+            if (SP) {
+                // ---- the diagonal blocks of A and P by position pairs (see dg_index):
+                // this thread's two channels' share of every pair sum of its sub-tile,
+                // on the conv outputs (the norm factors of both tokens are applied after
+                // the sum over the warp's 64 channels); the back adds the two warps
+                float* dg = reinterpret_cast<float*>(sb + S_DG) + (((k_iter & 1u) * 4 + a_sub) * 2 + hf) * 256;
+                auto ex2d = [&](float2 hi, float2 lo) {   // e^{hi - lo} per channel (hi <= lo)
+                    return make_float2(ex2f((hi.x - lo.x) * LOG2E), ex2f((hi.y - lo.y) * LOG2E));
+                };
+                auto dot2 = [](float2 x, float2 y) { return fmaf(x.x, y.x, x.y * y.y); };
+                // one batch of 16 pair values: lanes 2q and 2q + 1 hold value 16 kb + q,
+                // whose row jr, column js and matrix (A or P) they name
+                const int q = lane >> 1;
+                auto finish = [&](float (&v)[16], int kb, int jr, int js, int isP) {
+                    const float sum = reduce_scatter16(v, lane);
+                    const float nq_r = __shfl_sync(0xffffffffu, nvq, 2 * jr);
+                    const float nk_r = __shfl_sync(0xffffffffu, nvk, 2 * jr);
+                    const float nk_s = __shfl_sync(0xffffffffu, nvk, 2 * js);
+                    if ((lane & 1) == 0) dg[16 * kb + q] = sum * (isP ? nq_r : nk_r) * nk_s;
+                };
+                // level 3: rows 8-15 against columns 0-7, through token 7
+                {
+                    float2 ks[8];
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) ks[s] = s == 7 ? h2f(ak[7]) : __fmul2_rn(h2f(ak[s]), ex2d(gc[7], gc[s]));
+#pragma unroll 1
+                    for (int kb = 0; kb < 8; ++kb) {
+                        const int r = 8 + kb;
+                        float2 gr = gc[8], akr = h2f(ak[8]), aqr = h2f(aq[8]);
+#pragma unroll
+                        for (int i = 9; i < 16; ++i)
+                            if (r == i) gr = gc[i], akr = h2f(ak[i]), aqr = h2f(aq[i]);
+                        const float2 rho = ex2d(gr, gc[7]);
+                        const float2 kr = __fmul2_rn(akr, rho), qr = __fmul2_rn(aqr, rho);
+                        float v[16];
+#pragma unroll
+                        for (int s = 0; s < 8; ++s) {
+                            v[s] = dot2(kr, ks[s]);
+                            v[8 + s] = dot2(qr, ks[s]);
+                        }
+                        finish(v, kb, r, q & 7, q >> 3);
+                    }
+                }
+                // level 2: in each half, rows 4-7 against columns 0-3, through token 3
+#pragma unroll
+                for (int bb = 0; bb < 2; ++bb) {
+                    const int m = 8 * bb + 3;
+                    float2 ks[4];
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)
+                        ks[s] = s == 3 ? h2f(ak[m]) : __fmul2_rn(h2f(ak[8 * bb + s]), ex2d(gc[m], gc[8 * bb + s]));
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        float v[16];
+#pragma unroll
+                        for (int rr = 0; rr < 2; ++rr) {
+                            const int r = 8 * bb + 4 + 2 * half + rr;
+                            const float2 rho = ex2d(gc[r], gc[m]);
+                            const float2 kr = __fmul2_rn(h2f(ak[r]), rho), qr = __fmul2_rn(h2f(aq[r]), rho);
+#pragma unroll
+                            for (int s = 0; s < 4; ++s) {
+                                v[8 * rr + s] = dot2(kr, ks[s]);
+                                v[8 * rr + 4 + s] = dot2(qr, ks[s]);
+                            }
+                        }
+                        finish(v, 8 + 2 * bb + half, 8 * bb + 4 + 2 * half + (q >> 3), 8 * bb + (q & 3), (q >> 2) & 1);
+                    }
+                }
+                // level 1: in each quarter, rows 2-3 against columns 0-1, through token 1
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    float v[16];
+#pragma unroll
+                    for (int bq = 0; bq < 2; ++bq) {
+                        const int bb = 2 * hb + bq, m = 4 * bb + 1;
+                        const float2 ks0 = __fmul2_rn(h2f(ak[4 * bb]), ex2d(gc[m], gc[4 * bb])), ks1 = h2f(ak[m]);
+#pragma unroll
+                        for (int rr = 0; rr < 2; ++rr) {
+                            const int r = 4 * bb + 2 + rr;
+                            const float2 rho = ex2d(gc[r], gc[m]);
+                            const float2 kr = __fmul2_rn(h2f(ak[r]), rho), qr = __fmul2_rn(h2f(aq[r]), rho);
+                            v[8 * bq + 4 * rr + 0] = dot2(kr, ks0);
+                            v[8 * bq + 4 * rr + 1] = dot2(kr, ks1);
+                            v[8 * bq + 4 * rr + 2] = dot2(qr, ks0);
+                            v[8 * bq + 4 * rr + 3] = dot2(qr, ks1);
+                        }
+                    }
+                    const int bb = 2 * hb + (q >> 3), w = q & 7;
+                    finish(v, 12 + hb, 4 * bb + 2 + (w >> 2), 4 * bb + (w & 1), (w >> 1) & 1);
+                }
+                // level 0: each odd row against the token before it
+                {
+                    float v[16];
+#pragma unroll
+                    for (int bb = 0; bb < 8; ++bb) {
+                        const int r = 2 * bb + 1, s = 2 * bb;
+                        const float2 ks = __fmul2_rn(h2f(ak[s]), ex2d(gc[r], gc[s]));
+                        v[2 * bb] = dot2(h2f(ak[r]), ks);
+                        v[2 * bb + 1] = dot2(h2f(aq[r]), ks);
+                    }
+                    finish(v, 14, 2 * (q >> 1) + 1, 2 * (q >> 1), q & 1);
+                }
+                // P[r][r]
+                {
+                    float v[16];
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) v[r] = dot2(h2f(aq[r]), h2f(ak[r]));
+                    finish(v, 15, q, q, 1);
+                }
+            }
             // ---- per-channel factors from the sub-tile ends G_en(b):
             // E = e^{G_en(a)}, F = e^{G_last - G_en(a)}, Cb = e^{G_en(a) - G_en(b)}
             float2 gen[4];
@@ -616,11 +791,20 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                 }
             }
             const float2 ge = a_sub == 0 ? gen[0] : a_sub == 1 ? gen[1] : a_sub == 2 ? gen[2] : gen[3];
-            const float2 E = make_float2(ex2f(ge.x * LOG2E), ex2f(ge.y * LOG2E));
             const float2 F = make_float2(ex2f((gen[3].x - ge.x) * LOG2E), ex2f((gen[3].y - ge.y) * LOG2E));
-            float2 Cb[3];
+            // bounded gate: E and Cb as factors (iY E and iY Cb stay in range);
+            // unbounded: their exponents, added to the token's before one 2^x each
+            float2 E, Cb[3];
+            if (SP) {
+                E = make_float2(ge.x * LOG2E, ge.y * LOG2E);
 #pragma unroll
-            for (int b = 0; b < 3; ++b) Cb[b] = make_float2(ex2f((ge.x - gen[b].x) * LOG2E), ex2f((ge.y - gen[b].y) * LOG2E));
+                for (int b = 0; b < 3; ++b) Cb[b] = make_float2((ge.x - gen[b].x) * LOG2E, (ge.y - gen[b].y) * LOG2E);
+            } else {
+                E = make_float2(ex2f(ge.x * LOG2E), ex2f(ge.y * LOG2E));
+#pragma unroll
+                for (int b = 0; b < 3; ++b)
+                    Cb[b] = make_float2(ex2f((ge.x - gen[b].x) * LOG2E), ex2f((ge.y - gen[b].y) * LOG2E));
+            }
             if (a_sub == 0)
                 *reinterpret_cast<float2*>(rec + REC_DECAY + 4 * c0) =
                     make_float2(ex2f(gen[3].x * LOG2E), ex2f(gen[3].y * LOG2E));
@@ -660,33 +844,51 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                 // (G_r - G_en(a)) log2 e >= 0 (the running sum decreases)
                 const float2 d = __fmul2_rn(__fadd2_rn(gc[j], make_float2(-gl.x, -gl.y)), L2);
                 const float2 y = make_float2(ex2f(-d.x), ex2f(-d.y));          // Y  = e^{G_en(a) - G_r} <= 1
-                const float2 iy = make_float2(ex2f(d.x), ex2f(d.y));           // iY = e^{G_r - G_en(a)} >= 1
                 const float2 ky = __fmul2_rn(k, y);
                 const uint32_t rh = pack_bf16(ky.x, ky.y);
                 const float2 rhf = bf2f(rh);
                 const float2 rlo = __fadd2_rn(ky, make_float2(-rhf.x, -rhf.y));
                 sts32(sRHL + jo, rh);
                 sts32(sRHL + 64 * 128 + jo, pack_bf16(rlo.x, rlo.y));
-                const float2 ki = __fmul2_rn(k, iy), qi = __fmul2_rn(q, iy);
-                sts32(sLAP + offA_diag + jo, pack_bf16(ki.x, ki.y));      // A row of the diagonal sub-tile
+                float2 qp, kpf;   // q e^G (the Q+ record) and k e^G
+                if (SP) {
+                    // every factor is one 2^x of a non-positive exponent
 #pragma unroll
-                for (int b = 0; b < 3; ++b) {
-                    if (b < a_sub) {
-                        const float2 kf = __fmul2_rn(ki, Cb[b]), qf = __fmul2_rn(qi, Cb[b]);
-                        sts32(sLAP + lap_off(kRowA[b] + tok0) + jo, pack_bf16(kf.x, kf.y));
-                        sts32(sLAP + lap_off(kRowP[b] + tok0) + jo, pack_bf16(qf.x, qf.y));
+                    for (int b = 0; b < 3; ++b) {
+                        if (b < a_sub) {   // e^{G_r - G_en(b)}
+                            const float2 f = make_float2(ex2f(d.x + Cb[b].x), ex2f(d.y + Cb[b].y));
+                            const float2 kf = __fmul2_rn(k, f), qf = __fmul2_rn(q, f);
+                            sts32(sLAP + lap_off(kRowA[b] + tok0) + jo, pack_bf16(kf.x, kf.y));
+                            sts32(sLAP + lap_off(kRowP[b] + tok0) + jo, pack_bf16(qf.x, qf.y));
+                        }
                     }
+                    const float2 eg = make_float2(ex2f(d.x + E.x), ex2f(d.y + E.y));   // e^{G_r}
+                    qp = __fmul2_rn(q, eg);
+                    kpf = __fmul2_rn(k, eg);
+                } else {
+                    const float2 iy = make_float2(ex2f(d.x), ex2f(d.y));       // iY = e^{G_r - G_en(a)} >= 1
+                    const float2 ki = __fmul2_rn(k, iy), qi = __fmul2_rn(q, iy);
+                    sts32(sLAP + offA_diag + jo, pack_bf16(ki.x, ki.y));      // A row of the diagonal sub-tile
+#pragma unroll
+                    for (int b = 0; b < 3; ++b) {
+                        if (b < a_sub) {
+                            const float2 kf = __fmul2_rn(ki, Cb[b]), qf = __fmul2_rn(qi, Cb[b]);
+                            sts32(sLAP + lap_off(kRowA[b] + tok0) + jo, pack_bf16(kf.x, kf.y));
+                            sts32(sLAP + lap_off(kRowP[b] + tok0) + jo, pack_bf16(qf.x, qf.y));
+                        }
+                    }
+                    const uint32_t qh = pack_bf16(qi.x, qi.y);
+                    const float2 qhf = bf2f(qh);
+                    const float2 qlo = __fadd2_rn(qi, make_float2(-qhf.x, -qhf.y));
+                    sts32(sQD + jo, qh);
+                    sts32(sQD + 64 * 128 + jo, pack_bf16(qlo.x, qlo.y));
+                    qp = __fmul2_rn(qi, E);    // q iY E
+                    kpf = __fmul2_rn(ki, E);   // k iY E
                 }
-                const uint32_t qh = pack_bf16(qi.x, qi.y);
-                const float2 qhf = bf2f(qh);
-                const float2 qlo = __fadd2_rn(qi, make_float2(-qhf.x, -qhf.y));
-                sts32(sQD + jo, qh);
-                sts32(sQD + 64 * 128 + jo, pack_bf16(qlo.x, qlo.y));
-                // record: Q+ = q e^{G} = q iY E
-                const float2 qp = __fmul2_rn(qi, E);
+                // record: Q+ = q e^{G}
                 *reinterpret_cast<uint32_t*>(gQ + jo) = pack_f16(qp.x, qp.y);
-                // Kt = k e^{G_last - G} = k Y F;  (k e^G) = k iY E
-                const float2 ktf = __fmul2_rn(ky, F), kpf = __fmul2_rn(ki, E);
+                // Kt = k e^{G_last - G} = k Y F
+                const float2 ktf = __fmul2_rn(ky, F);
                 const uint32_t t_kt = pack_f16(ktf.x, ktf.y), t_kp = pack_f16(kpf.x, kpf.y);
                 if (j & 1) {
                     const int w = j >> 1;
@@ -770,9 +972,10 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         }
     } else {
         // ================================ back =================================
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_BACK));
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_BACK<SP>));
         const int bt = tid - NF, bw = warp - NF / 32;   // 0..255, 0..7
         const int qd = warp & 3;                          // TMEM lane quarter of this warp
+        const float* dgb = reinterpret_cast<const float*>(sb + S_DG);
         uint32_t k = 0;
 #pragma unroll 1
         while (true) {
@@ -797,8 +1000,9 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                                  IDESC_BF16_N64, kk > 0);
                     ptx::mma_f16(tmem + TM_D1, ptx::sdesc_sw128(base + S_LAP + 32768 + pn * 16384 + koff), bR,
                                  IDESC_BF16_N64, kk > 0);
-                    ptx::mma_f16(tmem + TM_D2, ptx::sdesc_sw128(base + S_QD + pn * 16384 + koff), bR,
-                                 IDESC_BF16_N128, kk > 0);
+                    if (!SP)
+                        ptx::mma_f16(tmem + TM_D2, ptx::sdesc_sw128(base + S_QD + pn * 16384 + koff), bR,
+                                     IDESC_BF16_N128, kk > 0);
                 }
                 ptx::mma_commit(bar_mma1);
             }
@@ -834,6 +1038,15 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                 float v[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(b == b_first ? r0[i] : r1[i]);
+                if (SP && !isP && (r >> 4) == b) {   // diagonal block: the front's position-pair sums
+                    const float* d = dgb + ((k & 1u) * 4 + b) * 512;
+                    const int jr = r & 15;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int x = i < jr ? dg_index(jr, i, 0) : 0;
+                        v[i] = i < jr ? d[x] + d[256 + x] : 0.f;
+                    }
+                }
                 if (isP) {
                     *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 16 * b, C)) = pack8_f16(v);
                     *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 16 * b + 8, C)) = pack8_f16(v + 8);
@@ -850,10 +1063,26 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                     }
                 }
             }
+            // ---- diagonal P blocks, unbounded gate (warps 8-11): the front's position-pair
+            // sums, row r = bt % 64, columns 8 (bt / 64) .. + 7 of each block
+            if (SP && bw < 4) {
+                const int r = bt & 63, hh = bt >> 6, ta = r >> 4, jr = r & 15;
+                const float* d = dgb + ((k & 1u) * 4 + ta) * 512;
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int js = 8 * hh + e;
+                    const int x = js <= jr ? dg_index(jr, js, 1) : 0;
+                    v[e] = js <= jr ? d[x] + d[256 + x] : 0.f;
+                }
+                *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 16 * ta + 8 * hh, C)) = pack8_f16(v);
+                for (int tb = ta + 1; tb < 4; ++tb)
+                    *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 16 * tb + 8 * hh, C)) = make_uint4(0, 0, 0, 0);
+            }
             // ---- diagonal P blocks (warps 8-11): D2 rows are [q hi; q lo], columns
             // [R hi | R lo].  Warps 10-11 hand the lo*hi terms (lanes 64-127) to warps
             // 8-9 through shared memory; warps 8-9 add hi*hi + hi*lo + lo*hi.
-            if (bw < 4) {
+            if (!SP && bw < 4) {
                 float* pdl = reinterpret_cast<float*>(sb + S_PDL);   // fp32 [64 r][16]
                 const int r = 32 * (qd & 1) + lane;                  // 0..63
                 const int ta = r >> 4;
@@ -1095,8 +1324,8 @@ cudaError_t launch_chunk_prep(const PrepArgs& args, cudaStream_t s, int max_ctas
         if (!encode_rows(&a.map67[pl], planes[pl], a.T, (int64_t)a.H * D, C + RING) ||
             !encode_rows(&a.map64[pl], planes[pl], a.T, (int64_t)a.H * D, C))
             return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+    void (*kern)(PrepArgs) = a.gate_kind == KDA_GATE_SOFTPLUS ? chunk_prep_kernel<true> : chunk_prep_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     e = cudaGetDevice(&dev);
@@ -1105,7 +1334,7 @@ cudaError_t launch_chunk_prep(const PrepArgs& args, cudaStream_t s, int max_ctas
     if (e != cudaSuccess) return e;
     int64_t grid = items < sms ? items : sms;
     if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
-    chunk_prep_kernel<<<(unsigned)grid, PT, SMEM_BYTES, s>>>(a);
+    kern<<<(unsigned)grid, PT, SMEM_BYTES, s>>>(a);
     return cudaGetLastError();
 }
 

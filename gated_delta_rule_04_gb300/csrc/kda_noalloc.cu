@@ -205,7 +205,7 @@ extern "C" kda_status kda_prefill_noalloc(const kda_params* p, const void* q, co
         if (launch_scan(sa, s) != cudaSuccess) return KDA_ERR_CUDA;
     } else {
         PrepArgs pr{q, k, v, z, b, ring_in, p->conv_w, p->A_log, p->dt_bias, p->gate_lower_bound, p->l2_eps, qs,
-                    d_chunks, (int32_t)nc, H, total_tokens, ws + L.rec, status, nullptr, PREP_BATCH, prep_wait_limit_ns(p), {}, {}};
+                    d_chunks, (int32_t)nc, H, total_tokens, ws + L.rec, status, nullptr, PREP_BATCH, prep_wait_limit_ns(p), {}, {}, p->gate_kind};
         if (launch_chunk_prep(pr, s) != cudaSuccess) return KDA_ERR_CUDA;
         ChunkRecArgs ca{ws + L.rec, S_in, S_out, gout, p->norm_w, o, p->norm_eps, d_cu, d_coff, d_order, status,
                         n_seqs, H};

@@ -72,10 +72,10 @@ typedef enum {
 
 typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
 
-/* Prefill algorithm.  AUTO picks CHUNKED for bf16 I/O with the bounded gate
- * and a bound >= -5.5 (the tensor-core form needs every 16-token rescaling
- * factor below e^88) and SCAN otherwise.  SCAN is the fp32 sequential
- * recurrence.
+/* Prefill algorithm.  AUTO picks CHUNKED for bf16 I/O with the softplus gate
+ * or with the bounded gate and a bound >= -5.5 (the bounded gate's
+ * tensor-core diagonal blocks need every 16-token rescaling factor below
+ * e^88), and SCAN otherwise.  SCAN is the fp32 sequential recurrence.
  * Segments: the recurrence of a single sequence whose heads leave SMs idle
  * can run as P segments in parallel: each segment's map S -> M S + B (the
  * state exchange a context-parallel split of one sequence needs), composed by
@@ -96,9 +96,12 @@ typedef enum { KDA_ALGO_AUTO = 0, KDA_ALGO_SCAN = 1, KDA_ALGO_CHUNKED = 2, KDA_A
  *   SOFTPLUS: g = -exp(A_log) softplus(z + dt_bias), unbounded below. This is
  *     the earlier Kimi-Linear gate ("Kimi Delta Attention (KDA) -- analysis &
  *     C kernel plan", status note; fused_kda_gate with bias = dt_bias). With it
- *     gate_lower_bound is ignored and prefill runs the fp32 scan: the
- *     tensor-core chunk form needs the bound to keep its rescaling factors
- *     finite. */
+ *     gate_lower_bound is ignored.  The chunked form (bf16 I/O) then sums the
+ *     diagonal 16 x 16 blocks of each chunk position pair by position pair on
+ *     the CUDA cores, as the retention-gate page says the old gate needed
+ *     ("Kimi K3 - Retention gate", section "Why"), so that no rescaling factor
+ *     leaves fp32 range; its chunk preparation is about 1.5x slower than with
+ *     the bounded gate. */
 typedef enum { KDA_GATE_BOUNDED = 0, KDA_GATE_SOFTPLUS = 1 } kda_gate;
 
 typedef struct {

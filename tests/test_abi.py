@@ -182,11 +182,16 @@ def test_decode_multi_validation(L):
 
 
 def test_gate_kind_validation(L):
-    assert L.kda_prefill_algo(ctypes.byref(params(gate_kind=1))) == kda.KDA_ALGO_SCAN
-    assert prefill(L, params(gate_kind=1, algo=kda.KDA_ALGO_CHUNKED), [0, 64]) == kda.KDA_ERR_UNSUPPORTED
+    # the softplus gate runs the chunked form with bf16 I/O (diagonal blocks by
+    # position pairs) and the scan with fp32 I/O
+    assert L.kda_prefill_algo(ctypes.byref(params(gate_kind=1))) == kda.KDA_ALGO_CHUNKED
+    assert L.kda_prefill_algo(ctypes.byref(params(gate_kind=1, io_dtype=kda.KDA_DTYPE_F32))) == kda.KDA_ALGO_SCAN
+    assert prefill(L, params(gate_kind=1, algo=kda.KDA_ALGO_CHUNKED, io_dtype=kda.KDA_DTYPE_F32),
+                   [0, 64]) == kda.KDA_ERR_UNSUPPORTED
     assert prefill(L, params(gate_kind=2), [0, 64]) == kda.KDA_ERR_INVALID_ARG
     # the lower bound is not used by the softplus gate
-    assert L.kda_prefill_algo(ctypes.byref(params(gate_kind=1, gate_lower_bound=0.5))) == kda.KDA_ALGO_SCAN
+    assert L.kda_prefill_algo(ctypes.byref(params(gate_kind=1, gate_lower_bound=0.5))) == kda.KDA_ALGO_CHUNKED
+    assert L.kda_prefill_algo(ctypes.byref(params(gate_kind=1, gate_lower_bound=-80.0))) == kda.KDA_ALGO_CHUNKED
 
 
 # ---------------------------------------------------------------- kda_prefill_host
@@ -322,7 +327,7 @@ def noalloc(L, p, cu, T=None, **ptrs):
     (dict(head_dim=64), [0, 64]),
     (dict(conv_w=0, algo=kda.KDA_ALGO_CHUNKED), [0, 64]),
     (dict(num_heads=0, head_dim=96), [0, 64]),
-    (dict(gate_kind=1, algo=kda.KDA_ALGO_CHUNKED), [0, 64]),
+    (dict(gate_kind=1, algo=kda.KDA_ALGO_CHUNKED, io_dtype=kda.KDA_DTYPE_F32), [0, 64]),
     (dict(l2_eps=-1.0), [0, 64]),
     (dict(), [0, 70, 60]),
     (dict(), [1, 64]),

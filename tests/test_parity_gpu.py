@@ -222,20 +222,22 @@ def test_zero_tokens_copies_state():
 
 
 # ---------------------------------------------------------------- softplus gate
-@pytest.mark.parametrize("io", ["f32", "bf16"])
-def test_softplus_gate_prefill_and_verify(io):
+@pytest.mark.parametrize("io, algo, runs", [("f32", "auto", "scan"), ("bf16", "scan", "scan"),
+                                            ("bf16", "auto", "chunked")])
+def test_softplus_gate_prefill_and_verify(io, algo, runs):
     """The earlier Kimi-Linear gate (unbounded below) on the scan prefill and
-    on a multi-token decode round continuing from it."""
+    on the chunked form (bf16 I/O), and on a multi-token decode round
+    continuing from it."""
     lens = [70, 3, 131]
     p, tk, cu = small_case(io, lens, seed=91)
     p.gate_kind = 1
     n, H = len(lens), p.num_heads
-    kp = kda_params(p, io)
-    assert kda.kda_prefill_algo(kp) == "scan"
+    kp = kda_params(p, io, algo)
+    assert kda.kda_prefill_algo(kp) == runs
     g = torch.Generator().manual_seed(92)
     S_in = torch.randn(n, H, 128, 128, generator=g) * 0.05
     ring_in = torch.randn(n, 3, 3, H * 128, generator=g).to(kda_synth.io_dtype(io))
-    o, S, ring = run_prefill(p, tk, cu, io, S_in=S_in, ring_in=ring_in)
+    o, S, ring = run_prefill(p, tk, cu, io, algo, S_in=S_in, ring_in=ring_in)
     ref = check_against_oracle(p, tk, cu, io, o, S, ring, S_in=S_in, ring_in=ring_in)
     # a 3-token round per session from the prefill's state
     n_tok = 3
