@@ -27,7 +27,10 @@
 // <= 1.  For r in sub-tile a the left factor is iY_r C_ab with
 // iY_r = e^{G_r - G_en(a)} in [1, e^{75}] and C_ab = e^{G_en(a) - G_en(b)} <= 1,
 // which bf16 holds; a factor that underflows stands for a product far below
-// every other term.
+// every other term.  Under the unbounded gate (template flag SP) iY_r has no
+// bound: the off-diagonal factors are then taken as one exponential each,
+// e^{G_r - G_en(b)} <= 1, and the diagonal blocks of A and P by position pairs
+// on the CUDA cores (see dg_index).
 //
 // Tensor cores.  A and the off-diagonal blocks of P are two bf16 M = 128 MMAs
 // against the right operand R = k Y (N = 64, K = 128 keys).  The 256 left
@@ -49,10 +52,10 @@
 //     memory, the solve, T, the W / U0^T products, their readout and the
 //     record stores of P, W and U0^T.
 // So the element-wise work of one item overlaps the short, dependent solve of
-// the one before.  The front reads the raw q/k/v and z rows straight from
-// global memory into registers (coalesced 128-byte row pieces; a TMA prefetch
-// one item ahead brings them into L2): shared memory holds the operand tiles
-// of both groups, and staging the raw rows as well would not fit.
+// the one before.  The raw q/k/v rows of an item (with the three rows before
+// the chunk) arrive by TMA into the operand region, issued by the back once
+// the previous item's first batch has read that region; the gate inputs and
+// beta logits are plain loads, and an L2 prefetch runs one item ahead.
 //
 // Front thread mapping: warp w, lane l -> sub-tile a = w / 2 (tokens 16a ..
 // 16a+15) and channel pair p = 32 (w % 2) + l (channels 2p, 2p+1).  Each
@@ -62,9 +65,9 @@
 // cumulative gate is a per-thread running sum plus a prefix over sub-tiles.
 //
 // Hand-offs (all mbarriers, one phase per item, in item order):
-//   mma1   the first batch of item j finished: the back may read A and P, the
-//          front may overwrite the operand tiles;
-//   dfree  the back has read A and P of item j: the next first batch may run;
+//   mma1   the first batch of item j finished: the back may read A and P, and
+//          the next item's raw rows may land in the operand region;
+//   raw    the raw rows of item j have landed: the front may start on it;
 //   info   item j's record address and beta are published to the back (a
 //          null address ends the back's loop);
 //   mma2   the W / U0^T products of item j finished: the front may overwrite
