@@ -13,7 +13,9 @@ inputs resident in HBM.  Alongside it:
   roofline   the dominant kernel against the method's own bytes (fused single pass)
   step       the whole step's HBM fraction and tensor-core fraction
   kernels    each kernel's own bytes over its time
-  other_prefill  the same for the single-sequence T=4096 H=32 and the varlen H=64 workloads
+  other_prefill  the same for the single-sequence T=4096 H=32 and the varlen H=64 workloads,
+                 the long workload with the softplus gate, and the long workload with 8 heads
+                 (one sequence whose recurrence runs as segments)
   cpu_baseline  the fp64 oracle on a bounded sample of the same workload
 
 --impl reference times the oracle (the only other implementation) as the
@@ -243,14 +245,14 @@ def verify_bytes_per_session_head(io_bytes, n_tok):
 PREFILL_WORKLOADS = {"long": 3, "prefill": 2, "varlen": 4}
 
 
-def prefill_arm(args, dev, world, rank, idx=None, heads=None, steps=None):
+def prefill_arm(args, dev, world, rank, idx=None, heads=None, steps=None, gate="bounded"):
     import gated_delta_rule_04_gb300 as kda
     idx = PREFILL_WORKLOADS[args.workload] if idx is None else idx
     steps = steps or args.steps
     w = kda_synth.workload(idx, device=dev, H=heads if heads is not None else args.heads)
     H, T, W = w.H, w.total_tokens, w.H * D
     kp = kda.make_params(w.params.conv_w, w.params.A_log, w.params.dt_bias, w.params.norm_w,
-                         io_dtype=w.io, algo=args.algo)
+                         io_dtype=w.io, algo=args.algo, gate=gate)
     toks = list(w.tokens.fields())
     n = w.n_seqs
     cu = w.cu_seqlens
@@ -305,13 +307,20 @@ def prefill_arm(args, dev, world, rank, idx=None, heads=None, steps=None):
     ws_status = kda.kda_workspace_status(ws, stream)
     algo = kda.kda_prefill_algo(kp)
     windows = kda.kda_prefill_windows(kp, n, T, ws_bytes)
+    segments = kda.kda_prefill_segments(kp, n, T, ws_bytes)
     # chunked single pass: metadata, prep, recurrence, ring; windows: the windows' metadata, a prep
-    # part per window (two from the second on), a recurrence per window and the ring; scan:
-    # metadata, pre-stage, scan, epilogue, ring
-    per_step = (4 if windows == 1 else 3 * windows + 1) if algo == "chunked" else 5
+    # part per window (two from the second on), a recurrence per window and the ring; segments:
+    # metadata, prep, two recurrence passes, the scan of the segment maps, ring; scan: metadata,
+    # pre-stage, scan, epilogue, ring
+    if algo != "chunked":
+        per_step = 5
+    elif segments:
+        per_step = 6
+    else:
+        per_step = 4 if windows == 1 else 3 * windows + 1
     return dict(w=w, ms=ms, ms_max=ms_max, stage_ms=stage_ms, single_ms=single_ms, windows=windows,
-                clocks=clk.summary(), kp=kp, launches=per_step * steps, ws_status=ws_status,
-                algo_resolved=algo)
+                segments=segments, clocks=clk.summary(), kp=kp, launches=per_step * steps, ws_status=ws_status,
+                algo_resolved=algo, gate=gate)
 
 
 def e2e_arm(args, dev, w, kp):
@@ -506,16 +515,23 @@ def prefill_report(r, hbm, tc, tc_sus, peak_kind):
     return {"roofline": roofline, "step": step, "kernels": kern}
 
 
-def other_workload(args, dev, world, rank, idx, hbm, tc, tc_sus, peak_kind):
+def other_workload(args, dev, world, rank, idx, hbm, tc, tc_sus, peak_kind, heads=None, gate="bounded"):
     """A sub-line for another prefill workload: its own value, step and roofline."""
-    r = prefill_arm(args, dev, world, rank, idx=idx, heads=kda_synth.WORKLOADS[idx]["H"],
-                    steps=max(args.steps, 20))
+    r = prefill_arm(args, dev, world, rank, idx=idx, heads=heads or kda_synth.WORKLOADS[idx]["H"],
+                    steps=max(args.steps, 20), gate=gate)
     w = r["w"]
     rep = prefill_report(r, hbm, tc, tc_sus, peak_kind)
-    return {"workload": kda_synth.describe(w.idx, w.H) + ", fp32 state", "metric": "KDA tokens/s/layer",
+    if r["segments"]:
+        schedule = f"{r['segments']} segments (affine maps composed by a scan)"
+    else:
+        schedule = "single pass" if r["windows"] == 1 else f"{r['windows']} overlapped windows"
+    gate_txt = ", softplus gate" if gate == "softplus" else ""
+    if gate == "softplus":   # the stored counters are the bounded-gate kernel's
+        rep["roofline"]["traffic"] = None
+    return {"workload": kda_synth.describe(w.idx, w.H) + gate_txt + ", fp32 state", "metric": "KDA tokens/s/layer",
             "value": whole_job_value(w.total_tokens, r["ms_max"], world), "unit": "tokens/s/layer",
             "ms_per_step": r["ms_max"], "steps": max(args.steps, 20), "algo": r["algo_resolved"],
-            "schedule": ("single pass" if r["windows"] == 1 else f"{r['windows']} overlapped windows"),
+            "schedule": schedule,
             "step": rep["step"], "roofline": rep["roofline"], "kernels": rep["kernels"],
             "clocks": r["clocks"], "workspace_status": r["ws_status"]}, r["launches"]
 
@@ -585,8 +601,11 @@ def main():
     if not args.no_other and args.heads is None and args.workload == "long":
         # the other prefill workloads, each with its own value and fractions
         line["other_prefill"] = {}
-        for name, idx in (("prefill", 2), ("varlen", 4)):
-            sub, launches = other_workload(args, dev, world, rank, idx, hbm, tc, tc_sus, peak_kind)
+        for name, idx, heads, gate in (("prefill", 2, None, "bounded"), ("varlen", 4, None, "bounded"),
+                                       ("long_softplus_gate", 3, None, "softplus"),
+                                       ("long_8_heads", 3, 8, "bounded")):
+            sub, launches = other_workload(args, dev, world, rank, idx, hbm, tc, tc_sus, peak_kind,
+                                           heads=heads, gate=gate)
             line["other_prefill"][name] = sub
     if not args.no_decode:
         dr = decode_arm(args, dev)

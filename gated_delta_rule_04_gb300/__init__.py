@@ -4,7 +4,7 @@ Argument marshalling only: every step of the mixer runs in the CUDA kernels
 behind the C ABI declared in ``include/kda.h``; PyTorch supplies device
 memory and the stream.  The functions carry the C names:
 
-    kda_prefill_algo, kda_prefill_workspace_bytes, kda_prefill_windows, kda_prefill,
+    kda_prefill_algo, kda_prefill_workspace_bytes, kda_prefill_windows, kda_prefill_segments, kda_prefill,
     kda_prefill_with_events (as kda_prefill(..., stage_events=...)),
     kda_prefill_host_scratch_bytes, kda_prefill_host, kda_decode, kda_decode_multi,
     kda_workspace_status, kda_status_str
@@ -80,6 +80,8 @@ def lib():
         L.kda_prefill_workspace_bytes.restype = sz
         L.kda_prefill_windows.argtypes = [P, i32, i64, sz]
         L.kda_prefill_windows.restype = i32
+        L.kda_prefill_segments.argtypes = [P, i32, i64, sz]
+        L.kda_prefill_segments.restype = i32
         L.kda_prefill.argtypes = [P] + [_vp] * 6 + [ctypes.POINTER(ctypes.c_int64), i32, i64] + [_vp] * 5 + [_vp, sz, _vp]
         L.kda_prefill.restype = ctypes.c_int
         L.kda_prefill_with_events.argtypes = L.kda_prefill.argtypes + [ctypes.POINTER(_vp)]
@@ -170,6 +172,11 @@ def kda_prefill_workspace_bytes(params: Params, n_seqs: int, total_tokens: int) 
 def kda_prefill_windows(params: Params, n_seqs: int, total_tokens: int, workspace_bytes: int) -> int:
     """How many overlapped windows kda_prefill runs (1 = single pass)."""
     return int(lib().kda_prefill_windows(params.ref, int(n_seqs), int(total_tokens), int(workspace_bytes)))
+
+
+def kda_prefill_segments(params: Params, n_seqs: int, total_tokens: int, workspace_bytes: int) -> int:
+    """How many segments kda_prefill runs one sequence's recurrence as (0 = none)."""
+    return int(lib().kda_prefill_segments(params.ref, int(n_seqs), int(total_tokens), int(workspace_bytes)))
 
 
 def _cu_array(cu_seqlens: Sequence[int]):

@@ -603,6 +603,18 @@ int32_t kda_prefill_windows(const kda_params* p, int32_t n_seqs, int64_t total_t
     return 1;
 }
 
+int32_t kda_prefill_segments(const kda_params* p, int32_t n_seqs, int64_t total_tokens, size_t workspace_bytes) {
+    if (check_params(p) != KDA_OK || n_seqs < 0 || total_tokens < 0) return -1;
+    Algo algo;
+    if (resolve_algo(p, &algo) != KDA_OK) return -1;
+    if (algo != Algo::Chunked || n_seqs != 1) return 0;
+    SegPlan sp;
+    const int64_t n_chunks = (total_tokens + CHUNK - 1) / CHUNK;
+    if (plan_segments(p, total_tokens, layout(p, algo, 1, total_tokens, n_chunks).total, workspace_bytes, &sp))
+        return sp.P;
+    return 0;
+}
+
 kda_status kda_prefill(const kda_params* p, const void* q, const void* k, const void* v,
                        const void* z, const void* b, const void* gout,
                        const int64_t* cu_seqlens_host, int32_t n_seqs, int64_t total_tokens,

@@ -183,6 +183,14 @@ kda_status kda_prefill(const kda_params* p,
  * -1 for arguments kda_prefill would reject. */
 int32_t kda_prefill_windows(const kda_params* p, int32_t n_seqs, int64_t total_tokens, size_t workspace_bytes);
 
+/* The number of segments P >= 3 kda_prefill runs the recurrence of one
+ * sequence as (see kda_algo), or 0 when it does not segment; -1 for arguments
+ * kda_prefill would reject.  Like kda_prefill_windows it reads the current
+ * device's SM count and takes the caller's workspace size.  A segmented call
+ * launches the chunk preparation, two recurrence passes and the scan of the
+ * segment maps (besides the metadata and ring kernels every call runs). */
+int32_t kda_prefill_segments(const kda_params* p, int32_t n_seqs, int64_t total_tokens, size_t workspace_bytes);
+
 /* Same as kda_prefill, and records caller-created CUDA events on `stream` at
  * the stage boundaries, for profiling: stage_events[0] before the pre-stage,
  * [1] after the pre-stage (conv, norms, gate, beta), [2] after the chunk

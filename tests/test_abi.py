@@ -291,6 +291,17 @@ def test_prefill_windows_query(L):
     assert L.kda_prefill_windows(ctypes.byref(p), 1, 32768, 1 << 40) >= 1   # needs a device for more
 
 
+def test_prefill_segments_query(L):
+    p = params()
+    assert L.kda_prefill_segments(ctypes.byref(params(head_dim=64)), 1, 32768, 1 << 40) == -1
+    assert L.kda_prefill_segments(ctypes.byref(p), -1, 32768, 1 << 40) == -1
+    # several sequences, the scan path, or the plain chunked schedule: no segments
+    assert L.kda_prefill_segments(ctypes.byref(p), 2, 32768, 1 << 40) == 0
+    assert L.kda_prefill_segments(ctypes.byref(params(algo=kda.KDA_ALGO_SCAN)), 1, 32768, 1 << 40) == 0
+    assert L.kda_prefill_segments(ctypes.byref(params(algo=kda.KDA_ALGO_CHUNKED)), 1, 32768, 1 << 40) == 0
+    assert L.kda_prefill_segments(ctypes.byref(p), 1, 32768, 1 << 40) in (0, 9)   # 2 heads: 9 with a device
+
+
 @pytest.mark.parametrize("H", [8, 96])
 @pytest.mark.parametrize("T", [2048, 4096 + 37, 16384, 20384, 32768, 32768 + 64 * 7 + 5])
 def test_workspace_covers_overlapped_windows(L, T, H):

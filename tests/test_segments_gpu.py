@@ -120,7 +120,10 @@ def test_auto_picks_segments_from_four(H, T, auto_segments):
     big = 1 << 40
     if auto_segments:
         assert kda.kda_prefill_windows(auto, 1, T, big) == 1
+        assert kda.kda_prefill_segments(auto, 1, T, big) >= 4
+        assert kda.kda_prefill_segments(chunked, 1, T, big) == 0
         assert kda.kda_prefill_workspace_bytes(auto, 1, T) > kda.kda_prefill_workspace_bytes(chunked, 1, T)
     else:
         assert kda.kda_prefill_windows(auto, 1, T, big) == kda.kda_prefill_windows(chunked, 1, T, big)
+        assert kda.kda_prefill_segments(auto, 1, T, big) == 0
 
