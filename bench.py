@@ -547,6 +547,8 @@ def main():
     ap.add_argument("--workload", default="long", choices=sorted(PREFILL_WORKLOADS),
                     help="prefill workload of the headline line: long (T=32768, H=96; the default), "
                          "prefill (T=4096, H=32) or varlen (8 sequences, H=64); the others are for profiling")
+    ap.add_argument("--gate", default="bounded", choices=["bounded", "softplus"],
+                    help="decay gate of the headline prefill (softplus: the unbounded gate, for profiling)")
     ap.add_argument("--heads", type=int, default=None,
                     help="override the head count of the prefill workload (smaller cases for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -573,7 +575,7 @@ def main():
     kbuild.build()
 
     hbm, tc, tc_sus, peak_kind = peaks()
-    r = prefill_arm(args, dev, world, rank)
+    r = prefill_arm(args, dev, world, rank, gate=args.gate)
     w = r["w"]
     H, T = w.H, w.total_tokens
     value = whole_job_value(T, r["ms_max"], world)
@@ -585,9 +587,11 @@ def main():
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_max"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": kda_synth.describe(w.idx, w.H) + ", fp32 state",
+        "config": {"workload": kda_synth.describe(w.idx, w.H) + (", softplus gate" if args.gate == "softplus" else "")
+                               + ", fp32 state",
                    "global_batch": world * w.n_seqs, "seq_len": T, "heads": H, "algo": r["algo_resolved"],
-                   "schedule": ("single pass" if r["windows"] == 1 else
+                   "schedule": (f"{r['segments']} segments (kda_prefill_segments)" if r["segments"] else
+                                "single pass" if r["windows"] == 1 else
                                 f"{r['windows']} overlapped windows (kda_prefill_windows)"),
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": f"inputs ({sum(t.numel() * t.element_size() for t in w.tokens.fields()) / 1e9:.2f} GB) larger than L2 (129 MB); no flush"},

@@ -174,12 +174,17 @@ constexpr int64_t SEG_MIN_CHUNKS = 8;   // shortest segment
 constexpr int SMS_GB300 = 152;
 
 // The fewest segments a call runs as: KDA_ALGO_CHUNKED_SEGMENTS takes any
-// P >= 3; KDA_ALGO_AUTO takes P >= 4 (with P = 3, two thirds of the chain
-// remain serial and the overlapped windows are faster on GB300: 1.49 against
-// 1.67 ms for T = 32768, H = 32); KDA_ALGO_CHUNKED never segments.
-int segment_min(const kda_params* p) {
+// P >= 3 and KDA_ALGO_CHUNKED none.  KDA_ALGO_AUTO takes P >= 5, and P >= 3
+// for sequences of 64 to 128 chunks.  Measured on GB300 against the overlapped
+// windows: with P >= 5 segments halve the step of long few-head sequences
+// (T = 32768, H = 8: 1.07 -> 0.55 ms); with P = 3 or 4, two thirds or half of
+// the chain stay serial, after the whole preparation, and the windows, which
+// overlap the chain with the preparation, win on long sequences (T = 16384,
+// H = 32: 0.81 against 0.87 ms) while segments win from 4096 to 8192 tokens
+// (T = 4096, H = 32: 0.273 against 0.296 ms).
+int segment_min(const kda_params* p, int64_t chunks) {
     if (p->algo == KDA_ALGO_CHUNKED_SEGMENTS) return 3;
-    if (p->algo == KDA_ALGO_AUTO) return 4;
+    if (p->algo == KDA_ALGO_AUTO) return (chunks >= 64 && chunks <= 128) ? 3 : 5;
     return 1 << 30;
 }
 
@@ -202,7 +207,7 @@ bool segment_layout(const kda_params* p, int64_t T, int sms, size_t single_bytes
     const int64_t chunks = (T + CHUNK - 1) / CHUNK;
     const size_t slot = (size_t)p->num_heads * D * D * sizeof(float);
     const size_t base = align_up(single_bytes, WS_ALIGN);
-    const int P_min = segment_min(p);
+    const int P_min = segment_min(p, chunks);
     int P = segment_count(p->num_heads, sms, chunks);
     while (P >= P_min && ws_bytes != 0 && base + (size_t)(3 * P - 5) * slot > ws_bytes) --P;
     if (P < P_min || P < 3) return false;

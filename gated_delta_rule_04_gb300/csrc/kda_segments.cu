@@ -10,44 +10,58 @@
 // B_seg from running it from zero.  With X_1 = B_0 (the state after segment 0,
 // which starts from the caller's state), the state entering segment p + 1 is
 // X_{p+1} = M_p X_p + B_p.  Value columns never mix, so each CTA takes one
-// head and a block of 16 value columns through every segment in order.
+// head and a block of 8 value columns through every segment in order, M_p
+// passing through shared memory 32 keys at a time.
 #include "kda_chunk_layout.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int ST = 256;   // threads
-constexpr int VB = 16;    // value columns per CTA
+constexpr int ST = 128;   // threads: one key row each
+constexpr int VB = 8;     // value columns per CTA
+constexpr int JC = 32;    // keys of M_p staged in shared memory at a time
 
 __global__ void __launch_bounds__(ST) affine_scan_kernel(const __grid_constant__ ScanArgs2 a) {
-    __shared__ float xs[D][VB];   // X_p, this block of columns
+    __shared__ float xs[D][VB];        // X_p, this block of columns
+    __shared__ float ms[D][JC + 1];    // 32 columns of M_p (padded: row reads are conflict-free)
     const int h = blockIdx.x, vb = blockIdx.y * VB;
-    const int tid = threadIdx.x;
-    const int key = tid >> 1, vh = (tid & 1) * (VB / 2);   // thread: one key row, 8 value columns
+    const int key = threadIdx.x;
     const size_t hoff = (size_t)h * D * D;
     // X_1 = B_0
-    for (int i = tid; i < D * VB; i += ST) xs[i / VB][i % VB] = a.B[0][hoff + (size_t)(i / VB) * D + vb + i % VB];
-    __syncthreads();
+    for (int i = key; i < D * VB; i += ST) xs[i / VB][i % VB] = a.B[0][hoff + (size_t)(i / VB) * D + vb + i % VB];
     for (int p = 1; p + 1 < a.P; ++p) {
-        const float* Mp = a.M[p] + hoff + (size_t)key * D;
-        const float* Bp = a.B[p] + hoff + (size_t)key * D + vb + vh;
-        float acc[VB / 2];
+        const float* Mp = a.M[p] + hoff;
+        const float* Bp = a.B[p] + hoff + (size_t)key * D + vb;
+        float acc[VB];
 #pragma unroll
-        for (int e = 0; e < VB / 2; ++e) acc[e] = Bp[e];
-#pragma unroll 4
-        for (int j = 0; j < D; ++j) {
-            const float m = __ldg(Mp + j);
+        for (int e = 0; e < VB; ++e) acc[e] = Bp[e];
+        for (int jc = 0; jc < D; jc += JC) {
+            __syncthreads();   // the previous block of M_p (and X_p's update) is done with
+            // rows of 32 keys as float4: each warp reads four whole 128-byte row pieces
 #pragma unroll
-            for (int e = 0; e < VB / 2; ++e) acc[e] = fmaf(m, xs[j][vh + e], acc[e]);
+            for (int i = 0; i < D * JC / 4 / ST; ++i) {
+                const int idx = key + ST * i, r = idx >> 3, c = (idx & 7) * 4;
+                const float4 m4 = __ldg(reinterpret_cast<const float4*>(Mp + (size_t)r * D + jc + c));
+                ms[r][c] = m4.x;
+                ms[r][c + 1] = m4.y;
+                ms[r][c + 2] = m4.z;
+                ms[r][c + 3] = m4.w;
+            }
+            __syncthreads();
+#pragma unroll 8
+            for (int jj = 0; jj < JC; ++jj) {
+                const float m = ms[key][jj];
+#pragma unroll
+                for (int e = 0; e < VB; ++e) acc[e] = fmaf(m, xs[jc + jj][e], acc[e]);
+            }
         }
         __syncthreads();   // every thread has read X_p
-        float* Xn = a.X[p + 1] + hoff + (size_t)key * D + vb + vh;
+        float* Xn = a.X[p + 1] + hoff + (size_t)key * D + vb;
 #pragma unroll
-        for (int e = 0; e < VB / 2; ++e) {
-            xs[key][vh + e] = acc[e];
+        for (int e = 0; e < VB; ++e) {
+            xs[key][e] = acc[e];
             Xn[e] = acc[e];
         }
-        __syncthreads();
     }
 }
 

@@ -82,9 +82,12 @@ typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
  * a scan, then every segment again from its true starting state.  This
  * computes the same function up to rounding and takes the single-pass
  * workspace plus 3P - 5 states of H x 128 x 128 fp32 (included in
- * kda_prefill_workspace_bytes).  AUTO segments when P >= 4 segments of at
- * least 8 chunks fit (2P - 3 CTAs per head on the device's SMs); otherwise a
- * single sequence runs as the overlapped windows of kda_prefill_windows.
+ * kda_prefill_workspace_bytes).  AUTO segments when P >= 5 segments of at
+ * least 8 chunks fit (2P - 3 CTAs per head on the device's SMs), or P >= 3
+ * for a sequence of 64 to 128 chunks (measured on GB300: below and above that
+ * range the overlapped windows are as fast or faster with 3 or 4 segments);
+ * otherwise a single sequence runs as the overlapped windows of
+ * kda_prefill_windows.
  * CHUNKED_SEGMENTS segments from P = 3; CHUNKED never segments.
  * kda_prefill_algo reports CHUNKED for all three. */
 typedef enum { KDA_ALGO_AUTO = 0, KDA_ALGO_SCAN = 1, KDA_ALGO_CHUNKED = 2, KDA_ALGO_CHUNKED_SEGMENTS = 3 } kda_algo;

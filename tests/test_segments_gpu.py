@@ -109,18 +109,20 @@ def test_segments_workspace_reserve():
 
 
 @pytest.mark.parametrize("H, T, auto_segments", [(8, 4096, True), (16, 32768, True), (32, 32768, False),
-                                                 (8, 512, False)])
-def test_auto_picks_segments_from_four(H, T, auto_segments):
+                                                 (8, 512, False), (32, 4096, True), (32, 8192 + 64, False),
+                                                 (24, 16384, False)])
+def test_auto_picks_segments(H, T, auto_segments):
     """kda_prefill with KDA_ALGO_AUTO runs one sequence as segments when at
-    least four fit the SMs (2P - 3 CTAs per head, 8 chunks per segment);
-    otherwise the overlapped windows where they apply."""
+    least five fit the SMs (2P - 3 CTAs per head, 8 chunks per segment), or
+    three for 64 to 128 chunks; otherwise the overlapped windows where they
+    apply."""
     p = kda_synth.draw_params(H, 221)
     auto = kda_params(p, "bf16", algo="auto")
     chunked = kda_params(p, "bf16", algo="chunked")
     big = 1 << 40
     if auto_segments:
         assert kda.kda_prefill_windows(auto, 1, T, big) == 1
-        assert kda.kda_prefill_segments(auto, 1, T, big) >= 4
+        assert kda.kda_prefill_segments(auto, 1, T, big) >= 3
         assert kda.kda_prefill_segments(chunked, 1, T, big) == 0
         assert kda.kda_prefill_workspace_bytes(auto, 1, T) > kda.kda_prefill_workspace_bytes(chunked, 1, T)
     else:
