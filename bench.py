@@ -526,7 +526,8 @@ def other_workload(args, dev, world, rank, idx, hbm, tc, tc_sus, peak_kind, head
     else:
         schedule = "single pass" if r["windows"] == 1 else f"{r['windows']} overlapped windows"
     gate_txt = ", softplus gate" if gate == "softplus" else ""
-    if gate == "softplus":   # the stored counters are the bounded-gate kernel's
+    if gate == "softplus" or r["segments"]:
+        # the stored counters are the bounded-gate kernels' in the single pass
         rep["roofline"]["traffic"] = None
     return {"workload": kda_synth.describe(w.idx, w.H) + gate_txt + ", fp32 state", "metric": "KDA tokens/s/layer",
             "value": whole_job_value(w.total_tokens, r["ms_max"], world), "unit": "tokens/s/layer",

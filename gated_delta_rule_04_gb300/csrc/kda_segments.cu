@@ -27,27 +27,40 @@ __global__ void __launch_bounds__(ST) affine_scan_kernel(const __grid_constant__
     const int h = blockIdx.x, vb = blockIdx.y * VB;
     const int key = threadIdx.x;
     const size_t hoff = (size_t)h * D * D;
+    constexpr int NLD = D * JC / 4 / ST;   // float4 loads per thread per block of M_p
+    // the next block of M_p is loaded into registers while the current one is used:
+    // the loads do not depend on X, so the chain waits for one block's latency at most
+    float4 nx[NLD];
+    auto load_block = [&](int p, int jc) {
+        const float* Mp = a.M[p] + hoff;
+#pragma unroll
+        for (int i = 0; i < NLD; ++i) {
+            const int idx = key + ST * i, r = idx >> 3, c = (idx & 7) * 4;
+            nx[i] = __ldg(reinterpret_cast<const float4*>(Mp + (size_t)r * D + jc + c));
+        }
+    };
     // X_1 = B_0
     for (int i = key; i < D * VB; i += ST) xs[i / VB][i % VB] = a.B[0][hoff + (size_t)(i / VB) * D + vb + i % VB];
+    load_block(1, 0);
     for (int p = 1; p + 1 < a.P; ++p) {
-        const float* Mp = a.M[p] + hoff;
         const float* Bp = a.B[p] + hoff + (size_t)key * D + vb;
         float acc[VB];
 #pragma unroll
         for (int e = 0; e < VB; ++e) acc[e] = Bp[e];
         for (int jc = 0; jc < D; jc += JC) {
             __syncthreads();   // the previous block of M_p (and X_p's update) is done with
-            // rows of 32 keys as float4: each warp reads four whole 128-byte row pieces
+            // rows of 32 keys as float4: each warp holds four whole 128-byte row pieces
 #pragma unroll
-            for (int i = 0; i < D * JC / 4 / ST; ++i) {
+            for (int i = 0; i < NLD; ++i) {
                 const int idx = key + ST * i, r = idx >> 3, c = (idx & 7) * 4;
-                const float4 m4 = __ldg(reinterpret_cast<const float4*>(Mp + (size_t)r * D + jc + c));
-                ms[r][c] = m4.x;
-                ms[r][c + 1] = m4.y;
-                ms[r][c + 2] = m4.z;
-                ms[r][c + 3] = m4.w;
+                ms[r][c] = nx[i].x;
+                ms[r][c + 1] = nx[i].y;
+                ms[r][c + 2] = nx[i].z;
+                ms[r][c + 3] = nx[i].w;
             }
             __syncthreads();
+            if (jc + JC < D) load_block(p, jc + JC);
+            else if (p + 2 < a.P) load_block(p + 1, 0);
 #pragma unroll 8
             for (int jj = 0; jj < JC; ++jj) {
                 const float m = ms[key][jj];
