@@ -305,15 +305,19 @@ def test_prefill_segments_query(L):
 @pytest.mark.parametrize("H", [8, 96])
 @pytest.mark.parametrize("T", [2048, 4096 + 37, 16384, 20384, 32768, 32768 + 64 * 7 + 5])
 def test_workspace_covers_overlapped_windows(L, T, H):
-    """A single sequence may run as up to 4 windows of at least 1024 tokens
-    (up to 64 heads) or 8192 tokens (more heads); the workspace query covers
-    two windows' records (window sizes round up to whole 64-token chunks)."""
+    """A single sequence may run as up to 4 windows (at least 1024 tokens per
+    window up to 64 heads, 8192 with more), the last one 1/d as long as the
+    others (d = 4 above 32 heads, 2 up to 32); the workspace query covers two
+    windows' records (window sizes round up to whole 64-token chunks)."""
     rec = 74240
     p = params(num_heads=H)
     need = L.kda_prefill_workspace_bytes(ctypes.byref(p), 1, T)
     windows = min(4, T // (1024 if H <= 64 else 8192))
     if windows >= 2:
-        seg_chunks = -(-(-(-T // windows)) // 64)
+        d = 4 if H > 32 else 2
+        seg = -(-(d * T) // (d * windows - d + 1))
+        seg_chunks = -(-seg // 64)
+        assert (windows - 1) * seg_chunks * 64 < T <= windows * seg_chunks * 64   # no empty last window
         assert need >= 2 * seg_chunks * H * rec
     # and never less than the single pass needs for several sequences' worth of chunks
     assert need >= (T // 64 + 1) * H * rec
