@@ -453,3 +453,44 @@ def test_ring_in_place_alias():
     ring = rng.standard_normal((1, 3, 3, H * D))
     ref = oracle.mixer(p, [0, 2], **tk, ring_in=ring.copy())
     np.testing.assert_array_equal(ref["ring"][0, :, 0], ring[0, :, 2])
+
+def test_p13_recurrence_is_affine_in_its_starting_state():
+    """The segment maps of a context-parallel split rest on this: over any run
+    of tokens the final state is M S_0 + B with M independent of S_0 and of the
+    values, and B independent of S_0 (each step is S <- (I - beta k k^T)
+    Diag(e^g) S + beta k v^T).  Checked on the oracle's recurrence: the
+    difference to the zero start is linear in S_0, unchanged when the values
+    change, and the zero-start run is the values' part alone."""
+    rng = np.random.default_rng(13)
+    T, H, D = 24, 2, 8
+    q, k, v, g, beta = rand_core(rng, T, H, D, g_lo=-0.05)
+    beta = 0.2 * beta   # a long memory, so that the start still matters at the end
+    S1, S2 = rng.standard_normal((2, H, D, D))
+    zero = np.zeros((H, D, D))
+    _, B = oracle.core(q, k, v, g, beta, zero)
+    _, E1 = oracle.core(q, k, v, g, beta, S1)
+    _, E2 = oracle.core(q, k, v, g, beta, S2)
+    _, E12 = oracle.core(q, k, v, g, beta, 2.0 * S1 - 3.0 * S2)
+    # linear part: M S for S1, S2 and a combination
+    np.testing.assert_allclose(E12 - B, 2.0 * (E1 - B) - 3.0 * (E2 - B), rtol=0, atol=1e-12)
+    # M does not depend on the values: the same difference with other values
+    v2 = rng.standard_normal(v.shape)
+    _, B2 = oracle.core(q, k, v2, g, beta, zero)
+    _, E1b = oracle.core(q, k, v2, g, beta, S1)
+    np.testing.assert_allclose(E1b - B2, E1 - B, rtol=0, atol=1e-12)
+    # the part of the values alone: zero values give a zero offset
+    _, B0 = oracle.core(q, k, np.zeros_like(v), g, beta, zero)
+    np.testing.assert_allclose(B0, 0.0, atol=0)
+    # the linear part is not trivial on these inputs (the start still matters)
+    assert np.linalg.norm(E1 - B) > 0.1 * np.linalg.norm(S1)
+    # and composing two runs' maps gives the whole run
+    half = T // 2
+    _, Bh1 = oracle.core(q[:half], k[:half], v[:half], g[:half], beta[:half], zero)
+    _, Bh2 = oracle.core(q[half:], k[half:], v[half:], g[half:], beta[half:], zero)
+    _, Eh2 = oracle.core(q[half:], k[half:], v[half:], g[half:], beta[half:], Bh1)
+    np.testing.assert_allclose(Eh2, B, rtol=0, atol=1e-12)
+    # the maps compose: M S_1 = M_2 (M_1 S_1), with M_i X the run from X minus
+    # the run from zero (B_2 is what a context-parallel rank would send)
+    _, E1h1 = oracle.core(q[:half], k[:half], v[:half], g[:half], beta[:half], S1)
+    _, M2M1 = oracle.core(q[half:], k[half:], v[half:], g[half:], beta[half:], E1h1 - Bh1)
+    np.testing.assert_allclose(M2M1 - Bh2, E1 - B, rtol=0, atol=1e-12)
