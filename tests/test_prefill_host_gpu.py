@@ -62,6 +62,20 @@ def test_host_prefill_matches_oracle(io, cu, seg):
     np.testing.assert_array_equal(ring.double().cpu().numpy(), ref["ring"])
 
 
+def test_host_prefill_softplus_gate_matches_oracle():
+    """The unbounded softplus gate through the host-buffer prefill (each
+    segment on the chunked form), cuts inside chunks."""
+    io, cu = "bf16", [0, 70, 300, 301]
+    p, tk, S0, ring0 = inputs(io, cu, seed=85)
+    p.gate_kind = 1
+    o, S, ring = run_host(p, tk, cu, io, 100, S0, ring0)
+    ref = oracle_run(p, tk, cu, S_in=S0, ring_in=ring0)
+    tol = tol_for(io)
+    assert_close("o", o, ref["o"], tol)
+    assert_close("S", S, ref["S"], tol)
+    np.testing.assert_array_equal(ring.double().cpu().numpy(), ref["ring"])
+
+
 def test_host_prefill_in_place_zero_start():
     """No initial state or ring (zeros), and the in-place form."""
     io, cu = "bf16", [0, 150, 400]

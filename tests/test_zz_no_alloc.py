@@ -53,11 +53,12 @@ def call_noalloc(f, kp, tokens, cu, S_in=None, ring_in=None):
     return st, o, S_out, ring_out
 
 
-@pytest.mark.parametrize("io, algo", [("bf16", "auto"), ("f32", "scan")])
-def test_noalloc_matches_kda_prefill_twice(io, algo):
+@pytest.mark.parametrize("io, algo, gate_kind", [("bf16", "auto", 0), ("f32", "scan", 0), ("bf16", "auto", 1)])
+def test_noalloc_matches_kda_prefill_twice(io, algo, gate_kind):
     f = noalloc_fn()
     H = 4
     p = kda_synth.draw_params(H, 21)
+    p.gate_kind = gate_kind   # 1: the softplus gate (chunked form with bf16 I/O)
     kp = kda_params(p, io, algo)
     g = torch.Generator().manual_seed(22)
     cases = [[130, 7, 64], [3, 200, 1, 65]]  # second call: other shapes, nonzero state and ring
