@@ -76,6 +76,24 @@ def test_host_prefill_softplus_gate_matches_oracle():
     np.testing.assert_array_equal(ring.double().cpu().numpy(), ref["ring"])
 
 
+def test_host_prefill_segments_that_run_as_segmented_recurrences():
+    """Host segments of 4096 tokens of one 8192-token sequence with 32 heads:
+    each runs its recurrence as 3 segments (affine maps composed by a scan);
+    sampled heads against the oracle."""
+    io, cu, H = "bf16", [0, 8192], 32
+    p, tk, S0, ring0 = inputs(io, cu, H=H, seed=89)
+    kp = kda_params(p, io)
+    assert kda.kda_prefill_segments(kp, 1, 4096, 1 << 40) == 3
+    o, S, ring = run_host(p, tk, cu, io, 4096, S0, ring0)
+    heads = [0, 31]
+    ref = oracle_run(p, tk, cu, S_in=S0, ring_in=ring0, heads=heads)
+    cols = head_cols(heads)
+    tol = tol_for(io)
+    assert_close("o", o[:, cols], ref["o"], tol)
+    assert_close("S", S[:, heads], ref["S"], tol)
+    np.testing.assert_array_equal(ring[..., cols].double().cpu().numpy(), ref["ring"])
+
+
 def test_host_prefill_in_place_zero_start():
     """No initial state or ring (zeros), and the in-place form."""
     io, cu = "bf16", [0, 150, 400]

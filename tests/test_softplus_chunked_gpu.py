@@ -129,3 +129,16 @@ def test_softplus_chunked_segments_vs_oracle():
     o, S, ring = run(p, tk, [0, T], S_in=S_in)
     check(p, tk, [0, T], o, S, ring, S_in=S_in, heads=[1, 3])
     assert math.isfinite(float(S.abs().max()))
+
+
+def test_softplus_chunked_windows_vs_oracle():
+    """The softplus gate under the overlapped windows (one sequence of 8256
+    tokens, 8 heads, KDA_ALGO_CHUNKED), sampled heads against the oracle."""
+    T, H = 8192 + 64, 8
+    p = softplus_params(H, 341)
+    tk = kda_synth.draw_tokens(T, H, 342, torch.bfloat16)
+    kp = kda_params(p, "bf16", algo="chunked")
+    assert kda.kda_prefill_windows(kp, 1, T, kda.kda_prefill_workspace_bytes(kp, 1, T)) >= 2
+    o, S, ring = run(p, tk, [0, T], algo="chunked")
+    check(p, tk, [0, T], o, S, ring, heads=[0, 7])
+
