@@ -138,13 +138,15 @@ int64_t window_min(int H) { return H <= 64 ? 1024 : 8192; }
 bool overlap_layout(const kda_params* p, int64_t T, OverlapPlan* pl) {
     const int64_t wmin = window_min(p->num_heads);
     if (T < 2 * wmin) return false;
-    const int64_t s0 = std::min<int64_t>(4, T / wmin);   // up to 4 windows of at least wmin tokens
-    // The last window's recurrence runs alone, after every preparation, so the last
-    // window is shorter than the others: 1/d of their length, d = 4 above 32 heads
-    // and 2 up to 32 (GB300, four windows: T = 32768 with 96 heads 3.85 -> 3.78 ms,
-    // with 64 heads 2.66 -> 2.57 ms, with 32 heads 1.50 -> 1.47 ms; a quarter was
-    // slower than a half with 32 heads, 1.52 ms).
-    const int64_t d = p->num_heads > 32 ? 4 : 2;
+    // Up to 4 windows of at least wmin tokens (3 above 48 heads), the last one 1/d
+    // as long as the others, since its recurrence runs alone after every
+    // preparation: d = 6 above 64 heads, 4 above 32, 2 up to 32.  Measured on
+    // GB300 at T = 32768: 96 heads 3.85 ms with four equal windows, 3.78 with
+    // four and d = 4, 3.72 with three and d = 6; 64 heads 2.66 / 2.56 (four,
+    // d = 4) / 2.55 (three, d = 4); 48 heads 2.04 with four and d = 4 against
+    // 2.06 with three; 32 heads 1.50 / 1.47 (four, d = 2) against 1.51 with three.
+    const int64_t s0 = std::min<int64_t>(p->num_heads > 48 ? 3 : 4, T / wmin);
+    const int64_t d = p->num_heads > 64 ? 6 : p->num_heads > 32 ? 4 : 2;
     const int64_t seg = ((d * T + d * s0 - d) / (d * s0 - (d - 1)) + CHUNK - 1) / CHUNK * CHUNK;
     pl->S = (int)((T + seg - 1) / seg);
     if (pl->S < 2) return false;

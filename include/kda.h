@@ -174,11 +174,13 @@ kda_status kda_prefill(const kda_params* p,
  * pass, S >= 2 when one long sequence's recurrence would leave SMs idle
  * (chunked path, one sequence, fewer heads than SMs, at least 2048 tokens
  * with up to 64 heads or 16384 with more, and a workspace that holds two
- * windows' records).  Then the sequence runs as S <= 4 windows of whole
- * chunks of at least 1024 tokens (up to 64 heads) or 8192 tokens each, the
- * last shorter by the rounding to chunks.  Window w's chunk preparation
- * overlaps the recurrence of window w - 1 on a second, high-priority stream,
- * and the result is bit-identical to the single pass.  That stream and seven
+ * windows' records).  Then the sequence runs as S <= 4 windows (S <= 3
+ * above 48 heads) of whole chunks, of at least 1024 tokens (up to 64 heads) or
+ * 8192 tokens each except the last, which is 1/d as long as the others (d = 6
+ * above 64 heads, 4 above 32, 2 up to 32): its recurrence runs alone.
+ * Window w's chunk preparation overlaps the recurrence of window w - 1 on a
+ * second, high-priority stream, and the result is bit-identical to the single
+ * pass.  That stream and seven
  * events are created on a host thread's first windowed call on a device and
  * kept for the thread's lifetime (one set per thread and device, never
  * shared between threads).  A call that runs as segments (see kda_algo)

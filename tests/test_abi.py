@@ -302,19 +302,20 @@ def test_prefill_segments_query(L):
     assert L.kda_prefill_segments(ctypes.byref(p), 1, 32768, 1 << 40) in (0, 9)   # 2 heads: 9 with a device
 
 
-@pytest.mark.parametrize("H", [8, 96])
+@pytest.mark.parametrize("H", [8, 48, 64, 96])
 @pytest.mark.parametrize("T", [2048, 4096 + 37, 16384, 20384, 32768, 32768 + 64 * 7 + 5])
 def test_workspace_covers_overlapped_windows(L, T, H):
-    """A single sequence may run as up to 4 windows (at least 1024 tokens per
-    window up to 64 heads, 8192 with more), the last one 1/d as long as the
-    others (d = 4 above 32 heads, 2 up to 32); the workspace query covers two
-    windows' records (window sizes round up to whole 64-token chunks)."""
+    """A single sequence may run as up to 4 windows (3 above 48 heads; at least
+    1024 tokens per window up to 64 heads, 8192 with more), the last one 1/d as
+    long as the others (d = 6 above 64 heads, 4 above 32, 2 up to 32); the
+    workspace query covers two windows' records (window sizes round up to whole
+    64-token chunks)."""
     rec = 74240
     p = params(num_heads=H)
     need = L.kda_prefill_workspace_bytes(ctypes.byref(p), 1, T)
-    windows = min(4, T // (1024 if H <= 64 else 8192))
+    windows = min(3 if H > 48 else 4, T // (1024 if H <= 64 else 8192))
     if windows >= 2:
-        d = 4 if H > 32 else 2
+        d = 6 if H > 64 else 4 if H > 32 else 2
         seg = -(-(d * T) // (d * windows - d + 1))
         seg_chunks = -(-seg // 64)
         assert (windows - 1) * seg_chunks * 64 < T <= windows * seg_chunks * 64   # no empty last window
