@@ -77,7 +77,9 @@ def test_clock_summary_uses_samples_inside_the_region():
     c.lines = [(9.0, "900, 2070, 300, Not Active, Not Active, Not Active, Not Active\n"),
                (10.2, "2070, 2070, 900, Not Active, Not Active, Not Active, Active\n"),
                (10.4, "2055, 2070, 950, Not Active, Not Active, Not Active, Not Active\n"),
-               (10.515, "2040, 2070, 950, Not Active, Not Active, Not Active, Not Active\n"),
+               # half a sampling period after the region closed: it still covers the end
+               (10.5 + bench.Clocks.PERIOD_MS / 2000,
+                "2040, 2070, 950, Not Active, Not Active, Not Active, Not Active\n"),
                (12.0, "600, 2070, 100, Active, Not Active, Not Active, Not Active\n")]
     s = c.summary()
     assert s["samples"] == 3
