@@ -119,8 +119,12 @@ constexpr uint32_t S_RAW = 0;                      // bf16 [3 planes][67 rows][1
                                                    //   is read before this item's tiles are written
 constexpr uint32_t S_LAP = 0;                      // bf16 2 x [128 rows][128 keys]: A / off-diagonal P left rows
 constexpr uint32_t S_QD = S_LAP + 65536;           // bf16 [128][128]: rows 0-63 q hi, 64-127 q lo
-constexpr uint32_t S_DG = S_QD;                    //   softplus gate: fp32 [2 slots][4 sub-tiles][2 halves][256]
-                                                   //   position-pair sums of the diagonal blocks (no split P)
+constexpr uint32_t S_DG = S_QD;                    //   softplus gate (no split P): fp32 [2 slots][4 sub-tiles]
+                                                   //   [2 halves][128] position-pair sums of the diagonal
+                                                   //   blocks below level 3, then the level-3 operand tiles:
+constexpr uint32_t S_L3A = S_QD + 8192;            //   fp16 2 panels x [64 rows][64 ch]: k^, q^ of rows 8-15
+constexpr uint32_t S_L3B = S_QD + 24576;           //   fp16 2 panels x [32 rows][64 ch]: k^ of columns 0-7
+constexpr uint32_t S_L3T = 0;                      //   (offset in the X tile) fp32 [A, P][4][8][8] level-3 sums
 constexpr uint32_t S_RHL = S_QD + 32768;           // bf16 [128][128 keys] R: rows 0-63 hi, 64-127 lo
 constexpr uint32_t S_TT = S_RHL + 32768;           // fp16 [64 r][64 s] T; the W product reads it as 128 A
                                                    //   rows, rows 64-127 being the first 8 KiB of (k e^G)^T
@@ -144,7 +148,9 @@ static_assert(S_RAW + 3 * RAW_PLANE <= S_QD, "raw rows inside the left-row tiles
 static_assert(S_KPT == S_TT + 8192, "the W product's junk A rows are the first 8 KiB of (k e^G)^T");
 static_assert(S_WUST + 32768 <= S_NRM, "W / U0^T staging inside the solve tiles");
 static_assert(S_XM + 64 * 16 * 4 <= S_NRM, "lo*hi exchange inside X");
-static_assert(2 * 4 * 2 * 256 * 4 <= 32768, "diagonal pair sums inside the diagonal-P operand tile");
+static_assert(2 * 4 * 2 * 128 * 4 <= S_L3A - S_DG && S_L3B + 2 * 4096 == S_QD + 32768,
+              "pair sums and level-3 tiles inside the diagonal-P operand tile");
+static_assert(S_L3A % 1024 == 0 && S_L3B % 1024 == 0, "level-3 tiles on 1 KiB boundaries");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 static_assert(S_LAP % 1024 == 0 && S_QD % 1024 == 0 && S_RHL % 1024 == 0 && S_TT % 1024 == 0 &&
                   S_KPT % 1024 == 0 && S_VT % 1024 == 0,
@@ -213,6 +219,12 @@ __device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, uint32_t (&r)[16]) 
         : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 32 lanes x 8 consecutive 32-bit TMEM columns, without waiting.
+__device__ __forceinline__ void tmem_ld8_nw(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
 
 // Waits for phase `parity` of an mbarrier for at most `limit_ns`, giving up
 // early once the CTA's abort flag is set.  Returns false when it gave up; a
@@ -290,13 +302,17 @@ __device__ __forceinline__ void solve_level(const float* Am, float* Xm, int bt) 
 // pair takes its factor from a recursive halving of the 16-token sub-tile:
 // at level t (halves of h = 2^t tokens) the pairs with r in the upper and s in
 // the lower half of a 2h-block use the last token m of the lower half,
-// e^{G_r - G_s} = e^{G_r - G_m} e^{G_m - G_s}, both factors <= 1.  Pair values
-// are numbered level by level (t = 3, 2, 1, 0), block by block, row by row,
-// A before P within a row; the 16 values P[r][r] come last (indices 240 + r).
+// e^{G_r - G_s} = e^{G_r - G_m} e^{G_m - G_s}, both factors <= 1.  Level 3
+// (rows 8-15 against columns 0-7 through token 7, 64 of the 120 A pairs and 64
+// of the 136 P pairs) is one rank-128 product per sub-tile, so it runs on the
+// tensor cores in fp16 (every factor <= 1); the other pair values are
+// numbered level by level (t = 2, 1, 0), block by block, row by row, A before
+// P within a row, and the 16 values P[r][r] come last (indices 112 + r).
+__device__ __forceinline__ bool dg_level3(int jr, int js) { return jr >= 8 && js < 8; }
 __device__ __forceinline__ int dg_index(int jr, int js, int isP) {
-    if (jr == js) return 240 + jr;
+    if (jr == js) return 112 + jr;
     const int t = 31 - __clz(jr ^ js), h = 1 << t, b0 = (jr >> (t + 1)) << (t + 1);
-    const int lvl = t == 3 ? 0 : t == 2 ? 128 : t == 1 ? 192 : 224;
+    const int lvl = t == 2 ? 0 : t == 1 ? 64 : 96;
     return lvl + (b0 >> (t + 1)) * 2 * h * h + (jr - b0 - h) * 2 * h + isP * h + (js - b0);
 }
 
@@ -673,11 +689,15 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                 nvk = rsqrtf(mine.y + other.y + a.l2_eps);
             }
             if (SP) {
-                // ---- the diagonal blocks of A and P by position pairs (see dg_index):
-                // this thread's two channels' share of every pair sum of its sub-tile,
-                // on the conv outputs (the norm factors of both tokens are applied after
-                // the sum over the warp's 64 channels); the back adds the two warps
-                float* dg = reinterpret_cast<float*>(sb + S_DG) + (((k_iter & 1u) * 4 + a_sub) * 2 + hf) * 256;
+                // ---- the diagonal blocks of A and P by position pairs (see dg_index).
+                // Level 3: this thread's two channels of k^ and q^ (norm factor and
+                // e^{G_r - G_7}) for rows 8-15 and of k^ (norm factor and e^{G_7 - G_s})
+                // for columns 0-7 into the level-3 operand tiles, for the back's first
+                // tcgen05 batch.  Levels 2-0: this thread's share of every pair sum of its
+                // sub-tile, on the conv outputs (the norm factors of both tokens are
+                // applied after the sum over the warp's 64 channels); the back adds the
+                // two warps.
+                float* dg = reinterpret_cast<float*>(sb + S_DG) + (((k_iter & 1u) * 4 + a_sub) * 2 + hf) * 128;
                 auto ex2d = [&](float2 hi, float2 lo) {   // e^{hi - lo} per channel (hi <= lo)
                     return make_float2(ex2f((hi.x - lo.x) * LOG2E), ex2f((hi.y - lo.y) * LOG2E));
                 };
@@ -692,27 +712,29 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                     const float nk_s = __shfl_sync(0xffffffffu, nvk, 2 * js);
                     if ((lane & 1) == 0) dg[16 * kb + q] = sum * (isP ? nq_r : nk_r) * nk_s;
                 };
-                // level 3: rows 8-15 against columns 0-7, through token 7
+                // level 3 operand tiles: fp16, K-major with the 128-byte swizzle; channel
+                // pair c0 sits at chunk lane / 4, bytes 4 (lane & 3) of a 128-byte row of
+                // panel hf; rows 8 a_sub + i are one 8-row swizzle group
                 {
-                    float2 ks[8];
+                    const uint32_t cpart = ((uint32_t)(lane >> 2)) << 4, cbyte = 4u * (lane & 3);
+                    unsigned char* const tA = sb + S_L3A + (uint32_t)hf * 8192u + (uint32_t)(8 * a_sub) * 128u + cbyte;
+                    unsigned char* const tB = sb + S_L3B + (uint32_t)hf * 4096u + (uint32_t)(8 * a_sub) * 128u + cbyte;
 #pragma unroll
-                    for (int s = 0; s < 8; ++s) ks[s] = s == 7 ? h2f(ak[7]) : __fmul2_rn(h2f(ak[s]), ex2d(gc[7], gc[s]));
-#pragma unroll 1
-                    for (int kb = 0; kb < 8; ++kb) {
-                        const int r = 8 + kb;
-                        float2 gr = gc[8], akr = h2f(ak[8]), aqr = h2f(aq[8]);
-#pragma unroll
-                        for (int i = 9; i < 16; ++i)
-                            if (r == i) gr = gc[i], akr = h2f(ak[i]), aqr = h2f(aq[i]);
-                        const float2 rho = ex2d(gr, gc[7]);
-                        const float2 kr = __fmul2_rn(akr, rho), qr = __fmul2_rn(aqr, rho);
-                        float v[16];
-#pragma unroll
-                        for (int s = 0; s < 8; ++s) {
-                            v[s] = dot2(kr, ks[s]);
-                            v[8 + s] = dot2(qr, ks[s]);
-                        }
-                        finish(v, kb, r, q & 7, q >> 3);
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t ro = 128u * i + (cpart ^ ((uint32_t)i << 4));
+                        // column s = i: k^_s e^{G_7 - G_s}
+                        const float nks = __shfl_sync(0xffffffffu, nvk, 2 * i);
+                        float2 ks = __fmul2_rn(h2f(ak[i]), f2(nks));
+                        if (i < 7) ks = __fmul2_rn(ks, ex2d(gc[7], gc[i]));
+                        sts32(tB + ro, pack_f16(ks.x, ks.y));
+                        // row r = 8 + i: k^_r and q^_r times e^{G_r - G_7}
+                        const float nkr = __shfl_sync(0xffffffffu, nvk, 2 * (8 + i));
+                        const float nqr = __shfl_sync(0xffffffffu, nvq, 2 * (8 + i));
+                        const float2 rho = ex2d(gc[8 + i], gc[7]);
+                        const float2 kr = __fmul2_rn(__fmul2_rn(h2f(ak[8 + i]), f2(nkr)), rho);
+                        const float2 qr = __fmul2_rn(__fmul2_rn(h2f(aq[8 + i]), f2(nqr)), rho);
+                        sts32(tA + ro, pack_f16(kr.x, kr.y));
+                        sts32(tA + 32u * 128u + ro, pack_f16(qr.x, qr.y));
                     }
                 }
                 // level 2: in each half, rows 4-7 against columns 0-3, through token 3
@@ -737,7 +759,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                                 v[8 * rr + 4 + s] = dot2(qr, ks[s]);
                             }
                         }
-                        finish(v, 8 + 2 * bb + half, 8 * bb + 4 + 2 * half + (q >> 3), 8 * bb + (q & 3), (q >> 2) & 1);
+                        finish(v, 2 * bb + half, 8 * bb + 4 + 2 * half + (q >> 3), 8 * bb + (q & 3), (q >> 2) & 1);
                     }
                 }
                 // level 1: in each quarter, rows 2-3 against columns 0-1, through token 1
@@ -760,7 +782,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                         }
                     }
                     const int bb = 2 * hb + (q >> 3), w = q & 7;
-                    finish(v, 12 + hb, 4 * bb + 2 + (w >> 2), 4 * bb + (w & 1), (w >> 1) & 1);
+                    finish(v, 4 + hb, 4 * bb + 2 + (w >> 2), 4 * bb + (w & 1), (w >> 1) & 1);
                 }
                 // level 0: each odd row against the token before it
                 {
@@ -772,14 +794,14 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                         v[2 * bb] = dot2(h2f(ak[r]), ks);
                         v[2 * bb + 1] = dot2(h2f(aq[r]), ks);
                     }
-                    finish(v, 14, 2 * (q >> 1) + 1, 2 * (q >> 1), q & 1);
+                    finish(v, 6, 2 * (q >> 1) + 1, 2 * (q >> 1), q & 1);
                 }
                 // P[r][r]
                 {
                     float v[16];
 #pragma unroll
                     for (int r = 0; r < 16; ++r) v[r] = dot2(h2f(aq[r]), h2f(ak[r]));
-                    finish(v, 15, q, q, 1);
+                    finish(v, 7, q, q, 1);
                 }
             }
             // ---- per-channel factors from the sub-tile ends G_en(b):
@@ -979,6 +1001,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         const int bt = tid - NF, bw = warp - NF / 32;   // 0..255, 0..7
         const int qd = warp & 3;                          // TMEM lane quarter of this warp
         const float* dgb = reinterpret_cast<const float*>(sb + S_DG);
+        float* l3t = reinterpret_cast<float*>(sb + S_XM + S_L3T);   // free until the diagonal inverses
         uint32_t k = 0;
 #pragma unroll 1
         while (true) {
@@ -1007,6 +1030,16 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                         ptx::mma_f16(tmem + TM_D2, ptx::sdesc_sw128(base + S_QD + pn * 16384 + koff), bR,
                                      IDESC_BF16_N128, kk > 0);
                 }
+                if (SP) {   // the diagonal blocks' level-3 pairs: [k^ rows; q^ rows] x columns
+                    constexpr uint32_t IDESC_L3 = ptx::idesc_f16_f32(128, 32);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t koff = (kk & 3) * 32, pn = kk >> 2;
+                        // (A rows 64-127 are the next tile's bytes; their lanes are not read)
+                        ptx::mma_f16(tmem + TM_D2, ptx::sdesc_sw128(base + S_L3A + pn * 8192 + koff),
+                                     ptx::sdesc_sw128(base + S_L3B + pn * 4096 + koff), IDESC_L3, kk > 0);
+                    }
+                }
                 ptx::mma_commit(bar_mma1);
             }
             const float* bta = btab + (k % NSLOT) * C;
@@ -1023,6 +1056,30 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
             ptx::tc_fence_before();
             if (ptx::bar_sync_or(BAR_BACK, NB, bad)) break;
             ptx::tc_fence_after();
+
+            // ---- unbounded gate: the level-3 pair sums of the diagonal blocks, from the
+            // diagonal 8 x 8 blocks of the tcgen05 product (warp 8: k^ rows, lanes 0-31;
+            // warp 9: q^ rows, lanes 32-63; row 8 a + i of sub-tile a), to l3t
+            if (SP) {
+                if (bw < 2) {
+                    const uint32_t taddr = tmem + ((uint32_t)(32 * qd) << 16) + TM_D2;
+                    const int a3 = lane >> 3, i3 = lane & 7;
+                    float* dst = l3t + (bw * 4 + a3) * 64 + i3 * 8;
+#pragma unroll 1
+                    for (int g = 0; g < 4; ++g) {   // column block g; lanes of sub-tile g keep it
+                        uint32_t rg[8];
+                        tmem_ld8_nw(taddr + 8 * g, rg);
+                        tmem_wait_ld();
+                        if (a3 == g) {
+                            *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(rg[0]), __uint_as_float(rg[1]),
+                                                                          __uint_as_float(rg[2]), __uint_as_float(rg[3]));
+                            *reinterpret_cast<float4*>(dst + 4) = make_float4(__uint_as_float(rg[4]), __uint_as_float(rg[5]),
+                                                                              __uint_as_float(rg[6]), __uint_as_float(rg[7]));
+                        }
+                    }
+                }
+                bar_sync_n(BAR_BACK, NB);
+            }
 
             // ---- read out A (to fp32 Am, times beta_r) and the off-diagonal P (to its
             // staging tile).  A warp's 32 rows need the 16-column block of their column
@@ -1041,13 +1098,15 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                 float v[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(b == b_first ? r0[i] : r1[i]);
-                if (SP && !isP && (r >> 4) == b) {   // diagonal block: the front's position-pair sums
-                    const float* d = dgb + ((k & 1u) * 4 + b) * 512;
+                if (SP && !isP && (r >> 4) == b) {   // diagonal block: the position-pair sums
+                    const float* d = dgb + ((k & 1u) * 4 + b) * 256;
+                    const float* t3 = l3t + b * 64;
                     const int jr = r & 15;
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const int x = i < jr ? dg_index(jr, i, 0) : 0;
-                        v[i] = i < jr ? d[x] + d[256 + x] : 0.f;
+                        const bool l3 = dg_level3(jr, i);
+                        const int x = i < jr && !l3 ? dg_index(jr, i, 0) : 0;
+                        v[i] = i >= jr ? 0.f : l3 ? t3[(jr - 8) * 8 + i] : d[x] + d[128 + x];
                     }
                 }
                 if (isP) {
@@ -1070,13 +1129,15 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
             // sums, row r = bt % 64, columns 8 (bt / 64) .. + 7 of each block
             if (SP && bw < 4) {
                 const int r = bt & 63, hh = bt >> 6, ta = r >> 4, jr = r & 15;
-                const float* d = dgb + ((k & 1u) * 4 + ta) * 512;
+                const float* d = dgb + ((k & 1u) * 4 + ta) * 256;
+                const float* t3 = l3t + (4 + ta) * 64;
                 float v[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int js = 8 * hh + e;
-                    const int x = js <= jr ? dg_index(jr, js, 1) : 0;
-                    v[e] = js <= jr ? d[x] + d[256 + x] : 0.f;
+                    const bool l3 = dg_level3(jr, js);
+                    const int x = js <= jr && !l3 ? dg_index(jr, js, 1) : 0;
+                    v[e] = js > jr ? 0.f : l3 ? t3[(jr - 8) * 8 + js] : d[x] + d[128 + x];
                 }
                 *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 16 * ta + 8 * hh, C)) = pack8_f16(v);
                 for (int tb = ta + 1; tb < 4; ++tb)
