@@ -143,7 +143,8 @@ constexpr uint32_t S_TOT = S_NRM + 1024;           // float2 [4 sub-tiles][64 pa
 constexpr uint32_t S_BT = S_TOT + 2048;            // fp32 [NSLOT][64] beta
 constexpr uint32_t S_INFO = S_BT + NSLOT * 256;    // [NSLOT] Handoff: record address, the next item
 constexpr uint32_t S_BAR = S_INFO + NSLOT * 32;    // mbarriers, TMEM slot, flags
-constexpr uint32_t SMEM_BYTES = S_BAR + 128 + 1024;
+constexpr uint32_t S_DGX = S_BAR + 128;             // u8 [A, P][16 r][16 s]: unbounded gate's pair codes
+constexpr uint32_t SMEM_BYTES = S_DGX + 512 + 1024;
 static_assert(S_RAW + 3 * RAW_PLANE <= S_QD, "raw rows inside the left-row tiles");
 static_assert(S_KPT == S_TT + 8192, "the W product's junk A rows are the first 8 KiB of (k e^G)^T");
 static_assert(S_WUST + 32768 <= S_NRM, "W / U0^T staging inside the solve tiles");
@@ -315,6 +316,14 @@ __device__ __forceinline__ int dg_index(int jr, int js, int isP) {
     const int lvl = t == 2 ? 0 : t == 1 ? 64 : 96;
     return lvl + (b0 >> (t + 1)) * 2 * h * h + (jr - b0 - h) * 2 * h + isP * h + (js - b0);
 }
+// The back group reads the pair values through a table of one code per (A or P,
+// r, s), built once per CTA: the index above, DG_L3 for a level-3 pair, DG_ZERO
+// above the diagonal (and on it for A).
+constexpr uint32_t DG_L3 = 0xFE, DG_ZERO = 0xFF;
+__device__ __forceinline__ uint32_t dg_code(int isP, int jr, int js) {
+    if (isP ? js > jr : js >= jr) return DG_ZERO;
+    return dg_level3(jr, js) ? DG_L3 : (uint32_t)dg_index(jr, js, isP);
+}
 
 // Sum of v[i] over the warp's 32 lanes, lanes 2i and 2i + 1 keeping the sum
 // of v[i] (recursive halving: 16 shuffles for 16 values).
@@ -445,6 +454,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
+    if (SP) sb[S_DGX + tid] = (unsigned char)dg_code(tid >> 8, (tid >> 4) & 15, tid & 15);   // (PT = 512)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -1102,11 +1112,12 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                     const float* d = dgb + ((k & 1u) * 4 + b) * 256;
                     const float* t3 = l3t + b * 64;
                     const int jr = r & 15;
+                    const uint4 cw = *reinterpret_cast<const uint4*>(sb + S_DGX + 16 * jr);
+                    const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const bool l3 = dg_level3(jr, i);
-                        const int x = i < jr && !l3 ? dg_index(jr, i, 0) : 0;
-                        v[i] = i >= jr ? 0.f : l3 ? t3[(jr - 8) * 8 + i] : d[x] + d[128 + x];
+                        const uint32_t code = (cws[i >> 2] >> (8 * (i & 3))) & 0xFFu, x = code & 127u;
+                        v[i] = code == DG_ZERO ? 0.f : code == DG_L3 ? t3[(jr & 7) * 8 + i] : d[x] + d[128 + x];
                     }
                 }
                 if (isP) {
@@ -1131,13 +1142,12 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                 const int r = bt & 63, hh = bt >> 6, ta = r >> 4, jr = r & 15;
                 const float* d = dgb + ((k & 1u) * 4 + ta) * 256;
                 const float* t3 = l3t + (4 + ta) * 64;
+                const uint2 cw = *reinterpret_cast<const uint2*>(sb + S_DGX + 256 + 16 * jr + 8 * hh);
                 float v[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const int js = 8 * hh + e;
-                    const bool l3 = dg_level3(jr, js);
-                    const int x = js <= jr && !l3 ? dg_index(jr, js, 1) : 0;
-                    v[e] = js > jr ? 0.f : l3 ? t3[(jr - 8) * 8 + js] : d[x] + d[128 + x];
+                    const uint32_t code = ((e < 4 ? cw.x : cw.y) >> (8 * (e & 3))) & 0xFFu, x = code & 127u;
+                    v[e] = code == DG_ZERO ? 0.f : code == DG_L3 ? t3[(jr & 7) * 8 + 8 * hh + e] : d[x] + d[128 + x];
                 }
                 *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 16 * ta + 8 * hh, C)) = pack8_f16(v);
                 for (int tb = ta + 1; tb < 4; ++tb)
