@@ -147,12 +147,16 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
     auto issue_load = [&](int64_t c) {
         const int s = (int)(c & 1);
         ptx::mbar_expect_tx(bar_load0 + 8 * s, REC_BYTES);
-        // four copies in flight at once rather than one long one
+        // two copies: each copy carries a fixed cost, and the record lands sooner in
+        // two than in four, eight or sixteen (the single-pass recurrence of a
+        // 32768-token sequence: 0.889, 0.922, 0.962 and 1.066 ms at 96 heads; one
+        // copy is as fast as two)
         const unsigned char* src = recs + ((size_t)(c0 + c) * H + h) * REC_BYTES;
+        static_assert((REC_BYTES / 2) % 16 == 0, "bulk copies move multiples of 16 bytes");
 #pragma unroll
-        for (int part = 0; part < 4; ++part)
-            ptx::bulk_g2s(base + s * STAGE_STRIDE + part * (REC_BYTES / 4), src + part * (REC_BYTES / 4),
-                          REC_BYTES / 4, bar_load0 + 8 * s);
+        for (int part = 0; part < 2; ++part)
+            ptx::bulk_g2s(base + s * STAGE_STRIDE + part * (REC_BYTES / 2), src + part * (REC_BYTES / 2),
+                          REC_BYTES / 2, bar_load0 + 8 * s);
         pend[s] = 1;
         pend[2 + s] = (int)((c >> 1) & 1);
         if (c + 2 < nc)  // the record after next goes to L2 already
