@@ -380,12 +380,12 @@ static_assert(sizeof(Handoff) == 32, "hand-off slot");
 // chunk alone (rows 3-66; the rows before it come from the conv ring or are zero).
 // Rows past the end of the tensor read as zero; rows past the chunk are not used.
 __device__ __forceinline__ void issue_raw(const PrepArgs& a, int32_t t0, int32_t pos, int h, uint32_t base,
-                                          uint32_t bar) {
-    ptx::mbar_expect_tx(bar, pos > 0 ? 3u * RAW_PLANE : 3u * C * RAW_ROW);
+                                          const uint32_t (&bar)[3]) {
 #pragma unroll
-    for (int pl = 0; pl < 3; ++pl) {
-        if (pos > 0) ptx::tma_load_2d(base + S_RAW + pl * RAW_PLANE, &a.map67[pl], h * D, t0 - RING, bar);
-        else ptx::tma_load_2d(base + S_RAW + pl * RAW_PLANE + RING * RAW_ROW, &a.map64[pl], h * D, t0, bar);
+    for (int pl = 0; pl < 3; ++pl) {   // one mbarrier per plane: the conv of q starts while k and v land
+        ptx::mbar_expect_tx(bar[pl], pos > 0 ? RAW_PLANE : C * RAW_ROW);
+        if (pos > 0) ptx::tma_load_2d(base + S_RAW + pl * RAW_PLANE, &a.map67[pl], h * D, t0 - RING, bar[pl]);
+        else ptx::tma_load_2d(base + S_RAW + pl * RAW_PLANE + RING * RAW_ROW, &a.map64[pl], h * D, t0, bar[pl]);
     }
 }
 
@@ -428,13 +428,14 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
     float* btab = reinterpret_cast<float*>(sb + S_BT);
     volatile Handoff* info = reinterpret_cast<volatile Handoff*>(sb + S_INFO);
     const uint32_t bar_mma1 = base + S_BAR, bar_mma2 = base + S_BAR + 8, bar_info = base + S_BAR + 16,
-                   bar_drain = base + S_BAR + 24, bar_raw = base + S_BAR + 32;
+                   bar_drain = base + S_BAR + 24;
+    // the raw q, k, v rows of an item, one mbarrier per plane
+    const uint32_t bar_raw[3] = {base + S_BAR + 32, base + S_BAR + 72, base + S_BAR + 80};
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sb + S_BAR + 48);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sb + S_BAR + 52);
     volatile int* s_take = reinterpret_cast<volatile int*>(sb + S_BAR + 56);
-    // raw-row loads issued and consumed (for the drain after a timeout)
+    // raw-row loads issued (for the drain after a timeout)
     volatile int* raw_issued = reinterpret_cast<volatile int*>(sb + S_BAR + 64);
-    volatile int* raw_seen = reinterpret_cast<volatile int*>(sb + S_BAR + 68);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint64_t lim = a.wait_limit_ns ? a.wait_limit_ns : WAIT_LIMIT_NS;
@@ -448,9 +449,8 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
         ptx::mbar_init(bar_mma2, 1);
         ptx::mbar_init(bar_info, 1);
         ptx::mbar_init(bar_drain, 1);
-        ptx::mbar_init(bar_raw, 1);
+        for (int pl = 0; pl < 3; ++pl) ptx::mbar_init(bar_raw[pl], 1);
         *raw_issued = 0;
-        *raw_seen = 0;
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -566,13 +566,11 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
             }
             const bool full = tok0 + 16 <= len;
 
-            // this item's raw rows (one thread polls, the others wait in the barrier)
+            // this item's raw q rows (one thread polls, the others wait in the barrier;
+            // the k and v rows are waited for before their conv)
             {
                 bool late = false;
-                if (ft == 0) {
-                    late = !wait_or_abort(bar_raw, k_iter & 1u, lim, abort_flag);
-                    if (!late) *raw_seen = *raw_seen + 1;
-                }
+                if (ft == 0) late = !wait_or_abort(bar_raw[0], k_iter & 1u, lim, abort_flag);
                 if (ptx::bar_sync_or(BAR_FRONT, NF, late)) break;
             }
 
@@ -675,8 +673,12 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                 uint32_t x[XR];
                 raw_rows(0, x);
                 sqq = conv_plane(x, 0, aq, true);
+                // (every thread observes the plane's barrier itself; after a timeout it
+                // reads stale rows, and the next agreement on the abort flag ends the loop)
+                wait_or_abort(bar_raw[1], k_iter & 1u, lim, abort_flag);
                 raw_rows(1, x);
                 sqk = conv_plane(x, 1, ak, true);
+                wait_or_abort(bar_raw[2], k_iter & 1u, lim, abort_flag);
                 raw_rows(2, x);
                 conv_plane(x, 2, av, false);
             }
@@ -1340,8 +1342,10 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
     __syncthreads();
     if (tid == 0 && *abort_flag) {
         atomicExch(a.status, ERR_TIMEOUT);
-        // a raw-row load still in flight lands before the CTA leaves
-        if (*raw_issued > *raw_seen) ptx::mbar_wait(bar_raw, (uint32_t)*raw_seen & 1u, WAIT_LIMIT_NS);
+        // raw-row loads still in flight land before the CTA leaves (the phases of a
+        // barrier complete in order: the last issued one covers the earlier ones)
+        if (*raw_issued > 0)
+            for (int pl = 0; pl < 3; ++pl) ptx::mbar_wait(bar_raw[pl], (uint32_t)(*raw_issued - 1) & 1u, WAIT_LIMIT_NS);
     }
     if (warp == 0) {
         __syncwarp();   // (thread 0 may have waited above; the dealloc is warp-collective)
