@@ -1227,8 +1227,10 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
             }
 
             // ---- X = (I + A)^{-1}: diagonal 16 x 16 inverses by forward substitution
-            if (bt < 64) {
-                const int ta = bt >> 4, j = bt & 15;
+            // (warps 10-11: warps 8-9 read out diagonal P and warp 8 issues the batches,
+            // so this spreads the back's work over the four SM sub-partitions)
+            if (bt >= 64 && bt < 128) {
+                const int ta = (bt - 64) >> 4, j = bt & 15;
                 const int ob = 16 * ta;
                 float x[16];
 #pragma unroll
