@@ -91,6 +91,10 @@ constexpr int PT = 512;                    // 16 warps
 constexpr int NF = 256;                    // front threads (warps 0-7)
 constexpr int NB = 256;                    // back threads (warps 8-15)
 constexpr int BAR_FRONT = 1, BAR_BACK = 2; // named barrier ids
+// the back thread that issues the tcgen05 batches, TMA boxes and bulk stores (and
+// waits for them): lane 0 of warp 11, on the SM sub-partition (warp index mod 4)
+// that the rest of the back group loads least
+constexpr int ISSUER = 96;
 constexpr int REG_LAUNCH = 65536 / PT;     // registers per thread at launch (__launch_bounds__(PT, 1))
 // register split (front, back); the unbounded gate's position pairs need more in front
 template <bool SP> constexpr int REG_FRONT = SP ? 160 : 152;
@@ -1018,12 +1022,12 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
 #pragma unroll 1
         while (true) {
             // one thread polls the hand-off, the others wait in the barrier
-            bool bad = bt == 0 && !wait_or_abort(bar_info, k & 1u, lim, abort_flag);
+            bool bad = bt == ISSUER && !wait_or_abort(bar_info, k & 1u, lim, abort_flag);
             if (ptx::bar_sync_or(BAR_BACK, NB, bad)) break;
             unsigned char* rec = info[k % NSLOT].rec;   // the same value in every thread
             if (rec == nullptr) break;
             // ---- the first tcgen05 batch: A, off-diagonal P, diagonal P
-            if (bt == 0) {
+            if (bt == ISSUER) {
                 ptx::tc_fence_after();
                 constexpr uint32_t IDESC_BF16_N64 = ptx::idesc_bf16_f32(128, 64);
                 constexpr uint32_t IDESC_BF16_N128 = ptx::idesc_bf16_f32(128, 128);
@@ -1055,7 +1059,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                 ptx::mma_commit(bar_mma1);
             }
             const float* bta = btab + (k % NSLOT) * C;
-            if (bt == 0) {
+            if (bt == ISSUER) {
                 bad = !wait_or_abort(bar_mma1, k & 1u, lim, abort_flag);
                 // the operand tiles are free: the next item's raw rows go there
                 const volatile Handoff& hd = info[k % NSLOT];
@@ -1221,7 +1225,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
             ptx::tc_fence_before();
             bar_sync_n(BAR_BACK, NB);
             // P leaves
-            if (bt == 0) {
+            if (bt == ISSUER) {
                 ptx::bulk_s2g(rec + REC_P, base + S_TT, 8192);
                 ptx::bulk_commit();
             }
@@ -1256,7 +1260,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
             solve_level<1>(Am, Xm, bt);
             solve_level<2>(Am, Xm, bt);
             solve_level<3>(Am, Xm, bt);
-            if (bt == 0) ptx::bulk_wait_read_all();   // P has left its staging tile, where T goes
+            if (bt == ISSUER) ptx::bulk_wait_read_all();   // P has left its staging tile, where T goes
             bar_sync_n(BAR_BACK, NB);
 
             // ---- T = X Diag(beta) (fp16, blocks above the diagonal zero)
@@ -1274,7 +1278,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
             ptx::fence_async_smem();
             ptx::tc_fence_before();
             bar_sync_n(BAR_BACK, NB);
-            if (bt == 0) {
+            if (bt == ISSUER) {
                 ptx::tc_fence_after();
                 constexpr uint32_t IDESC_W = ptx::idesc_f16_f32(128, 128);
                 constexpr uint32_t IDESC_U = ptx::idesc_f16_f32(128, 64);
@@ -1286,7 +1290,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                 }
                 ptx::mma_commit(bar_mma2);
             }
-            if (bt == 0) bad = !wait_or_abort(bar_mma2, k & 1u, lim, abort_flag);
+            if (bt == ISSUER) bad = !wait_or_abort(bar_mma2, k & 1u, lim, abort_flag);
             ptx::tc_fence_before();
             if (ptx::bar_sync_or(BAR_BACK, NB, bad)) break;
             ptx::tc_fence_after();
@@ -1323,7 +1327,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
             }
             ptx::fence_async_smem();
             bar_sync_n(BAR_BACK, NB);
-            if (bt == 0) {
+            if (bt == ISSUER) {
                 ptx::bulk_s2g(rec + REC_W, base + S_WUST, 8192);                   // W keys 0-63
                 ptx::bulk_s2g(rec + REC_W + REC_PANEL, base + S_WUST + 8192, 8192);  // W keys 64-127
                 ptx::bulk_s2g(rec + REC_UT, base + S_WUST + 16384, 16384);
@@ -1335,7 +1339,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
 
     // ---- drain: the MMA issuer lets its MMAs finish (a commit covers every earlier
     // one of that thread), and its bulk stores land, before TMEM is freed
-    if (tid == NF) {
+    if (tid == NF + ISSUER) {
         ptx::mma_commit(bar_drain);
         ptx::mbar_wait(bar_drain, 0, WAIT_LIMIT_NS);
         ptx::bulk_wait_all();
