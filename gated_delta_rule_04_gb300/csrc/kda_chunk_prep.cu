@@ -50,7 +50,8 @@
 //     batch (A, off-diagonal P, split diagonal P) of item j;
 //   back (warps 8-15): for item j - 1, the readout of A and P from tensor
 //     memory, the solve, T, the W / U0^T products, their readout and the
-//     record stores of P, W and U0^T.
+//     record stores of P, W and U0^T.  One thread of warp 11 issues the
+//     tcgen05 batches, TMA boxes and bulk stores.
 // So the element-wise work of one item overlaps the short, dependent solve of
 // the one before.  The raw q/k/v rows of an item (with the three rows before
 // the chunk) arrive by TMA into the operand region, issued by the back once
@@ -67,7 +68,8 @@
 // Hand-offs (all mbarriers, one phase per item, in item order):
 //   mma1   the first batch of item j finished: the back may read A and P, and
 //          the next item's raw rows may land in the operand region;
-//   raw    the raw rows of item j have landed: the front may start on it;
+//   raw    one per plane: the raw q (k, v) rows of item j have landed: the
+//          front may start on it (on the conv of k, of v);
 //   info   item j's record address and beta are published to the back (a
 //          null address ends the back's loop);
 //   mma2   the W / U0^T products of item j finished: the front may overwrite
