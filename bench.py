@@ -201,7 +201,7 @@ def scan_bytes_per_token_head():
     return 3 * D * 4 + 4 * D + 4 + 4 * D
 
 
-REC_BYTES = 74240  # one chunk-head record of operand tiles (kda_chunk_layout.cuh)
+REC_BYTES = 70656  # one chunk-head record of operand tiles (kda_chunk_layout.cuh)
 
 # The method's own per-token-head figures for prefill at bf16 I/O, independent of
 # how the work is split into kernels:

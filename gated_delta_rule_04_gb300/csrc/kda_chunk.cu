@@ -52,7 +52,8 @@ constexpr uint32_t TMEM_COLS = 512;        // [0,128) S^T, [128,384) D[0], D[1] 
 constexpr int NBUF = 2;                    // D buffers: the chain may run a chunk ahead of the output
 constexpr uint32_t TM_SH = 384;            // S^T as fp16 pairs: lane = value, column = 2 keys
 constexpr uint32_t TM_UH = 448;            // U^T as fp16 pairs: lane = value, column = 2 tokens
-constexpr uint32_t STAGE_STRIDE = 75776;   // REC_BYTES rounded up to 1 KiB
+constexpr uint32_t REC_PT = (REC_BYTES + 1023) / 1024 * 1024;   // a stage's expanded P tile (8 KiB)
+constexpr uint32_t STAGE_STRIDE = REC_PT + 8192;
 constexpr int LDYS = 132;                          // padded row stride of the output tile
 constexpr uint32_t OFF_Y = 2 * STAGE_STRIDE;       // fp32 [64 tok][132] output of a chunk
 constexpr uint32_t OFF_BAR = OFF_Y + CHUNK_T * LDYS * 4; // mbarriers + TMEM slot + flags
@@ -240,7 +241,19 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
                     issue_load(c + 1);
                 }
             }
-            // while it runs: S^T *= decay (per key column), back into TMEM before MMA2
+            // while it runs: P's lower triangle (in the record) into the stage's swizzled
+            // P tile, zero above the diagonal (MMA3 reads it after the U stage's barrier;
+            // the tile was last read by MMA3 of chunk c - 2, which finished before this
+            // record was loaded), then S^T *= decay (per key column), back into TMEM
+            // before MMA2
+#pragma unroll
+            for (int i = tid; i < 512; i += NSTATE) {
+                const int r = i >> 3, pos = i & 7, cq = pos ^ (r & 7);
+                const uint4 v = cq <= (r >> 3) ? *reinterpret_cast<const uint4*>(sp + REC_P + 16 * p_chunk(r, cq))
+                                               : make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(sb + s * STAGE_STRIDE + REC_PT + 128 * r + 16 * pos) = v;
+            }
+            ptx::fence_async_smem();
             {
                 const float* decay = reinterpret_cast<const float*>(sp + REC_DECAY);
 #pragma unroll
@@ -296,7 +309,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
                 ptx::mma_commit(bar_state);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)     // MMA3: O^T += U^T P^T, finishing under the next S copy
-                    ptx::mma_f16_ta(tmem + dcol + 64, tmem + TM_UH + 8 * kk, ptx::sdesc_sw128(stg + REC_P + kk * 32),
+                    ptx::mma_f16_ta(tmem + dcol + 64, tmem + TM_UH + 8 * kk, ptx::sdesc_sw128(stg + REC_PT + kk * 32),
                                     IDESC_N64, 1);
                 ptx::mma_commit(bar_mma23_0 + 8 * buf);
             }

@@ -27,9 +27,19 @@ constexpr int REC_Q = 8192;       // Q+    [64 tok rows][128 key]  2 panels, str
 constexpr int REC_PANEL = 16384;  // panel stride of W and Q+
 constexpr int REC_KT = 32768;     // Kt^T  [128 key rows][64 tok]  1 panel x 128 rows
 constexpr int REC_UT = 49152;     // U0^T  [128 val rows][64 tok]  1 panel x 128 rows
-constexpr int REC_P = 65536;      // P     [64 r rows][64 s]       1 panel x 64 rows
-constexpr int REC_DECAY = 73728;  // decay [128] fp32 = e^{G_last}
-constexpr int REC_BYTES = 74240;
+constexpr int REC_P = 65536;      // P     lower triangle [64 r rows][64 s]: see p_chunk
+constexpr int REC_P_BYTES = 288 * 16;
+constexpr int REC_DECAY = REC_P + REC_P_BYTES;  // decay [128] fp32 = e^{G_last}
+constexpr int REC_BYTES = REC_DECAY + 512;
+
+// P (s <= r) is stored as its lower triangle of 16-byte chunks: row r holds the
+// 8-column chunks c <= r / 8 (every element past them is zero), rows in order,
+// 288 chunks in all; p_chunk is the index of chunk c of row r.  The recurrence
+// expands it into a swizzled tile in shared memory.
+__host__ __device__ constexpr int p_chunk(int r, int c) {
+    return 4 * (r >> 3) * ((r >> 3) + 1) + (r & 7) * ((r >> 3) + 1) + c;
+}
+static_assert(p_chunk(63, 7) == 287 && p_chunk(8, 0) == 8 && p_chunk(16, 0) == 24, "P chunk numbering");
 
 // Byte offset of 16-bit element (row, k) in a K-major tile with the 128-byte
 // swizzle: 64 elements of K per 128-byte row, panels of `rows` rows for each

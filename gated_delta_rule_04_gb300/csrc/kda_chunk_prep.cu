@@ -1128,8 +1128,9 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                     }
                 }
                 if (isP) {
-                    *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 16 * b, C)) = pack8_f16(v);
-                    *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 16 * b + 8, C)) = pack8_f16(v + 8);
+                    // (an off-diagonal block: both chunks lie in the lower triangle)
+                    *reinterpret_cast<uint4*>(sb + S_TT + 16 * p_chunk(r, 2 * b)) = pack8_f16(v);
+                    *reinterpret_cast<uint4*>(sb + S_TT + 16 * p_chunk(r, 2 * b + 1)) = pack8_f16(v + 8);
                 } else {  // beta_r A, strictly lower part (zeros above in the diagonal block)
                     const float be = bta[r];
 #pragma unroll
@@ -1156,9 +1157,8 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
                     const uint32_t code = ((e < 4 ? cw.x : cw.y) >> (8 * (e & 3))) & 0xFFu, x = code & 127u;
                     v[e] = code == DG_ZERO ? 0.f : code == DG_L3 ? t3[(jr & 7) * 8 + 8 * hh + e] : d[x] + d[128 + x];
                 }
-                *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 16 * ta + 8 * hh, C)) = pack8_f16(v);
-                for (int tb = ta + 1; tb < 4; ++tb)
-                    *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 16 * tb + 8 * hh, C)) = make_uint4(0, 0, 0, 0);
+                if (2 * ta + hh <= (r >> 3))   // (the chunk above the diagonal is zero, and not stored)
+                    *reinterpret_cast<uint4*>(sb + S_TT + 16 * p_chunk(r, 2 * ta + hh)) = pack8_f16(v);
             }
             // ---- diagonal P blocks (warps 8-11): D2 rows are [q hi; q lo], columns
             // [R hi | R lo].  Warps 10-11 hand the lo*hi terms (lanes 64-127) to warps
@@ -1214,12 +1214,9 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj)
                         if (16 * ta + jj > r) v[jj] = 0.f;
-                    *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 16 * ta, C)) = pack8_f16(v);
-                    *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 16 * ta + 8, C)) = pack8_f16(v + 8);
-                    for (int tb = ta + 1; tb < 4; ++tb) {
-                        *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 16 * tb, C)) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4*>(sb + S_TT + sw128_off(r, 16 * tb + 8, C)) = make_uint4(0, 0, 0, 0);
-                    }
+                    *reinterpret_cast<uint4*>(sb + S_TT + 16 * p_chunk(r, 2 * ta)) = pack8_f16(v);
+                    if (2 * ta + 1 <= (r >> 3))   // (otherwise above the diagonal: zero, not stored)
+                        *reinterpret_cast<uint4*>(sb + S_TT + 16 * p_chunk(r, 2 * ta + 1)) = pack8_f16(v + 8);
                 }
             }
             ptx::fence_async_smem();
@@ -1227,7 +1224,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prep_kernel(const __grid_constant
             bar_sync_n(BAR_BACK, NB);
             // P leaves
             if (bt == ISSUER) {
-                ptx::bulk_s2g(rec + REC_P, base + S_TT, 8192);
+                ptx::bulk_s2g(rec + REC_P, base + S_TT, REC_P_BYTES);
                 ptx::bulk_commit();
             }
 
