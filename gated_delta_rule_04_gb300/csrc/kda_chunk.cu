@@ -35,7 +35,9 @@
 // token row is normalised by the 8 threads holding it and the gate logits
 // are read and the output written as 64-byte row segments per 8 threads.  Each
 // chunk's record arrives with bulk copies into a two-stage ring, issued by a
-// chain thread as soon as the chunk before has finished its last MMA.  Every
+// chain thread as soon as the chunk before has finished its last MMA; P comes
+// as its lower triangle, which the chain warps expand into a swizzled tile
+// while the chunk's first MMA batch runs.  Every
 // wait is bounded; on timeout the kernel records the timeout in the
 // workspace status word, drains its own copies and MMAs and returns after
 // freeing its tensor memory.
