@@ -183,6 +183,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
                        : S_in ? S_in[soff + (size_t)(32 * j + x) * D + vrow] : 0.f;
             ptx::tmem_st32(tlane + 32 * j, v);
         }
+        ptx::tmem_wait_st();   // (the first copy below reads these columns back)
+        // both stages' P tiles start zero: the expansion below writes only the lower
+        // triangle, and the record copies never reach the tiles
+        for (int i = tid; i < 2 * 512; i += NSTATE)
+            *reinterpret_cast<uint4*>(sb + (i >> 9) * STAGE_STRIDE + REC_PT + 16 * (i & 511)) = make_uint4(0, 0, 0, 0);
 #pragma unroll 1
         for (int64_t c = 0; c < nc; ++c) {
             const int s = (int)(c & 1);
@@ -244,16 +249,16 @@ __global__ void __launch_bounds__(NT, 1) chunk_recurrence_kernel(ChunkRecArgs a)
                 }
             }
             // while it runs: P's lower triangle (in the record) into the stage's swizzled
-            // P tile, zero above the diagonal (MMA3 reads it after the U stage's barrier;
-            // the tile was last read by MMA3 of chunk c - 2, which finished before this
-            // record was loaded), then S^T *= decay (per key column), back into TMEM
-            // before MMA2
+            // P tile, whose chunks above the diagonal stay zero from the kernel's start
+            // (MMA3 reads it after the U stage's barrier; the tile was last read by MMA3
+            // of chunk c - 2, which finished before this record was loaded), then
+            // S^T *= decay (per key column), back into TMEM before MMA2
 #pragma unroll
             for (int i = tid; i < 512; i += NSTATE) {
                 const int r = i >> 3, pos = i & 7, cq = pos ^ (r & 7);
-                const uint4 v = cq <= (r >> 3) ? *reinterpret_cast<const uint4*>(sp + REC_P + 16 * p_chunk(r, cq))
-                                               : make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(sb + s * STAGE_STRIDE + REC_PT + 128 * r + 16 * pos) = v;
+                if (cq <= (r >> 3))
+                    *reinterpret_cast<uint4*>(sb + s * STAGE_STRIDE + REC_PT + 128 * r + 16 * pos) =
+                        *reinterpret_cast<const uint4*>(sp + REC_P + 16 * p_chunk(r, cq));
             }
             ptx::fence_async_smem();
             {
