@@ -310,7 +310,8 @@ def test_workspace_covers_overlapped_windows(L, T, H):
     long as the others (d = 6 above 64 heads, 4 above 32, 2 up to 32); the
     workspace query covers two windows' records (window sizes round up to whole
     64-token chunks)."""
-    rec = 70656
+    import bench
+    rec = bench.REC_BYTES   # equal to the layout header's (tests/test_record_layout.py)
     p = params(num_heads=H)
     need = L.kda_prefill_workspace_bytes(ctypes.byref(p), 1, T)
     windows = min(3 if H > 48 else 4, T // (1024 if H <= 64 else 8192))

@@ -2,7 +2,8 @@
 disjoint and in range, and p_chunk numbers the 16-byte chunks of P's lower
 triangle (row r, 8-column chunk c <= r / 8) one to one onto 0 .. 287, rows in
 order.  A small host program includes the layout header and prints what it
-computes; nvcc compiles it (host code only)."""
+computes; nvcc compiles it (host code only).  The bench's byte accounting
+carries its own copy of the record size, checked against the header here."""
 import os
 import shutil
 import subprocess
@@ -65,3 +66,9 @@ def test_p_chunk_numbers_the_lower_triangle_in_row_order(layout):
     # the chunks past r / 8 are the ones every element of which lies above the diagonal
     for r, c, _ in chunks:
         assert 8 * c <= r
+
+
+def test_bench_record_size_matches_the_header(layout):
+    (*_, total), _ = layout
+    import bench
+    assert bench.REC_BYTES == total, "bench.py's record size differs from the layout header's REC_BYTES"
